@@ -1,0 +1,211 @@
+/*
+ * CPU oracle for the load-balanced CSR SpMV library (see oracle.h).
+ *
+ * TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg; never by the product library.
+ *
+ * Everything is a direct restatement of a definition on the pages, in the
+ * plainest loop that states it.  Sums are carried in long double.
+ * Build with -ffp-contract=off so the compiler does not fuse operations.
+ */
+#include "oracle.h"
+
+#include <stddef.h>
+
+static int check_row_ptr_basic(int32_t m, const int32_t *row_ptr) {
+    return m >= 0 && row_ptr != NULL;
+}
+
+/* [LBPM] section 4.3 / [RgCSR] section 3: y_i = alpha * sum_k a_ik x_k + beta * y_i */
+int oracle_spmv_f64(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx,
+                    const double *vals, const double *x, double alpha, double beta,
+                    const double *y_old, const int32_t *rows, int64_t nrows, double *y_out,
+                    double *mag_out) {
+    if (!check_row_ptr_basic(m, row_ptr) || n < 0 || y_out == NULL) return 1;
+    if (beta != 0.0 && y_old == NULL) return 1;
+    const long double a = (long double)(double)alpha;
+    const long double b = (long double)(double)beta;
+    int64_t count = rows ? nrows : m;
+    for (int64_t t = 0; t < count; ++t) {
+        int32_t i = rows ? rows[t] : (int32_t)t;
+        if (i < 0 || i >= m) return 1;
+        long double acc = 0.0L, mag = 0.0L;
+        for (int32_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) {
+            long double prod = (long double)vals[k] * (long double)x[col_idx[k]];
+            acc += prod;
+            mag += prod < 0 ? -prod : prod;
+        }
+        long double y = a * acc;
+        long double by = 0.0L;
+        if (beta != 0.0) {
+            by = b * (long double)y_old[i];
+            y += by;
+        }
+        y_out[t] = (double)y;
+        if (mag_out) {
+            long double aa = a < 0 ? -a : a;
+            mag_out[t] = (double)(aa * mag + (by < 0 ? -by : by));
+        }
+    }
+    return 0;
+}
+
+int oracle_spmv_f32(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx,
+                    const float *vals, const float *x, double alpha, double beta,
+                    const float *y_old, const int32_t *rows, int64_t nrows, float *y_out,
+                    double *mag_out) {
+    if (!check_row_ptr_basic(m, row_ptr) || n < 0 || y_out == NULL) return 1;
+    if (beta != 0.0 && y_old == NULL) return 1;
+    const long double a = (long double)(float)alpha;
+    const long double b = (long double)(float)beta;
+    int64_t count = rows ? nrows : m;
+    for (int64_t t = 0; t < count; ++t) {
+        int32_t i = rows ? rows[t] : (int32_t)t;
+        if (i < 0 || i >= m) return 1;
+        long double acc = 0.0L, mag = 0.0L;
+        for (int32_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) {
+            long double prod = (long double)vals[k] * (long double)x[col_idx[k]];
+            acc += prod;
+            mag += prod < 0 ? -prod : prod;
+        }
+        long double y = a * acc;
+        long double by = 0.0L;
+        if (beta != 0.0) {
+            by = b * (long double)y_old[i];
+            y += by;
+        }
+        y_out[t] = (float)y;
+        if (mag_out) {
+            long double aa = a < 0 ? -a : a;
+            mag_out[t] = (double)(aa * mag + (by < 0 ? -by : by));
+        }
+    }
+    return 0;
+}
+
+/*
+ * [LBPM] section 5.2.1.  The row end r is the unit at merge position
+ * row_ptr[r+1] + r (all of row r's nonzeros and the r earlier row ends come
+ * before it).  So after d units, the row ends taken are those with
+ * row_ptr[r+1] + r < d.  The diagonals d_p rise with p and so does
+ * row_ptr[r+1] + r with r, so one forward sweep over the rows counts them
+ * for every p in turn.
+ */
+int oracle_merge_path_partition(int32_t m, int32_t nnz, const int32_t *row_ptr, int64_t T,
+                                int64_t P, int32_t *part) {
+    if (!check_row_ptr_basic(m, row_ptr) || nnz < 0 || T <= 0 || P < 1 || part == NULL) return 1;
+    const int64_t total = (int64_t)m + (int64_t)nnz;
+    int64_t i = 0;
+    for (int64_t p = 0; p <= P; ++p) {
+        int64_t d = p * T < total ? p * T : total;
+        while (i < m && (int64_t)row_ptr[i + 1] + i < d) ++i;
+        part[2 * p] = (int32_t)i;
+        part[2 * p + 1] = (int32_t)(d - i);
+    }
+    return 0;
+}
+
+static int length_class(int32_t len) {
+    int k = 0;
+    while (k < 31 && (len >> k) != 0) ++k;
+    return k; /* 0 for len == 0, else 1 + floor(log2(len)) */
+}
+
+int oracle_row_stats(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
+                     const int32_t *col_idx, oracle_stats_t *out) {
+    if (!check_row_ptr_basic(m, row_ptr) || out == NULL || nnz < 0 || n < 0) return 1;
+    for (int b = 0; b < 32; ++b) out->hist[b] = 0;
+    for (int g = 0; g < 4; ++g) out->rg_slots[g] = 0;
+    out->sum_len = 0;
+    out->min_len = 0;
+    out->max_len = 0;
+    out->n_empty = 0;
+    out->flags = 0;
+
+    if (row_ptr[0] != 0) out->flags |= 1;
+    for (int32_t i = 0; i < m; ++i)
+        if (row_ptr[i + 1] < row_ptr[i]) out->flags |= 2;
+    if (row_ptr[m] != nnz) out->flags |= 4;
+    if (out->flags) return 0;
+
+    for (int32_t k = 0; k < nnz; ++k)
+        if (col_idx[k] < 0 || col_idx[k] >= n) out->flags |= 8;
+
+    for (int32_t i = 0; i < m; ++i) {
+        int32_t len = row_ptr[i + 1] - row_ptr[i];
+        out->hist[length_class(len)] += 1;
+        out->sum_len += len;
+        if (i == 0 || len < out->min_len) out->min_len = len;
+        if (i == 0 || len > out->max_len) out->max_len = len;
+        if (len == 0) out->n_empty += 1;
+    }
+    for (int g = 0; g < 4; ++g) {
+        int32_t G = 32 << g;
+        for (int32_t start = 0; start < m; start += G) {
+            int32_t longest = 0;
+            for (int32_t i = start; i < start + G && i < m; ++i) {
+                int32_t len = row_ptr[i + 1] - row_ptr[i];
+                if (len > longest) longest = len;
+            }
+            out->rg_slots[g] += (int64_t)G * longest;
+        }
+    }
+    return 0;
+}
+
+/* [RgCSR] section 3, Figure 5 */
+int oracle_rgcsr_layout(int32_t m, const int32_t *row_ptr, int32_t G, int64_t *group_ptr,
+                        int32_t *row_len) {
+    if (!check_row_ptr_basic(m, row_ptr) || G <= 0 || group_ptr == NULL) return 1;
+    int32_t ngroups = (m + G - 1) / G;
+    group_ptr[0] = 0;
+    for (int32_t g = 0; g < ngroups; ++g) {
+        int32_t longest = 0;
+        for (int32_t i = g * G; i < (g + 1) * G && i < m; ++i) {
+            int32_t len = row_ptr[i + 1] - row_ptr[i];
+            if (len > longest) longest = len;
+        }
+        group_ptr[g + 1] = group_ptr[g] + (int64_t)G * longest;
+    }
+    if (row_len)
+        for (int32_t i = 0; i < m; ++i) row_len[i] = row_ptr[i + 1] - row_ptr[i];
+    return 0;
+}
+
+int oracle_rgcsr_pack_f64(int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
+                          const double *vals, int32_t G, const int64_t *group_ptr,
+                          int32_t *rg_col, double *rg_val) {
+    if (!check_row_ptr_basic(m, row_ptr) || G <= 0 || !group_ptr || !rg_col || !rg_val) return 1;
+    int32_t ngroups = (m + G - 1) / G;
+    for (int64_t s = 0; s < group_ptr[ngroups]; ++s) {
+        rg_col[s] = 0;
+        rg_val[s] = 0.0;
+    }
+    for (int32_t i = 0; i < m; ++i) {
+        int64_t base = group_ptr[i / G] + (i % G);
+        for (int32_t k = 0; k < row_ptr[i + 1] - row_ptr[i]; ++k) {
+            rg_col[base + (int64_t)k * G] = col_idx[row_ptr[i] + k];
+            rg_val[base + (int64_t)k * G] = vals[row_ptr[i] + k];
+        }
+    }
+    return 0;
+}
+
+int oracle_rgcsr_pack_f32(int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
+                          const float *vals, int32_t G, const int64_t *group_ptr,
+                          int32_t *rg_col, float *rg_val) {
+    if (!check_row_ptr_basic(m, row_ptr) || G <= 0 || !group_ptr || !rg_col || !rg_val) return 1;
+    int32_t ngroups = (m + G - 1) / G;
+    for (int64_t s = 0; s < group_ptr[ngroups]; ++s) {
+        rg_col[s] = 0;
+        rg_val[s] = 0.0f;
+    }
+    for (int32_t i = 0; i < m; ++i) {
+        int64_t base = group_ptr[i / G] + (i % G);
+        for (int32_t k = 0; k < row_ptr[i + 1] - row_ptr[i]; ++k) {
+            rg_col[base + (int64_t)k * G] = col_idx[row_ptr[i] + k];
+            rg_val[base + (int64_t)k * G] = vals[row_ptr[i] + k];
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,111 @@
+/*
+ * CPU oracle for the load-balanced CSR SpMV library.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Plain, single-threaded, obviously-correct C that
+ * the tests, the smoke check and the benchmark's CPU-baseline leg use to
+ * judge the CUDA path.  The product library never includes, links or calls
+ * anything here, and nothing here includes or calls the product library.
+ *
+ * Sources (web pages on load-balanced CSR SpMV):
+ *   [RgCSR]  "New Row-grouped CSR format for storing the sparse matrices on
+ *            GPU with implementation in CUDA" (arXiv 1012.2270): CSR
+ *            definition (section 3, Figure 1), Row-grouped CSR layout
+ *            (section 3, Figure 5), bytes-per-nonzero peak model (section 3).
+ *   [LBPM]   Osama, Porumbescu, Owens, "A GPU load-balancing programming
+ *            model" (PPoPP'23): CSR as atoms/tiles (section 4.1, Listing 1),
+ *            SpMV as a row loop (section 4.3, Listing 3), merge-path
+ *            schedule (section 5.2.1).
+ *   [OpSparse] "OpSparse: a highly optimized framework for sparse general
+ *            matrix multiplication on GPUs" (arXiv 2206.07244): row binning
+ *            by length class (section 5.1, Algorithms 1-3).
+ */
+#ifndef SPMV_ORACLE_H
+#define SPMV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * y = alpha*A*x + beta*y_old, accumulated in long double.  [LBPM] section
+ * 4.3 (Listing 3: for every row, sum values[nz]*x[indices[nz]] over the row's
+ * nonzeros, then store the sum); [RgCSR] section 3 (CSR definition).
+ * alpha and beta are first rounded to the value type (they reach the library
+ * as double).  If beta == 0, y_old is not read.  If rows != NULL only the
+ * listed rows are computed and y_out[t], mag_out[t] refer to rows[t];
+ * otherwise all m rows.  mag_out (may be NULL) receives
+ *   |alpha| * sum_k |val[k] * x[col[k]]| + |beta * y_old[i]|,
+ * the scale of the accuracy tolerance.  Returns 0, or 1 on bad arguments.
+ */
+int oracle_spmv_f64(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx,
+                    const double *vals, const double *x, double alpha, double beta,
+                    const double *y_old, const int32_t *rows, int64_t nrows, double *y_out,
+                    double *mag_out);
+int oracle_spmv_f32(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx,
+                    const float *vals, const float *x, double alpha, double beta,
+                    const float *y_old, const int32_t *rows, int64_t nrows, float *y_out,
+                    double *mag_out);
+
+/*
+ * Merge-path partition.  [LBPM] section 5.2.1: every nonzero and every row
+ * end is one unit of work; the m + nnz units are split evenly; a worker's
+ * start is the (row, nonzero) pair where its share begins.  Units are taken
+ * in merge order: in state (i, j) the next unit is the end of row i when
+ * row_ptr[i+1] <= j, otherwise nonzero j.  After d units the state is
+ *   i(d) = #{ r in [0, m) : row_ptr[r+1] + r < d },  j(d) = d - i(d).
+ * For p = 0..P the split of diagonal d_p = min(p*T, m+nnz) is written to
+ * part[2p] = i(d_p), part[2p+1] = j(d_p).  Returns 0, or 1 on bad arguments.
+ */
+int oracle_merge_path_partition(int32_t m, int32_t nnz, const int32_t *row_ptr, int64_t T,
+                                int64_t P, int32_t *part);
+
+/*
+ * Row-length statistics.  Length classes after [OpSparse] section 5.1
+ * (rows binned by size): class 0 holds empty rows, class k >= 1 holds lengths
+ * in [2^(k-1), 2^k).  rg_slots[g] is the storage a Row-grouped CSR layout
+ * with group size 32 << g needs ([RgCSR] section 3: each group of G rows is
+ * padded to its longest row): sum over groups of G * max length, the last
+ * partial group padded with empty rows.
+ * Flags: bit0 row_ptr[0] != 0, bit1 row_ptr decreases somewhere,
+ * bit2 row_ptr[m] != nnz, bit3 a column index outside [0, n).
+ * Statistics are computed only if no row_ptr flag (bits 0-2) is set.
+ */
+typedef struct {
+    int64_t hist[32];
+    int64_t sum_len;
+    int64_t rg_slots[4];
+    int32_t min_len;
+    int32_t max_len;
+    int32_t n_empty;
+    int32_t flags;
+} oracle_stats_t;
+
+int oracle_row_stats(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
+                     const int32_t *col_idx, oracle_stats_t *out);
+
+/*
+ * Row-grouped CSR layout, [RgCSR] section 3 and Figure 5: rows are taken in
+ * groups of G; within a group the k-th nonzeros of all rows are stored
+ * together, padded to the group's longest row.  group_ptr[g] (ngroups + 1
+ * entries, ngroups = ceil(m / G)) is the offset of group g; element k of row
+ * i lives at group_ptr[i / G] + k*G + (i mod G).  Padding slots get column 0
+ * and value 0.  row_len[i] = row_ptr[i+1] - row_ptr[i].
+ * oracle_rgcsr_layout fills group_ptr and row_len; the pack functions also
+ * fill the interleaved column and value arrays (group_ptr[ngroups] slots).
+ */
+int oracle_rgcsr_layout(int32_t m, const int32_t *row_ptr, int32_t G, int64_t *group_ptr,
+                        int32_t *row_len);
+int oracle_rgcsr_pack_f64(int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
+                          const double *vals, int32_t G, const int64_t *group_ptr,
+                          int32_t *rg_col, double *rg_val);
+int oracle_rgcsr_pack_f32(int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
+                          const float *vals, int32_t G, const int64_t *group_ptr,
+                          int32_t *rg_col, float *rg_val);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
