@@ -1,0 +1,425 @@
+"""Benchmark: CSR SpMV y = alpha*A*x + beta*y on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--all] [--impl reference]
+
+One step is one product through the C ABI with every input resident in HBM
+(plan built beforehand, its time reported as plan_ms).  W untimed steps,
+then exactly K timed steps between a barrier and a device synchronisation,
+each bracketed by CUDA events on the launching stream.  Prints one JSON line
+(rank 0).  The default workload is the 3-D 27-point stencil on a 128^3 grid
+(fp32, 55.7M nonzeros, 479.5 MB of compulsory traffic -- larger than L2, so
+no flush between steps; x stays L2-resident as in an iterative solver).
+
+--gpus N > 1 (under torchrun): N independent replicas, one per GPU, each on
+the full workload; the product has no exchange step on one matrix per GPU
+(weak scaling, value = all ranks' flops / max time over ranks).
+
+--impl reference: the CPU oracle (single-threaded, long double) timed on a
+bounded sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import platform
+import shutil
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "SpMV GFLOP/s and achieved HBM GB/s (% of roofline) per matrix, 1 GB300"
+DEFAULT_WORKLOAD = "stencil27_128"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def compulsory_bytes(A) -> int:
+    """nnz*(4+s) + (m+1)*4 + n*s + 2*m*s: every index and value once, x once,
+    y read and written once (the bytes-per-nonzero model of the Row-grouped
+    CSR page, section 3, extended by row_ptr, x and y)."""
+    s = A.vals.dtype.itemsize
+    return A.nnz * (4 + s) + (A.m + 1) * 4 + A.n * s + 2 * A.m * s
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "load_balanced_csr_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None, None
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None, None
+    return e.get("dram_bytes_per_launch"), e.get("note")
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.err = None
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            self.err = "nvidia-smi not found"
+            return
+        sel = self._select(device_index)
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                      "-lms", "50", "-i", sel], stdout=self.fh, stderr=subprocess.DEVNULL)
+
+    @staticmethod
+    def _select(device_index: int) -> str:
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            return vis.split(",")[device_index] if vis else str(device_index)
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"unavailable": self.err}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.03 <= r[0] <= t1 + 0.03]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "sampler run (timed region shorter than one sample)"
+        if not inside:
+            return {"unavailable": "no samples"}
+        reasons = sorted({self.NAMES[i] for r in inside for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def run_gpu(args, workload_name: str) -> dict | None:
+    import torch
+    import torch.distributed as dist
+
+    import load_balanced_csr_gb300 as lb
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    W = synth.workload(workload_name)
+    A = W.A
+    vt = torch.float64 if A.dtype == "f64" else torch.float32
+    rp = torch.from_numpy(A.row_ptr).to(dev)
+    col = torch.from_numpy(A.col_idx).to(dev)
+    val = torch.from_numpy(A.vals).to(dev)
+    x = torch.from_numpy(W.x).to(dev)
+    y0 = torch.from_numpy(W.y0).to(dev) if W.y0 is not None else None
+    y = y0.clone() if y0 is not None else torch.zeros(A.m, dtype=vt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    plan = lb.Plan(rp, col, val, A.n, kernel=args.kernel, items_per_thread=args.ipt)
+    torch.cuda.synchronize(dev)
+    plan_ms = (time.perf_counter() - t) * 1e3
+    info = plan.info()
+
+    for _ in range(args.warmup):
+        plan(x, y, W.alpha, W.beta, stream)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.15 if sampler else 0)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start_all = torch.cuda.Event(enable_timing=True)
+    end_all = torch.cuda.Event(enable_timing=True)
+    start_all.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        plan(x, y, W.alpha, W.beta, stream)
+        ev[k][1].record(stream)
+    end_all.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+
+    total_ms = start_all.elapsed_time(end_all)
+    per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3  # us
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # end to end through the public API: pinned host x in, host y out, every step
+    e2e = None
+    if True:
+        x_h = torch.from_numpy(W.x).pin_memory()
+        y_h = torch.empty(A.m, dtype=vt).pin_memory()
+        y0_h = torch.from_numpy(W.y0).pin_memory() if W.y0 is not None else None
+        ke = max(3, min(K, args.e2e_steps))
+        for _ in range(2):
+            x.copy_(x_h, non_blocking=True)
+            plan(x, y, W.alpha, W.beta, stream)
+            y_h.copy_(y, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        s_e, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_e.record(stream)
+        for _ in range(ke):
+            x.copy_(x_h, non_blocking=True)
+            if y0_h is not None:
+                y.copy_(y0_h, non_blocking=True)
+            plan(x, y, W.alpha, W.beta, stream)
+            y_h.copy_(y, non_blocking=True)
+        e_e.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s_e.elapsed_time(e_e) / ke
+        if world > 1:
+            te = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+            e2e_ms = float(te.item())
+        s = A.vals.dtype.itemsize
+        h2d = A.n * s + (A.m * s if W.y0 is not None else 0)
+        e2e = {"value": round(2.0 * A.nnz / (e2e_ms * 1e-3) / 1e9 * world, 3), "unit": "GFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(A.m * s), "ms_per_step": round(e2e_ms, 4),
+               "steps": ke}
+    plan.close()
+    if rank != 0:
+        return None
+
+    ms_step = total_ms / K
+    bc = compulsory_bytes(A)
+    gflops = 2.0 * A.nnz / (ms_step * 1e-3) / 1e9 * world
+    mean_us = float(per.mean())
+    achieved = bc / (mean_us * 1e-6) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic, traffic_note = recorded_traffic(workload_name, info["kernel_name"])
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
+            "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4), "traffic": traffic,
+            "kernel": info["kernel_name"], "algorithmic_bytes_per_launch": int(bc)}
+    if traffic_note:
+        roof["traffic_note"] = traffic_note
+    out = {
+        "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": A.dtype, "data": "synthetic",
+        "config": {"workload": workload_name, "description": W.description, "m": A.m, "n": A.n, "nnz": A.nnz,
+                   "alpha": W.alpha, "beta": W.beta, "kernel": info["kernel_name"],
+                   "items_per_tile": info["items_per_tile"], "num_tiles": info["num_tiles"],
+                   "l2": "inputs larger than L2, no flush (x stays L2-resident across steps)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "gbs_effective": round(achieved, 1),
+        "median_us": round(float(np.median(per)), 3), "p10_us": round(float(np.percentile(per, 10)), 3),
+        "p90_us": round(float(np.percentile(per, 90)), 3), "compulsory_bytes": int(bc),
+        "plan_ms": round(plan_ms, 3), "roofline": roof,
+        "gpu_launches": int(K * info["launches_per_execute"]),
+        "e2e": e2e, "clocks": clocks,
+    }
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+
+def oracle_sample(W, budget_s: float):
+    """Time the oracle on a leading block of rows sized to ~budget_s seconds."""
+    import oracle
+    A = W.A
+    lens = np.diff(A.row_ptr.astype(np.int64))
+    cum = np.cumsum(lens)
+
+    def rows_for(nnz_target):
+        r = int(np.searchsorted(cum, nnz_target)) + 1
+        return max(1, min(A.m, r))
+
+    def run(r):
+        rows = np.arange(r, dtype=np.int32)
+        t = time.perf_counter()
+        oracle.spmv(A.row_ptr, A.col_idx, A.vals, W.x, W.alpha, W.beta, W.y0, rows=rows)
+        return time.perf_counter() - t
+
+    r = rows_for(200_000)
+    t = run(r)
+    nnz_r = int(A.row_ptr[r])
+    rate = max(nnz_r, 1) / max(t, 1e-6)
+    r = rows_for(rate * budget_s)
+    return r, int(A.row_ptr[r])
+
+
+def run_reference(args, workload_name: str) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    W = synth.workload(workload_name)
+    A = W.A
+    per_step = max(0.05, min(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    r, nnz_s = oracle_sample(W, per_step)
+    rows = np.arange(r, dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle.spmv(A.row_ptr, A.col_idx, A.vals, W.x, W.alpha, W.beta, W.y0, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.spmv(A.row_ptr, A.col_idx, A.vals, W.x, W.alpha, W.beta, W.y0, rows=rows)
+        times.append(time.perf_counter() - t)
+    tot = float(np.sum(times))
+    gflops = 2.0 * nnz_s * args.steps / tot / 1e9
+    sample = f"rows [0, {r}) of {A.m} ({nnz_s} of {A.nnz} nonzeros) per step"
+    return {
+        "metric": METRIC, "value": round(gflops, 4), "unit": "GFLOP/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": A.dtype, "data": "synthetic", "impl": "reference",
+        "config": {"workload": workload_name, "description": W.description, "m": A.m, "n": A.n, "nnz": A.nnz,
+                   "alpha": W.alpha, "beta": W.beta},
+        "cpu_baseline": {"value": round(gflops, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": round(gflops, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                low = line.lower()
+                if low.startswith("model name") or low.startswith("cpu part") or low.startswith("hardware"):
+                    return f"{platform.machine()} {line.split(':', 1)[1].strip()} ({os.cpu_count()} cores)"
+    except Exception:
+        pass
+    return f"{platform.machine()} ({os.cpu_count()} cores)"
+
+
+def cpu_baseline_leg(workload_name: str, budget_s: float) -> dict:
+    import oracle
+    W = synth.workload(workload_name)
+    A = W.A
+    r, nnz_s = oracle_sample(W, budget_s / 3)
+    rows = np.arange(r, dtype=np.int32)
+    ts = []
+    for _ in range(3):
+        t = time.perf_counter()
+        oracle.spmv(A.row_ptr, A.col_idx, A.vals, W.x, W.alpha, W.beta, W.y0, rows=rows)
+        ts.append(time.perf_counter() - t)
+    t = float(np.median(ts))
+    return {"value": round(2.0 * nnz_s / t / 1e9, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"rows [0, {r}) of {A.m} ({nnz_s} of {A.nnz} nonzeros), median of 3, long double",
+            "cpu": cpu_model()}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS)
+    ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="auto")
+    ap.add_argument("--ipt", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        for name in (synth.WORKLOADS if args.all else [args.workload]):
+            out = run_reference(args, name)
+            if out is not None:
+                print(json.dumps(out), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    names = synth.WORKLOADS if args.all else [args.workload]
+    for name in names:
+        out = run_gpu(args, name)
+        if out is not None:
+            # the oracle is timed on rank 0 at N = 1 only
+            out["cpu_baseline"] = cpu_baseline_leg(name, args.cpu_budget) \
+                if world == 1 and not args.no_cpu_baseline else None
+            out["source_hash"] = kernel_source_hash()
+            print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

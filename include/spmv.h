@@ -1,0 +1,195 @@
+/*
+ * Load-balanced CSR sparse matrix-vector product for one GB300 (sm_103a).
+ *
+ *     y = alpha * A * x + beta * y
+ *
+ * A is an m-by-n matrix in CSR form with int32 indices and fp32 or fp64
+ * values.  CSR as defined on the Row-grouped CSR page ("New Row-grouped CSR
+ * format for storing the sparse matrices on GPU with implementation in CUDA",
+ * section 3, Figure 1): the nonzeros are stored row by row in `vals` with
+ * their column indices in `col_idx`; `row_ptr` has m+1 entries, row i owns
+ * positions row_ptr[i] .. row_ptr[i+1]-1, and row_ptr[m] = nnz.  The same
+ * three arrays are the SpMV kernel's inputs in the load-balancing paper
+ * (Osama, Porumbescu, Owens, "A GPU load-balancing programming model",
+ * section 4.3, Listing 3), which computes each y entry as the row's sum of
+ * values[nz] * x[indices[nz]].
+ *
+ * The library works in two steps.  spmv_plan_create analyses the row
+ * lengths on the GPU (statistics by length class, after OpSparse's row
+ * binning, section 5.1), chooses a kernel, and precomputes its schedule --
+ * for the default merge-path kernel, the exact split of the m + nnz units
+ * of work (every row end and every nonzero, "A GPU load-balancing
+ * programming model", section 5.2.1) into equal tiles.  spmv_execute then
+ * runs the product on a stream with no allocation and no synchronisation.
+ *
+ * All array arguments are DEVICE pointers (for example from torch CUDA
+ * tensors) on the current CUDA device, except where a function says HOST.
+ * Streams are cudaStream_t handles; NULL is the legacy default stream.
+ * Every function returns an spmv_status_t; spmv_last_error() gives a
+ * one-line description of the last failure on the calling thread.
+ */
+#ifndef LBCSR_SPMV_H
+#define LBCSR_SPMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* a cudaStream_t */
+typedef struct CUstream_st *spmv_stream_t;
+
+typedef struct spmv_plan_s *spmv_plan_t;
+
+typedef enum { SPMV_F32 = 0, SPMV_F64 = 1 } spmv_dtype_t;
+
+typedef enum {
+    SPMV_OK = 0,
+    SPMV_ERR_INVALID_ARG = 1, /* null pointer, negative size, size limits, bad option */
+    SPMV_ERR_INVALID_CSR = 2, /* row_ptr[0] != 0, row_ptr decreasing, row_ptr[m] != nnz,
+                                 or a column index outside [0, n) */
+    SPMV_ERR_ALLOC = 3,       /* device or host allocation failed in plan creation */
+    SPMV_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
+    SPMV_ERR_UNSUPPORTED = 5  /* device is not sm_103 / option not available */
+} spmv_status_t;
+
+/* Kernels a plan can run. */
+typedef enum {
+    SPMV_KERNEL_AUTO = 0,       /* let the plan choose from the row-length statistics */
+    SPMV_KERNEL_MERGE_PATH = 1, /* equal shares of rows + nonzeros per CTA, carry-out fix-up */
+    SPMV_KERNEL_THREAD_ROW = 2, /* one thread per row */
+    SPMV_KERNEL_RGCSR = 3,      /* Row-grouped CSR (interleaved copy of A built by the plan) */
+    SPMV_KERNEL_LONG_ROWS = 4   /* long rows by warp/CTA kernels, the rest by merge path */
+} spmv_kernel_t;
+
+/* Options for spmv_plan_create_ex; zero-initialise and set what you need. */
+typedef struct {
+    int32_t kernel;           /* spmv_kernel_t; SPMV_KERNEL_AUTO (0) = choose */
+    int32_t items_per_thread; /* merge-path work items per thread; 0 = default.
+                                 Allowed: 4, 8, 12, 16 */
+    int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = default.
+                                 Allowed: 32, 64, 128, 256 */
+    int32_t long_row_min;     /* rows with at least this many nonzeros count as
+                                 long (SPMV_KERNEL_LONG_ROWS); 0 = default */
+} spmv_options_t;
+
+/*
+ * Row-length statistics measured by the plan.  hist[k] counts rows whose
+ * length falls in class k: class 0 = empty rows, class k >= 1 = lengths in
+ * [2^(k-1), 2^k).  rg_slots[g] = storage (slots) a Row-grouped CSR layout
+ * with group size 32 << g would need (each group padded to its longest
+ * row).  flags: bit0 row_ptr[0] != 0, bit1 row_ptr decreases, bit2
+ * row_ptr[m] != nnz, bit3 a column index outside [0, n).
+ */
+typedef struct {
+    int64_t hist[32];
+    int64_t sum_len;
+    int64_t rg_slots[4];
+    int32_t min_len;
+    int32_t max_len;
+    int32_t n_empty;
+    int32_t flags;
+} spmv_row_stats_t;
+
+typedef struct {
+    int32_t m, n, nnz;
+    int32_t dtype;                /* spmv_dtype_t */
+    int32_t kernel;               /* spmv_kernel_t actually used */
+    int32_t threads_per_cta;      /* merge-path kernel */
+    int32_t items_per_thread;     /* merge-path kernel */
+    int32_t rgcsr_group;          /* Row-grouped CSR kernel */
+    int64_t items_per_tile;       /* merge-path tile T = threads * items (rows + nonzeros) */
+    int64_t num_tiles;            /* merge-path tiles P = ceil((m + nnz) / T), at least 1 */
+    int32_t num_long_rows;        /* rows handled by the long-row kernels */
+    int32_t launches_per_execute; /* kernel launches one spmv_execute issues */
+    int64_t workspace_bytes;      /* device memory the plan owns */
+    spmv_row_stats_t stats;
+} spmv_plan_info_t;
+
+/* What spmv_plan_export copies out. */
+typedef enum {
+    SPMV_EXPORT_PARTITION = 0,   /* int32 pairs (row, nonzero), num_tiles + 1 of them */
+    SPMV_EXPORT_RG_GROUP_PTR = 1,/* int64[ceil(m/G) + 1] */
+    SPMV_EXPORT_RG_ROW_LEN = 2,  /* int32[m] */
+    SPMV_EXPORT_RG_COL = 3,      /* int32[group_ptr[last]] */
+    SPMV_EXPORT_RG_VAL = 4,      /* value type [group_ptr[last]] */
+    SPMV_EXPORT_LONG_ROWS = 5    /* int32[num_long_rows], ascending */
+} spmv_export_t;
+
+/*
+ * Build a plan for A (device arrays row_ptr[m+1], col_idx[nnz], vals[nnz]).
+ *
+ * Limits: m >= 0, n >= 0, 0 <= nnz, m + nnz < 2^31.  When nnz > 0 the
+ * pointers must be non-null; row_ptr must be non-null when m >= 0.
+ * Ownership: the plan BORROWS row_ptr, col_idx and vals; they must stay
+ * allocated and unchanged until spmv_plan_destroy (values may change if
+ * spmv_plan_update_values is called afterwards).  The plan OWNS one device
+ * workspace, allocated here and freed by spmv_plan_destroy.
+ * Synchronisation: runs its analysis kernels on `stream` and waits for that
+ * stream once (to read the ~0.4 KB statistics back).  Results are
+ * synchronous.
+ * Errors: INVALID_ARG for bad sizes/pointers; INVALID_CSR when the analysis
+ * finds a malformed row_ptr or a column index outside [0, n); ALLOC; CUDA;
+ * UNSUPPORTED when the current device is not compute capability 10.3.
+ * On error *out is set to NULL and nothing is leaked.
+ */
+spmv_status_t spmv_plan_create(spmv_plan_t *out, int32_t m, int32_t n, int32_t nnz,
+                               const int32_t *row_ptr, const int32_t *col_idx, const void *vals,
+                               spmv_dtype_t dtype, spmv_stream_t stream);
+
+/* As spmv_plan_create, with options (NULL = defaults). */
+spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_t nnz,
+                                  const int32_t *row_ptr, const int32_t *col_idx, const void *vals,
+                                  spmv_dtype_t dtype, const spmv_options_t *options,
+                                  spmv_stream_t stream);
+
+/*
+ * y = alpha * A * x + beta * y on `stream` (device x[n], y[m] of the plan's
+ * value type).  alpha and beta are rounded to the value type.  If beta == 0
+ * y is write-only: its old contents (NaN included) are not read.  x and y
+ * must not overlap.  Asynchronous: returns after queueing the kernels; no
+ * allocation, no host synchronisation.  A plan must not run on two streams
+ * at once (its workspace holds per-execution carry state).
+ * Errors: INVALID_ARG (null plan, or null x/y when the sizes need them),
+ * CUDA (launch failure).
+ */
+spmv_status_t spmv_execute(spmv_plan_t plan, double alpha, const void *x, double beta, void *y,
+                           spmv_stream_t stream);
+
+/*
+ * Point the plan at new values with the same sparsity pattern (vals[nnz],
+ * device).  Plans that keep a reordered copy of the values (the
+ * Row-grouped CSR kernel) repack it on `stream`; the others only record the
+ * pointer.  Same ownership rule as at creation.
+ */
+spmv_status_t spmv_plan_update_values(spmv_plan_t plan, const void *vals, spmv_stream_t stream);
+
+/* Free the plan's workspace (waits for the device to finish using it). NULL is a no-op. */
+spmv_status_t spmv_plan_destroy(spmv_plan_t plan);
+
+/* Fill *info (HOST) with the plan's sizes, chosen kernel and statistics. */
+spmv_status_t spmv_plan_info(spmv_plan_t plan, spmv_plan_info_t *info);
+
+/*
+ * Copy one of the plan's internal arrays into HOST memory dst of `bytes`
+ * bytes (for tests and inspection; synchronous).  INVALID_ARG if the plan
+ * does not hold that array or bytes is smaller than its size; the size is
+ * written to *needed when needed != NULL.
+ */
+spmv_status_t spmv_plan_export(spmv_plan_t plan, spmv_export_t what, void *dst, size_t bytes,
+                               size_t *needed);
+
+/* Static text for a status code. */
+const char *spmv_status_string(spmv_status_t status);
+
+/* Description of the last error on the calling thread ("" if none). */
+const char *spmv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LBCSR_SPMV_H */

@@ -1,0 +1,213 @@
+"""Load-balanced CSR SpMV for GB300 -- Python binding of ``libspmv.so``.
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels (include/spmv.h documents the C ABI).  PyTorch supplies device
+memory and streams.  There is no CPU path: if the library cannot be loaded
+the import of ``lib()`` raises.
+
+    import torch, load_balanced_csr_gb300 as lb
+    plan = lb.Plan(row_ptr, col_idx, vals, n)      # CUDA tensors: int32, int32, f32/f64
+    plan(x, y, alpha=1.0, beta=0.0)               # y = alpha*A*x + beta*y on the current stream
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = ["Plan", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
+
+KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+EXPORTS = {"partition": 0, "rg_group_ptr": 1, "rg_row_len": 2, "rg_col": 3, "rg_val": 4, "long_rows": 5}
+STATUS = {0: "ok", 1: "invalid argument", 2: "invalid CSR matrix", 3: "allocation failed", 4: "CUDA error",
+          5: "unsupported"}
+
+
+class SpmvError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({detail})")
+        self.status = status
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("items_per_thread", ctypes.c_int32),
+                ("rgcsr_group", ctypes.c_int32), ("long_row_min", ctypes.c_int32)]
+
+
+class RowStats(ctypes.Structure):
+    _fields_ = [("hist", ctypes.c_int64 * 32), ("sum_len", ctypes.c_int64), ("rg_slots", ctypes.c_int64 * 4),
+                ("min_len", ctypes.c_int32), ("max_len", ctypes.c_int32), ("n_empty", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32), ("nnz", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32),
+                ("items_per_thread", ctypes.c_int32), ("rgcsr_group", ctypes.c_int32),
+                ("items_per_tile", ctypes.c_int64), ("num_tiles", ctypes.c_int64),
+                ("num_long_rows", ctypes.c_int32), ("launches_per_execute", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64), ("stats", RowStats)]
+
+
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/spmv.h declares."""
+    import re
+    with open(os.path.join(_build.INCLUDE, "spmv.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^(?:spmv_status_t|const char \*)\s*(spmv_\w+)\s*\(", text, re.M)))
+
+
+def lib() -> ctypes.CDLL:
+    """Load libspmv.so (building it first if its sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError("libspmv.so is missing and could not be built")
+        L = ctypes.CDLL(path)
+        vp, i32, sz, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_double
+        sigs = {
+            "spmv_plan_create": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int, vp],
+            "spmv_plan_create_ex": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int,
+                                    ctypes.POINTER(Options), vp],
+            "spmv_execute": [vp, dbl, vp, dbl, vp, vp],
+            "spmv_plan_update_values": [vp, vp, vp],
+            "spmv_plan_destroy": [vp],
+            "spmv_plan_info": [vp, ctypes.POINTER(PlanInfo)],
+            "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
+        }
+        for name, args in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.spmv_status_string.argtypes = [ctypes.c_int]
+        L.spmv_status_string.restype = ctypes.c_char_p
+        L.spmv_last_error.argtypes = []
+        L.spmv_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def check(status: int, what: str) -> None:
+    if status != 0:
+        raise SpmvError(status, what, lib().spmv_last_error().decode())
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.float64:
+        return 1
+    raise TypeError(f"values must be float32 or float64, got {t.dtype}")
+
+
+def _ptr(t) -> int | None:
+    return t.data_ptr() if t is not None and t.numel() > 0 else None
+
+
+class Plan:
+    """A plan for y = alpha*A*x + beta*y with A in CSR (CUDA tensors).
+
+    The plan borrows ``row_ptr``, ``col_idx`` and ``vals`` (kept referenced
+    here so they stay alive) and owns a device workspace freed by
+    ``close()``."""
+
+    def __init__(self, row_ptr, col_idx, vals, n: int, *, kernel: str = "auto", items_per_thread: int = 0,
+                 rgcsr_group: int = 0, long_row_min: int = 0, stream=None):
+        import torch
+        for name, t, dt in (("row_ptr", row_ptr, torch.int32), ("col_idx", col_idx, torch.int32)):
+            if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+        if not vals.is_cuda or not vals.is_contiguous():
+            raise TypeError("vals must be a contiguous CUDA tensor")
+        m = row_ptr.numel() - 1
+        nnz = col_idx.numel()
+        if vals.numel() != nnz:
+            raise ValueError("vals and col_idx differ in length")
+        self._keep = (row_ptr, col_idx, vals)
+        self.m, self.n, self.nnz = m, int(n), nnz
+        self.dtype = vals.dtype
+        opts = Options(KERNELS[kernel], items_per_thread, rgcsr_group, long_row_min)
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(row_ptr.device):
+            check(lib().spmv_plan_create_ex(ctypes.byref(handle), m, self.n, nnz, _ptr(row_ptr), _ptr(col_idx),
+                                            _ptr(vals), _dtype_code(vals), ctypes.byref(opts),
+                                            _stream_handle(stream)), "spmv_plan_create")
+        self._h = handle
+        self.device = row_ptr.device
+
+    def __call__(self, x, y, alpha: float = 1.0, beta: float = 0.0, stream=None):
+        return self.execute(x, y, alpha, beta, stream)
+
+    def execute(self, x, y, alpha: float = 1.0, beta: float = 0.0, stream=None):
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        if x.dtype != self.dtype or y.dtype != self.dtype:
+            raise TypeError("x and y must have the plan's value type")
+        if x.numel() != self.n or y.numel() != self.m or not x.is_contiguous() or not y.is_contiguous():
+            raise ValueError("x must have n and y m contiguous entries")
+        if not x.is_cuda or not y.is_cuda:
+            raise TypeError("x and y must be CUDA tensors")
+        check(lib().spmv_execute(self._h, float(alpha), _ptr(x), float(beta), _ptr(y), _stream_handle(stream)),
+              "spmv_execute")
+        return y
+
+    def update_values(self, vals, stream=None):
+        if vals.numel() != self.nnz or vals.dtype != self.dtype or not vals.is_contiguous():
+            raise ValueError("vals must match the plan's nnz and value type")
+        check(lib().spmv_plan_update_values(self._h, _ptr(vals), _stream_handle(stream)), "spmv_plan_update_values")
+        self._keep = (self._keep[0], self._keep[1], vals)
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        check(lib().spmv_plan_info(self._h, ctypes.byref(inf)), "spmv_plan_info")
+        out = {f: getattr(inf, f) for f, _ in PlanInfo._fields_ if f != "stats"}
+        s = inf.stats
+        out["stats"] = {"hist": list(s.hist), "sum_len": s.sum_len, "rg_slots": list(s.rg_slots),
+                        "min_len": s.min_len, "max_len": s.max_len, "n_empty": s.n_empty, "flags": s.flags}
+        out["kernel_name"] = KERNEL_NAMES.get(inf.kernel, str(inf.kernel))
+        return out
+
+    def export(self, what: str):
+        import numpy as np
+        code = EXPORTS[what]
+        need = ctypes.c_size_t(0)
+        check(lib().spmv_plan_export(self._h, code, None, 0, ctypes.byref(need)), "spmv_plan_export")
+        dtype = {"partition": np.int32, "rg_group_ptr": np.int64, "rg_row_len": np.int32, "rg_col": np.int32,
+                 "long_rows": np.int32,
+                 "rg_val": np.float64 if str(self.dtype) == "torch.float64" else np.float32}[what]
+        buf = np.empty(need.value // np.dtype(dtype).itemsize, dtype=dtype)
+        check(lib().spmv_plan_export(self._h, code, buf.ctypes.data if buf.size else None, need.value, None),
+              "spmv_plan_export")
+        return buf.reshape(-1, 2) if what == "partition" else buf
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            check(lib().spmv_plan_destroy(self._h), "spmv_plan_destroy")
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False

@@ -1,0 +1,326 @@
+// C ABI of the load-balanced CSR SpMV library: plan creation (analysis,
+// kernel choice, schedule), execution, inspection.  Declarations and the
+// contract of every entry point are in include/spmv.h.
+//
+// Memory: a plan makes its device allocations once, at creation, in one
+// arena (OpSparse, section 5.1: all metadata sized up front and allocated
+// with one cudaMalloc, since allocation is far slower than use), plus a
+// second allocation only for kernels that keep a reordered copy of A.
+// spmv_execute allocates and frees nothing and never waits for the device.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "internal.cuh"
+
+using namespace lbcsr;
+
+struct spmv_plan_s {
+    int32_t m = 0, n = 0, nnz = 0;
+    spmv_dtype_t dtype = SPMV_F32;
+    const int32_t *row_ptr = nullptr;
+    const int32_t *col_idx = nullptr;
+    const void *vals = nullptr;
+
+    spmv_kernel_t kernel = SPMV_KERNEL_MERGE_PATH;
+    int ipt = 7;
+    int64_t tile = 0;        // T
+    int64_t num_tiles = 0;   // P
+    int rgcsr_group = 0;
+    int32_t num_long_rows = 0;
+
+    void *arena = nullptr;
+    size_t arena_bytes = 0;
+    int2 *part = nullptr;
+    void *tail_partial = nullptr;
+    void *head_partial = nullptr;
+    int32_t *arrivals = nullptr;
+
+    spmv_row_stats_t stats{};
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+spmv_status_t fail(spmv_status_t s, const std::string &msg) {
+    g_last_error = msg;
+    return s;
+}
+
+spmv_status_t cuda_fail(cudaError_t e, const char *what) {
+    return fail(SPMV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t value_size(spmv_dtype_t d) { return d == SPMV_F64 ? 8 : 4; }
+
+int env_int(const char *name, int fallback) {
+    const char *v = std::getenv(name);
+    if (!v || !*v) return fallback;
+    return std::atoi(v);
+}
+
+spmv_kernel_t env_kernel() {
+    const char *v = std::getenv("SPMV_FORCE_KERNEL");
+    if (!v || !*v) return SPMV_KERNEL_AUTO;
+    if (!std::strcmp(v, "merge_path")) return SPMV_KERNEL_MERGE_PATH;
+    if (!std::strcmp(v, "thread_row")) return SPMV_KERNEL_THREAD_ROW;
+    if (!std::strcmp(v, "rgcsr")) return SPMV_KERNEL_RGCSR;
+    if (!std::strcmp(v, "long_rows")) return SPMV_KERNEL_LONG_ROWS;
+    return SPMV_KERNEL_AUTO;
+}
+
+// Kernel choice from the measured row-length statistics.
+//  * n == 1 with short rows: thread per row, CUB's special case for a
+//    single-column matrix named in "A GPU load-balancing programming model"
+//    (section 6.1): perfectly balanced work needs no balancing.
+//  * small matrices: the same paper's rule (section 6.2) -- merge path unless
+//    (rows < 500 or columns < 500) and nnz < 10000 -- with rows capped at 256
+//    nonzeros so the sequential per-row sum stays accurate.
+//  * everything else: merge path.
+spmv_kernel_t choose_kernel(const spmv_plan_s &p) {
+    const spmv_row_stats_t &s = p.stats;
+    if (p.n == 1 && s.max_len <= 32) return SPMV_KERNEL_THREAD_ROW;
+    if ((p.m < 500 || p.n < 500) && p.nnz < 10000 && s.max_len <= 256) return SPMV_KERNEL_THREAD_ROW;
+    return SPMV_KERNEL_MERGE_PATH;
+}
+
+void destroy_plan(spmv_plan_s *p) {
+    if (!p) return;
+    if (p->arena) cudaFree(p->arena);
+    delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *spmv_status_string(spmv_status_t s) {
+    switch (s) {
+    case SPMV_OK: return "ok";
+    case SPMV_ERR_INVALID_ARG: return "invalid argument";
+    case SPMV_ERR_INVALID_CSR: return "invalid CSR matrix";
+    case SPMV_ERR_ALLOC: return "allocation failed";
+    case SPMV_ERR_CUDA: return "CUDA error";
+    case SPMV_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+const char *spmv_last_error(void) { return g_last_error.c_str(); }
+
+spmv_status_t spmv_plan_create(spmv_plan_t *out, int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
+                               const int32_t *col_idx, const void *vals, spmv_dtype_t dtype,
+                               spmv_stream_t stream) {
+    return spmv_plan_create_ex(out, m, n, nnz, row_ptr, col_idx, vals, dtype, nullptr, stream);
+}
+
+spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_t nnz,
+                                  const int32_t *row_ptr, const int32_t *col_idx, const void *vals,
+                                  spmv_dtype_t dtype, const spmv_options_t *options,
+                                  spmv_stream_t stream_handle) {
+    g_last_error.clear();
+    if (!out) return fail(SPMV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (m < 0 || n < 0 || nnz < 0) return fail(SPMV_ERR_INVALID_ARG, "negative size");
+    if ((int64_t)m + (int64_t)nnz >= (1LL << 31)) return fail(SPMV_ERR_INVALID_ARG, "m + nnz must be < 2^31");
+    if (dtype != SPMV_F32 && dtype != SPMV_F64) return fail(SPMV_ERR_INVALID_ARG, "unknown dtype");
+    if (!row_ptr) return fail(SPMV_ERR_INVALID_ARG, "row_ptr is NULL");
+    if (nnz > 0 && (!col_idx || !vals)) return fail(SPMV_ERR_INVALID_ARG, "col_idx or vals is NULL");
+
+    spmv_options_t opt{};
+    if (options) opt = *options;
+    spmv_kernel_t forced = (spmv_kernel_t)opt.kernel;
+    if (forced == SPMV_KERNEL_AUTO) forced = env_kernel();
+    if (forced < SPMV_KERNEL_AUTO || forced > SPMV_KERNEL_LONG_ROWS)
+        return fail(SPMV_ERR_INVALID_ARG, "unknown kernel option");
+    if (forced == SPMV_KERNEL_RGCSR || forced == SPMV_KERNEL_LONG_ROWS)
+        return fail(SPMV_ERR_UNSUPPORTED, "kernel not built in this version");
+    int ipt = opt.items_per_thread ? opt.items_per_thread : env_int("SPMV_ITEMS_PER_THREAD", 7);
+    if (!merge_path_supported(ipt)) return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 5, 7, 9, 11 or 13");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(SPMV_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300) only");
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    spmv_plan_s *p = new (std::nothrow) spmv_plan_s();
+    if (!p) return fail(SPMV_ERR_ALLOC, "host allocation failed");
+    p->m = m;
+    p->n = n;
+    p->nnz = nnz;
+    p->dtype = dtype;
+    p->row_ptr = row_ptr;
+    p->col_idx = col_idx;
+    p->vals = vals;
+    p->ipt = ipt;
+    p->tile = (int64_t)merge_path_threads() * ipt;
+    const int64_t total = (int64_t)m + nnz;
+    p->num_tiles = total > 0 ? (total + p->tile - 1) / p->tile : 1;
+
+    // ---- one arena: analysis scratch + merge-path schedule and carry state
+    const int stats_ctas = stats_num_ctas(m, nnz);
+    const size_t vs = value_size(dtype);
+    const size_t P = (size_t)p->num_tiles;
+    size_t off = 0;
+    const size_t off_partials = off;
+    off = align_up(off + sizeof(StatsPartial) * stats_ctas, 256);
+    const size_t off_stats = off;
+    off = align_up(off + sizeof(spmv_row_stats_t), 256);
+    const size_t off_part = off;
+    off = align_up(off + sizeof(int2) * (P + 1), 256);
+    const size_t off_tail = off;
+    off = align_up(off + vs * P, 256);
+    const size_t off_head = off;
+    off = align_up(off + vs * P, 256);
+    const size_t off_arr = off;
+    off = align_up(off + sizeof(int32_t) * P, 256);
+    p->arena_bytes = off;
+    e = cudaMalloc(&p->arena, p->arena_bytes);
+    if (e != cudaSuccess) {
+        p->arena = nullptr;
+        destroy_plan(p);
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the plan workspace: ") + cudaGetErrorString(e));
+    }
+    char *base = static_cast<char *>(p->arena);
+    StatsPartial *partials = reinterpret_cast<StatsPartial *>(base + off_partials);
+    spmv_row_stats_t *d_stats = reinterpret_cast<spmv_row_stats_t *>(base + off_stats);
+    p->part = reinterpret_cast<int2 *>(base + off_part);
+    p->tail_partial = base + off_tail;
+    p->head_partial = base + off_head;
+    p->arrivals = reinterpret_cast<int32_t *>(base + off_arr);
+
+    // ---- analysis: statistics + validity, read back once
+    e = cudaMemsetAsync(p->arrivals, 0, sizeof(int32_t) * P, stream);
+    if (e == cudaSuccess) e = launch_row_stats(m, n, nnz, row_ptr, col_idx, partials, stats_ctas, d_stats, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&p->stats, d_stats, sizeof(spmv_row_stats_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        destroy_plan(p);
+        return cuda_fail(e, "plan analysis");
+    }
+    if (p->stats.flags) {
+        const int f = p->stats.flags;
+        destroy_plan(p);
+        char msg[160];
+        std::snprintf(msg, sizeof msg, "invalid CSR:%s%s%s%s", (f & 1) ? " row_ptr[0] != 0;" : "",
+                      (f & 2) ? " row_ptr decreases;" : "", (f & 4) ? " row_ptr[m] != nnz;" : "",
+                      (f & 8) ? " column index outside [0, n);" : "");
+        return fail(SPMV_ERR_INVALID_CSR, msg);
+    }
+
+    // ---- kernel choice and schedule
+    p->kernel = forced != SPMV_KERNEL_AUTO ? forced : choose_kernel(*p);
+    if (p->kernel == SPMV_KERNEL_MERGE_PATH && m > 0) {
+        e = launch_merge_path_partition(m, nnz, row_ptr, p->tile, p->num_tiles, p->part, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) {
+            destroy_plan(p);
+            return cuda_fail(e, "merge-path partition");
+        }
+    }
+    *out = p;
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double beta, void *y,
+                           spmv_stream_t stream_handle) {
+    if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
+    if (p->m == 0) return SPMV_OK;
+    if (!y) return fail(SPMV_ERR_INVALID_ARG, "y is NULL");
+    if (!x && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "x is NULL");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    cudaError_t e = cudaSuccess;
+    switch (p->kernel) {
+    case SPMV_KERNEL_THREAD_ROW:
+        e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, stream);
+        break;
+    case SPMV_KERNEL_MERGE_PATH:
+    default: {
+        MergePathArgs a;
+        a.m = p->m;
+        a.nnz = p->nnz;
+        a.row_ptr = p->row_ptr;
+        a.col_idx = p->col_idx;
+        a.vals = p->vals;
+        a.x = x;
+        a.y = y;
+        a.alpha = alpha;
+        a.beta = beta;
+        a.part = p->part;
+        a.num_tiles = p->num_tiles;
+        a.tail_partial = p->tail_partial;
+        a.head_partial = p->head_partial;
+        a.arrivals = p->arrivals;
+        e = launch_merge_path_spmv(p->dtype, p->ipt, a, stream);
+        break;
+    }
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_execute launch");
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stream_t) {
+    if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
+    if (!vals && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "vals is NULL");
+    p->vals = vals;
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_plan_destroy(spmv_plan_t p) {
+    if (!p) return SPMV_OK;
+    destroy_plan(p);
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
+    if (!p || !info) return fail(SPMV_ERR_INVALID_ARG, "plan or info is NULL");
+    std::memset(info, 0, sizeof *info);
+    info->m = p->m;
+    info->n = p->n;
+    info->nnz = p->nnz;
+    info->dtype = p->dtype;
+    info->kernel = p->kernel;
+    info->threads_per_cta = merge_path_threads();
+    info->items_per_thread = p->ipt;
+    info->rgcsr_group = p->rgcsr_group;
+    info->items_per_tile = p->tile;
+    info->num_tiles = p->num_tiles;
+    info->num_long_rows = p->num_long_rows;
+    info->launches_per_execute = p->m > 0 ? 1 : 0;
+    info->workspace_bytes = (int64_t)p->arena_bytes;
+    info->stats = p->stats;
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, size_t bytes, size_t *needed) {
+    if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
+    const void *src = nullptr;
+    size_t size = 0;
+    switch (what) {
+    case SPMV_EXPORT_PARTITION:
+        if (p->kernel != SPMV_KERNEL_MERGE_PATH) return fail(SPMV_ERR_INVALID_ARG, "plan has no merge-path partition");
+        src = p->part;
+        size = sizeof(int2) * (size_t)(p->num_tiles + 1);
+        break;
+    default: return fail(SPMV_ERR_INVALID_ARG, "plan does not hold this array");
+    }
+    if (needed) *needed = size;
+    if (!dst) return SPMV_OK;
+    if (bytes < size) return fail(SPMV_ERR_INVALID_ARG, "destination too small");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && size) e = cudaMemcpy(dst, src, size, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_export");
+    return SPMV_OK;
+}
+
+}  // extern "C"

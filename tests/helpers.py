@@ -1,0 +1,39 @@
+"""Shared test helpers: move seeded CSR inputs to the GPU and compare the
+CUDA path with the oracle under the accuracy bound
+
+    |y_i - y_ref_i| <= tau * (|alpha| sum_j |a_ij x_j| + |beta y_old_i|) + 1e-30,
+
+tau = 1e-5 for fp32 and 1e-13 for fp64."""
+import numpy as np
+
+import oracle
+
+TAU = {"f32": 1e-5, "f64": 1e-13}
+
+
+def to_gpu(A):
+    import torch
+    return (torch.from_numpy(A.row_ptr).cuda(), torch.from_numpy(A.col_idx).cuda(),
+            torch.from_numpy(A.vals).cuda())
+
+
+def assert_close_to_oracle(A, x, y_gpu, alpha, beta, y_old, rows=None, label=""):
+    """y_gpu: numpy result (all rows, or the rows listed)."""
+    ref, mag = oracle.spmv(A.row_ptr, A.col_idx, A.vals, x, alpha, beta, y_old, rows=rows)
+    got = y_gpu if rows is None else y_gpu[rows]
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    bound = TAU[A.dtype] * mag + 1e-30
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.flatnonzero(bad)[:5]
+        rr = idx if rows is None else np.asarray(rows)[idx]
+        raise AssertionError(f"{label}: {bad.sum()} rows out of tolerance, e.g. rows {rr.tolist()}: "
+                             f"got {got[idx].tolist()} want {ref[idx].tolist()} bound {bound[idx].tolist()}")
+    # empty rows: exactly beta*y_old in the value type (0 when beta == 0)
+    lens = np.diff(A.row_ptr)
+    sel = np.arange(A.m) if rows is None else np.asarray(rows)
+    empty = lens[sel] == 0
+    if empty.any():
+        t = np.float64 if A.dtype == "f64" else np.float32
+        want = (t(beta) * y_old[sel][empty]).astype(t) if beta != 0 else np.zeros(empty.sum(), t)
+        np.testing.assert_array_equal(got[empty], want, err_msg=f"{label}: empty rows")
