@@ -68,8 +68,9 @@ typedef enum {
 /* Options for spmv_plan_create_ex; zero-initialise and set what you need. */
 typedef struct {
     int32_t kernel;           /* spmv_kernel_t; SPMV_KERNEL_AUTO (0) = choose */
-    int32_t items_per_thread; /* merge-path work items per thread; 0 = default.
-                                 Allowed: 4, 8, 12, 16 */
+    int32_t items_per_thread; /* merge-path work items per thread; 0 = default
+                                 (11 for fp32, 7 for fp64). Allowed: 5, 7, 9,
+                                 11, 13, 15 */
     int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = default.
                                  Allowed: 32, 64, 128, 256 */
     int32_t long_row_min;     /* rows with at least this many nonzeros count as

@@ -140,8 +140,10 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
         return fail(SPMV_ERR_INVALID_ARG, "unknown kernel option");
     if (forced == SPMV_KERNEL_RGCSR || forced == SPMV_KERNEL_LONG_ROWS)
         return fail(SPMV_ERR_UNSUPPORTED, "kernel not built in this version");
-    int ipt = opt.items_per_thread ? opt.items_per_thread : env_int("SPMV_ITEMS_PER_THREAD", 7);
-    if (!merge_path_supported(ipt)) return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 5, 7, 9, 11 or 13");
+    int ipt = opt.items_per_thread ? opt.items_per_thread
+                                   : env_int("SPMV_ITEMS_PER_THREAD", dtype == SPMV_F64 ? 7 : 11);
+    if (!merge_path_supported(ipt))
+        return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 5, 7, 9, 11, 13 or 15");
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

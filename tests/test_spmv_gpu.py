@@ -43,7 +43,7 @@ def inputs(m, n, max_len, seed, dtype, empty_frac=0.2, dist=synth.DIST_NORMAL):
 @pytest.mark.parametrize("alpha,beta", ALPHA_BETA)
 @pytest.mark.parametrize("kernel", ["merge_path", "thread_row"])
 def test_random_matrices(dtype, alpha, beta, kernel):
-    for seed, (m, n, L) in enumerate([(5000, 3000, 20), (20011, 20011, 6), (1, 4000, 4000), (3333, 1, 1)]):
+    for seed, (m, n, L) in enumerate([(5000, 3000, 20), (20011, 20011, 6), (1, 4000, 4000), (9333, 1, 1)]):
         if kernel == "thread_row" and L > 256:
             continue  # sequential per-row sums: the plan uses this kernel for short rows only
         A, x, y0 = inputs(m, n, L, seed, dtype)
@@ -54,7 +54,7 @@ def test_random_matrices(dtype, alpha, beta, kernel):
         assert_close_to_oracle(A, x, y, alpha, beta, y0, label=f"{kernel} {dtype} m={m}")
 
 
-@pytest.mark.parametrize("ipt", [5, 7, 9, 11, 13])
+@pytest.mark.parametrize("ipt", [5, 7, 9, 11, 13, 15])
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
 def test_items_per_thread_variants(ipt, dtype):
     A, x, y0 = inputs(30000, 25000, 15, ipt, dtype)
