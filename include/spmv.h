@@ -183,6 +183,36 @@ spmv_status_t spmv_plan_info(spmv_plan_t plan, spmv_plan_info_t *info);
 spmv_status_t spmv_plan_export(spmv_plan_t plan, spmv_export_t what, void *dst, size_t bytes,
                                size_t *needed);
 
+/*
+ * One product y = alpha * A * x + beta * y that allocates nothing: no plan,
+ * no cudaMalloc/cudaFree, no allocating library call.  The pages have no
+ * counterpart; this entry point exists for callers that cannot allocate
+ * device memory when they need a product -- for example a service that
+ * hands the whole device to its own memory pool at start-up (a cudaMalloc
+ * would fail or fragment the pool), or a latency-critical loop where a
+ * cudaMalloc would synchronise the device and stall work queued on other
+ * streams.
+ *
+ * Arguments as spmv_plan_create plus spmv_execute (device arrays, the
+ * caller's stream).  It runs the merge-path kernel with its scratch in one
+ * fixed-size array (about 1.8 MB) inside the library's device image, which
+ * every GPU that loads the library holds until the process exits.  Limit:
+ * ceil((m + nnz) / T) <= 65536 tiles, T = 2,816 (fp32) or 1,792 (fp64),
+ * i.e. m + nnz up to about 184M (fp32) or 117M (fp64); larger sizes return
+ * SPMV_ERR_INVALID_ARG.  The matrix is NOT checked (use spmv_plan_create
+ * once to validate it); invalid indices give undefined results.
+ * All calls share the scratch array and each call clears what must start
+ * at zero, so calls that overlap on the GPU (two streams, two host threads)
+ * race.  The first call on a device looks up the array's device address;
+ * make that first call before any stream capture.  Asynchronous otherwise.
+ * Returns SPMV_OK, SPMV_ERR_INVALID_ARG or SPMV_ERR_CUDA (no message is set
+ * for spmv_last_error).
+ */
+spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
+                                   const int32_t *col_idx, const void *vals, spmv_dtype_t dtype,
+                                   double alpha, const void *x, double beta, void *y,
+                                   spmv_stream_t stream);
+
 /* Static text for a status code. */
 const char *spmv_status_string(spmv_status_t status);
 

@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "spmv_plan_destroy": [vp],
             "spmv_plan_info": [vp, ctypes.POINTER(PlanInfo)],
             "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
+            "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
