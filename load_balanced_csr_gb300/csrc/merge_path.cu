@@ -4,33 +4,34 @@
 // Owens), section 5.2.1 -- every row end and every nonzero is one unit of
 // work, the m + nnz units are split into equal tiles of T units, and each
 // worker finds where its share starts by a search over (row ends, nonzero
-// indices).  The plan computes the tile splits once (plan_kernels.cu); this
-// kernel does the rest inside each CTA:
+// indices).  The plan computes the tile splits once (plan_kernels.cu); each
+// CTA takes one tile:
 //
-//  1. stage the tile in shared memory: the row ends row_ptr[i0+1 .. i1], and
-//     for the nonzeros j in [j0, j1) either the products vals[j]*x[col[j]]
-//     (fp32) or the values and the gathered x[col[j]] side by side (fp64, so
-//     that the walk can use one fused multiply-add per nonzero).  col_idx and
-//     vals are read with 16-byte loads, all issued before the x gathers;
-//  2. each thread takes IPT consecutive units, finds its start by a binary
-//     search in shared memory, and walks them: a nonzero adds to the running
-//     sum, a row end closes the row;
+//  1. stage the tile in shared memory: the row ends row_ptr[i0+1 .. i1]
+//     (relative to the tile's first nonzero j0, with a sentinel), and for the
+//     nonzeros j in [j0, j1) either the products vals[j]*x[col[j]] (fp32) or
+//     the values and the gathered x[col[j]] (fp64).  col_idx and vals are
+//     read with 16-byte loads, all issued before the x gathers;
+//  2. the tile's nonzeros are split evenly over the threads (a thread's share
+//     differs from another's by at most one), and each thread walks its
+//     share: a nonzero adds to the running sum; after it, every row that
+//     ends there is closed.  Row ends cost no floating-point work, so every
+//     lane of every warp-wide add or FMA does useful work.  This matters on
+//     GB300: its fp64 unit runs 2 lanes per clock per SM and a warp
+//     instruction costs it the same whether 1 or 32 lanes are active;
 //  3. a segmented scan over the threads adds the sum carried into each
-//     thread's first finished row.  It stops as soon as every open segment
-//     has reached its start, so short rows cost one step;
-//  4. rows that start and end in the tile are written to y once, coalesced.
-//
-// GB300 runs fp64 arithmetic at 2 lanes per clock per SM, so the fp64 path
-// counts its floating-point instructions: one FMA per nonzero, 0-2 per row
-// (alpha = 1 and beta = 0 need none), and a few per thread for carries.
+//     thread's first closed row (it stops as soon as every open segment has
+//     reached its start, so short rows cost one step);
+//  4. a closed row's sum is kept in the slot of its last nonzero, which no
+//     other thread reads; rows are then written to y once, coalesced.
 //
 // Rows cut by a tile boundary ("partial tiles" in the section) are finished
 // without a second kernel and without any waiting: each tile holding part of
 // such a row stores its partial sum, then counts itself in on the row's
 // arrival counter; the tile that arrives last (the counter says how many to
 // expect: the tiles from the one holding the row's first nonzero to the one
-// holding its end) adds the partials in index order with a tree and writes
-// y.  The order of the sum does not depend on which tile arrives last, so
+// holding its end) adds the partials in tile order with a tree and writes y.
+// The order of the sum does not depend on which tile arrives last, so
 // results are deterministic.  (The CUB implementation the paper compares
 // with runs a separate fix-up step for these rows.)
 #include <climits>
@@ -62,14 +63,25 @@ struct MPParams {
     int32_t *arrivals;
 };
 
-template <typename V>
-__device__ __forceinline__ V finish_row(V s, V alpha, V beta, int mode, const V *y, int row) {
-    switch (mode) {
-    case 0: return s;
-    case 1: return alpha * s;
-    case 2: return fma(beta, y[row], s);
-    default: return fma(beta, y[row], alpha * s);
+// Shared memory of one tile (n = nonzeros, r = row ends, n + r <= T):
+//   fp32: prod[n + 4] | row_end[r + 1]
+//   fp64: val[n + 4] | xg[n + 4] | row_end[r + 1]
+// With sh <= 3 and n + r <= T this stays below the bound used here.
+template <typename V, int IPT>
+constexpr size_t tile_smem_bytes() {
+    constexpr int T = kThreads * IPT;
+    return (sizeof(V) == 8 ? 16 : 4) * (size_t)(T + 8) + 64;
+}
+
+// First row in [lo, hi) whose end is after position k (s_re ascends; the
+// sentinel s_re[hi] is larger than any position).
+__device__ __forceinline__ int rows_ending_by(const int *s_re, int lo, int hi, int k) {
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s_re[mid] <= k) lo = mid + 1;
+        else hi = mid;
     }
+    return lo;
 }
 
 template <typename V>
@@ -84,10 +96,14 @@ struct TileSmem {
     int run_finish[2];
 };
 
-template <typename V, int IPT>
-constexpr size_t dyn_smem_bytes() {
-    constexpr int T = kThreads * IPT;
-    return sizeof(V) * (T + 4) * (sizeof(V) == 8 ? 2 : 1) + sizeof(int) * T;
+template <typename V>
+__device__ __forceinline__ V finish_row(V s, V alpha, V beta, int mode, const V *y, int row) {
+    switch (mode) {
+    case 0: return s;
+    case 1: return alpha * s;
+    case 2: return fma(beta, y[row], s);
+    default: return fma(beta, y[row], alpha * s);
+    }
 }
 
 // Sum of the partials of one cut row, by the tile that arrived last.
@@ -118,9 +134,6 @@ merge_path_spmv_kernel(const MPParams<V> p) {
     constexpr bool F64 = sizeof(V) == 8;
     constexpr int T = kThreads * IPT;
     extern __shared__ __align__(16) unsigned char dsm[];
-    V *s_a = reinterpret_cast<V *>(dsm);                            // fp32 products / fp64 values
-    V *s_b = F64 ? s_a + (T + 4) : s_a;                              // fp64 gathered x
-    int *s_re = reinterpret_cast<int *>(dsm + sizeof(V) * (T + 4) * (F64 ? 2 : 1));
     __shared__ TileSmem<V> sm;
 
     const int tid = threadIdx.x;
@@ -133,12 +146,16 @@ merge_path_spmv_kernel(const MPParams<V> p) {
     const int i0 = c0.x, j0 = c0.y, i1 = c1.x, j1 = c1.y;
     const int nrows = i1 - i0;
     const int nnzt = j1 - j0;
-    const int nitems = nrows + nnzt;
-    const int base = VEC ? (j0 & ~3) : j0;  // staged element g sits at s_*[g - base]
-    const int sh = j0 - base;
+    const int base = VEC ? (j0 & ~3) : j0;  // staged nonzero g sits at index g - base
+    const int sh = j0 - base;               // tile nonzero k sits at index k + sh
+    const int nslots = (sh + nnzt + 4) & ~3;
+    V *s_a = reinterpret_cast<V *>(dsm);                  // fp32 products / fp64 values
+    V *s_b = F64 ? s_a + nslots : s_a;                    // fp64 gathered x
+    int *s_re = reinterpret_cast<int *>(F64 ? s_b + nslots : s_a + nslots);
 
     // ---- 1. stage
-    for (int r = tid; r < nrows; r += kThreads) s_re[r] = ld_stream(p.row_ptr + i0 + 1 + r);
+    for (int r = tid; r < nrows; r += kThreads) s_re[r] = ld_stream(p.row_ptr + i0 + 1 + r) - j0;
+    if (tid == 0) s_re[nrows] = INT_MAX;
     if (VEC) {
         constexpr int CH = ((T + 6) / 4 + kThreads - 1) / kThreads;
         const int nch = (j1 - base + 3) >> 2;
@@ -175,72 +192,71 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             if (c < nch) {
                 const int g = base + 4 * c;
                 const int ci[4] = {cc[u].x, cc[u].y, cc[u].z, cc[u].w};
+                V xv[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (g + e >= j0 && g + e < j1) {
-                        const V xv = ld_gather(p.x + ci[e]);
-                        if constexpr (F64) {
-                            s_a[g + e - base] = vv[u][e];
-                            s_b[g + e - base] = xv;
-                        } else {
-                            s_a[g + e - base] = vv[u][e] * xv;
-                        }
-                    }
+                for (int e = 0; e < 4; ++e) xv[e] = (g + e >= j0 && g + e < j1) ? ld_gather(p.x + ci[e]) : V(0);
+                if constexpr (F64) {
+                    reinterpret_cast<double2 *>(s_a)[2 * c] = make_double2(vv[u][0], vv[u][1]);
+                    reinterpret_cast<double2 *>(s_a)[2 * c + 1] = make_double2(vv[u][2], vv[u][3]);
+                    reinterpret_cast<double2 *>(s_b)[2 * c] = make_double2(xv[0], xv[1]);
+                    reinterpret_cast<double2 *>(s_b)[2 * c + 1] = make_double2(xv[2], xv[3]);
+                } else {
+                    reinterpret_cast<float4 *>(s_a)[c] =
+                        make_float4(vv[u][0] * xv[0], vv[u][1] * xv[1], vv[u][2] * xv[2], vv[u][3] * xv[3]);
                 }
             }
         }
     } else {
-#pragma unroll
-        for (int it = 0; it < IPT; ++it) {
-            const int k = tid + it * kThreads;
-            if (k < nnzt) {
-                const V xv = ld_gather(p.x + ld_stream(p.col_idx + j0 + k));
-                const V v = ld_stream(p.vals + j0 + k);
-                if constexpr (F64) {
-                    s_a[k] = v;
-                    s_b[k] = xv;
-                } else {
-                    s_a[k] = v * xv;
-                }
+        for (int k = tid; k < nnzt; k += kThreads) {
+            const V xv = ld_gather(p.x + ld_stream(p.col_idx + j0 + k));
+            const V v = ld_stream(p.vals + j0 + k);
+            if constexpr (F64) {
+                s_a[k] = v;
+                s_b[k] = xv;
+            } else {
+                s_a[k] = v * xv;
             }
         }
     }
     __syncthreads();
 
-    // ---- 2. thread split and walk: units [dt, dt + IPT) of the tile
-    const int dt = min(tid * IPT, nitems);
-    int lo = max(0, dt - nnzt), hi = min(dt, nrows);
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_re[mid] - j0 + mid < dt) lo = mid + 1;
-        else hi = mid;
-    }
-    const int r_first = lo;
-    int r = lo;
-    int k = dt - lo;
-    int re = r < nrows ? s_re[r] - j0 : INT_MAX;
+    // ---- 2. this thread's nonzeros [k0, k1) and the first row it meets
+    const int k0 = (tid * nnzt) >> 8;
+    const int k1 = ((tid + 1) * nnzt) >> 8;
+    // Rows ending at or before k0 were closed by earlier threads; thread 0
+    // closes the rows that end before the tile's first nonzero (the first of
+    // them takes the carry into the tile, which is zero here).
+    int r = rows_ending_by(s_re, 0, nrows, k0);
+    int re = s_re[r];
     V acc = V(0);
-    V out[IPT];
-    unsigned ends = 0;
-#pragma unroll
-    for (int it = 0; it < IPT; ++it) {
-        const bool valid = dt + it < nitems;
-        if (valid && k >= re) {  // row r has no nonzero left: its end is next
-            out[it] = acc;
+    V first_val = V(0);
+    int first_pos = INT_MIN;  // slot of the first closed row's last nonzero
+    bool ended = tid == 0 && r > 0;
+    if (ended) first_pos = -1;
+    for (int k = k0; k < k1; ++k) {
+        if constexpr (F64) acc = fma(s_a[k + sh], s_b[k + sh], acc);
+        else acc += s_a[k + sh];
+        if (re == k + 1) {  // row r ends after nonzero k; empty rows may follow it
+            if (!ended) {
+                ended = true;
+                first_val = acc;
+                first_pos = k;
+            } else {
+                s_a[k + sh] = acc;  // only this thread touches slot k
+            }
             acc = V(0);
-            ends |= 1u << it;
             ++r;
-            re = r < nrows ? s_re[r] - j0 : INT_MAX;
-        } else if (valid) {
-            if constexpr (F64) acc = fma(s_a[k + sh], s_b[k + sh], acc);
-            else acc += s_a[k + sh];
-            ++k;
+            re = s_re[r];
+            if (re == k + 1) {  // skip the empty rows in one search
+                r = rows_ending_by(s_re, r, nrows, k + 1);
+                re = s_re[r];
+            }
         }
     }
 
-    // ---- 3. segmented inclusive scan of (row end seen, running sum)
+    // ---- 3. segmented inclusive scan of (row closed, running sum)
     V v = acc;
-    int f = ends != 0;
+    int f = ended;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         if (!__any_sync(0xffffffffu, !f && lane >= off)) break;
@@ -255,13 +271,22 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         sm.warp_sum[warp] = v;
         sm.warp_flag[warp] = f;
     }
-    __syncthreads();  // also: every thread is done reading the staged tile
-    if (tid == 0) {
-        V run = V(0);
-        for (int w = 0; w < kWarps; ++w) {
-            sm.warp_prefix[w] = run;
-            run = sm.warp_flag[w] ? sm.warp_sum[w] : run + sm.warp_sum[w];
+    __syncthreads();
+    if (warp == 0) {  // segmented exclusive scan over the warps' totals
+        V ws = lane < kWarps ? sm.warp_sum[lane] : V(0);
+        int wf = lane < kWarps ? sm.warp_flag[lane] : 1;
+#pragma unroll
+        for (int off = 1; off < kWarps; off <<= 1) {
+            if (!__any_sync(0xffffffffu, !wf && lane >= off && lane < kWarps)) break;
+            const V pv = __shfl_up_sync(0xffffffffu, ws, off);
+            const int pf = __shfl_up_sync(0xffffffffu, wf, off);
+            if (lane >= off && !wf) {
+                ws = pv + ws;
+                wf = pf;
+            }
         }
+        const V ex = __shfl_up_sync(0xffffffffu, ws, 1);
+        if (lane < kWarps) sm.warp_prefix[lane] = lane == 0 ? V(0) : ex;
     }
     __syncthreads();
     const V wprefix = sm.warp_prefix[warp];
@@ -271,35 +296,21 @@ merge_path_spmv_kernel(const MPParams<V> p) {
     }
     V carry_in = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) carry_in = wprefix;
-    {
-        bool first = true;
-        int rr = r_first;
-#pragma unroll
-        for (int it = 0; it < IPT; ++it) {
-            if ((ends >> it) & 1u) {
-                V s = out[it];
-                if (first) s = carry_in + s;
-                first = false;
-                s_a[rr++] = s;
-            }
-        }
-    }
+    if (first_pos >= 0) s_a[first_pos + sh] = carry_in + first_val;
     __syncthreads();
 
-    // ---- 4. rows that start and end in this tile
+    // ---- 4. rows that start and end in this tile: the sum sits in the slot
+    // of the row's last nonzero in the tile (no nonzero here: the sum is 0)
     const int32_t rp_i0 = p.row_ptr[i0];
     const bool head_cut = nrows > 0 && rp_i0 < j0;
-    for (int q = tid + (head_cut ? 1 : 0); q < nrows; q += kThreads) {
-        const int row = i0 + q;
-        p.y[row] = finish_row(s_a[q], p.alpha, p.beta, p.mode, p.y, row);
-    }
-
-    // ---- cut rows: store partials and count arrivals
-    if (tid == 0) {
-        sm.run_finish[0] = 0;
-        if (head_cut) {
+    for (int q = tid; q < nrows; q += kThreads) {
+        const int e = s_re[q];
+        const int ep = q == 0 ? 0 : s_re[q - 1];
+        const V s = e > ep ? s_a[e - 1 + sh] : V(0);
+        if (q == 0 && head_cut) {
+            sm.run_finish[0] = 0;
             const long long first = ((long long)rp_i0 + i0) / T;
-            p.head_partial[tile] = s_a[0];
+            p.head_partial[tile] = s;
             __threadfence();
             const int before = atomicAdd(p.arrivals + tile, 1);
             if (before == (int)(tile - first)) {
@@ -309,12 +320,18 @@ merge_path_spmv_kernel(const MPParams<V> p) {
                 sm.run_first[0] = first;
                 sm.run_last[0] = tile;
             }
+        } else {
+            const int row = i0 + q;
+            p.y[row] = finish_row(s, p.alpha, p.beta, p.mode, p.y, row);
         }
     }
+    if (tid == 0 && !head_cut) sm.run_finish[0] = 0;
+
+    // ---- the row open at the tile's end
     if (tid == kThreads - 1) {
         sm.run_finish[1] = 0;
         if (i1 < p.m) {
-            const int32_t rp_i1 = nrows > 0 ? s_re[nrows - 1] : rp_i0;
+            const int32_t rp_i1 = nrows > 0 ? s_re[nrows - 1] + j0 : rp_i0;
             if (j1 > max(rp_i1, j0)) {  // the open row has nonzeros in this tile
                 const long long first = ((long long)rp_i1 + i1) / T;
                 const long long last = ((long long)p.row_ptr[i1 + 1] + i1) / T;
@@ -339,7 +356,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
 template <typename V, int IPT, bool VEC>
 cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     if (a.num_tiles <= 0) return cudaSuccess;
-    constexpr size_t smem = dyn_smem_bytes<V, IPT>();
+    constexpr size_t smem = tile_smem_bytes<V, IPT>();
     static unsigned long long configured = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
