@@ -68,9 +68,10 @@ typedef enum {
 /* Options for spmv_plan_create_ex; zero-initialise and set what you need. */
 typedef struct {
     int32_t kernel;           /* spmv_kernel_t; SPMV_KERNEL_AUTO (0) = choose */
-    int32_t items_per_thread; /* merge-path work items per thread; 0 = default
-                                 (11 for fp32, 7 for fp64). Allowed: 5, 7, 9,
-                                 11, 13, 15 */
+    int32_t items_per_thread; /* merge-path work items (rows + nonzeros) per
+                                 thread; a tile is one warp, T = 32 * items.
+                                 0 = default (16 for fp32, 8 for fp64).
+                                 Allowed: 8, 12, 16, 24, 32 */
     int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = default.
                                  Allowed: 32, 64, 128, 256 */
     int32_t long_row_min;     /* rows with at least this many nonzeros count as
@@ -99,7 +100,7 @@ typedef struct {
     int32_t m, n, nnz;
     int32_t dtype;                /* spmv_dtype_t */
     int32_t kernel;               /* spmv_kernel_t actually used */
-    int32_t threads_per_cta;      /* merge-path kernel */
+    int32_t threads_per_tile;     /* merge-path kernel: one warp per tile */
     int32_t items_per_thread;     /* merge-path kernel */
     int32_t rgcsr_group;          /* Row-grouped CSR kernel */
     int64_t items_per_tile;       /* merge-path tile T = threads * items (rows + nonzeros) */
@@ -195,11 +196,10 @@ spmv_status_t spmv_plan_export(spmv_plan_t plan, spmv_export_t what, void *dst, 
  *
  * Arguments as spmv_plan_create plus spmv_execute (device arrays, the
  * caller's stream).  It runs the merge-path kernel with its scratch in one
- * fixed-size array (about 1.8 MB) inside the library's device image, which
+ * fixed-size array (about 7.3 MB) inside the library's device image, which
  * every GPU that loads the library holds until the process exits.  Limit:
- * ceil((m + nnz) / T) <= 65536 tiles, T = 2,816 (fp32) or 1,792 (fp64),
- * i.e. m + nnz up to about 184M (fp32) or 117M (fp64); larger sizes return
- * SPMV_ERR_INVALID_ARG.  The matrix is NOT checked (use spmv_plan_create
+ * ceil((m + nnz) / 1024) <= 262,144 tiles, i.e. m + nnz <= 268,435,456;
+ * larger sizes return SPMV_ERR_INVALID_ARG.  The matrix is NOT checked (use spmv_plan_create
  * once to validate it); invalid indices give undefined results.
  * All calls share the scratch array and each call clears what must start
  * at zero, so calls that overlap on the GPU (two streams, two host threads)

@@ -44,7 +44,7 @@ class RowStats(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32), ("nnz", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("kernel", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("threads_per_tile", ctypes.c_int32),
                 ("items_per_thread", ctypes.c_int32), ("rgcsr_group", ctypes.c_int32),
                 ("items_per_tile", ctypes.c_int64), ("num_tiles", ctypes.c_int64),
                 ("num_long_rows", ctypes.c_int32), ("launches_per_execute", ctypes.c_int32),

@@ -141,9 +141,9 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     if (forced == SPMV_KERNEL_RGCSR || forced == SPMV_KERNEL_LONG_ROWS)
         return fail(SPMV_ERR_UNSUPPORTED, "kernel not built in this version");
     int ipt = opt.items_per_thread ? opt.items_per_thread
-                                   : env_int("SPMV_ITEMS_PER_THREAD", dtype == SPMV_F64 ? 7 : 11);
+                                   : env_int("SPMV_ITEMS_PER_THREAD", merge_path_default_items(dtype));
     if (!merge_path_supported(ipt))
-        return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 5, 7, 9, 11, 13 or 15");
+        return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 8, 12, 16, 24 or 32");
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -292,7 +292,7 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->nnz = p->nnz;
     info->dtype = p->dtype;
     info->kernel = p->kernel;
-    info->threads_per_cta = merge_path_threads();
+    info->threads_per_tile = merge_path_threads();
     info->items_per_thread = p->ipt;
     info->rgcsr_group = p->rgcsr_group;
     info->items_per_tile = p->tile;

@@ -67,7 +67,8 @@ struct MergePathArgs {
 };
 
 bool merge_path_supported(int items_per_thread);
-int merge_path_threads();
+int merge_path_threads();                       // threads per merge-path tile
+int merge_path_default_items(spmv_dtype_t dtype);  // items per thread by default
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int items_per_thread, const MergePathArgs &a,
                                    cudaStream_t stream);
 

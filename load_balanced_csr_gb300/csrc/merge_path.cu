@@ -1,29 +1,35 @@
-// Merge-path CSR SpMV with a fused carry-out fix-up.
+// Merge-path CSR SpMV on warp-sized tiles, with a fused carry-out fix-up.
 //
 // Schedule: "A GPU load-balancing programming model" (Osama, Porumbescu,
 // Owens), section 5.2.1 -- every row end and every nonzero is one unit of
 // work, the m + nnz units are split into equal tiles of T units, and each
 // worker finds where its share starts by a search over (row ends, nonzero
-// indices).  The plan computes the tile splits once (plan_kernels.cu); each
-// CTA takes one tile:
+// indices).  The plan computes the tile splits once (plan_kernels.cu).
 //
-//  1. stage the tile in shared memory: the row ends row_ptr[i0+1 .. i1]
-//     (relative to the tile's first nonzero j0, with a sentinel), and for the
-//     nonzeros j in [j0, j1) either the products vals[j]*x[col[j]] (fp32) or
-//     the values and the gathered x[col[j]] (fp64).  col_idx and vals are
-//     read with 16-byte loads, all issued before the x gathers;
-//  2. the tile's nonzeros are split evenly over the threads (a thread's share
-//     differs from another's by at most one), and each thread walks its
-//     share: a nonzero adds to the running sum; after it, every row that
-//     ends there is closed.  Row ends cost no floating-point work, so every
-//     lane of every warp-wide add or FMA does useful work.  This matters on
-//     GB300: its fp64 unit runs 2 lanes per clock per SM and a warp
-//     instruction costs it the same whether 1 or 32 lanes are active;
-//  3. a segmented scan over the threads adds the sum carried into each
-//     thread's first closed row (it stops as soon as every open segment has
-//     reached its start, so short rows cost one step);
-//  4. a closed row's sum is kept in the slot of its last nonzero, which no
-//     other thread reads; rows are then written to y once, coalesced.
+// Here a tile belongs to one warp (T = 32 * IPL units) and the warps of a
+// CTA never wait for each other, so a stalled warp never holds up its
+// neighbours.  For each tile the warp:
+//
+//  1. copies the tile's col_idx, vals and row ends row_ptr[i0+1 .. i1] into
+//     its own shared-memory region with 16-byte cp.async copies;
+//  2. marks in a bitmap, for every row that has a nonzero in the tile, the
+//     position of its last one;
+//  3. splits the tile's nonzeros over the 32 lanes in runs of Q = the odd
+//     number nearest above nnz/32 (odd, so the lanes' shared-memory reads
+//     hit distinct banks); each lane first gathers x for its whole run into
+//     registers through the read-only path, so all of its gathers are in
+//     flight at once;
+//  4. then adds its run up in order (one fused multiply-add per nonzero)
+//     and, where the bitmap marks a row's last nonzero, closes the row and
+//     keeps its sum in that nonzero's slot (no other lane reads it).  Row
+//     ends cost no floating-point work, so every lane of every warp-wide FMA
+//     does useful work -- this matters on GB300, whose fp64 unit runs 2 lanes
+//     per clock per SM and charges a warp instruction the same for 1 or 32
+//     lanes;
+//  5. a segmented warp scan adds the sum carried into each lane's first
+//     closed row (it stops once every open segment has reached its start);
+//  6. writes the rows that start and end in the tile to y, coalesced.  A
+//     row with no nonzero in the tile contributes 0.
 //
 // Rows cut by a tile boundary ("partial tiles" in the section) are finished
 // without a second kernel and without any waiting: each tile holding part of
@@ -58,43 +64,55 @@ struct MPParams {
     V beta;
     int mode;  // bit0: alpha != 1, bit1: beta != 0
     const int2 *part;
+    long long num_tiles;
     V *tail_partial;
     V *head_partial;
     int32_t *arrivals;
 };
 
-// Shared memory of one tile (n = nonzeros, r = row ends, n + r <= T):
-//   fp32: prod[n + 4] | row_end[r + 1]
-//   fp64: val[n + 4] | xg[n + 4] | row_end[r + 1]
-// With sh <= 3 and n + r <= T this stays below the bound used here.
-template <typename V, int IPT>
-constexpr size_t tile_smem_bytes() {
-    constexpr int T = kThreads * IPT;
-    return (sizeof(V) == 8 ? 16 : 4) * (size_t)(T + 8) + 64;
+// Per-warp shared memory for a tile with n nonzeros and r row ends
+// (n + r <= T), laid out as
+//   col[ns] | val[ns] | row_end[r] | bitmap[(n + 31) / 32 + 2]
+// with ns = (sh + n + 4) & ~3 <= n + 7 slots.  The size grows with n, so
+// it is largest for n = T, r = 0:
+template <typename V, int IPL>
+__host__ __device__ constexpr int warp_region_bytes() {
+    constexpr int T = 32 * IPL;
+    constexpr int per_nnz = sizeof(int) + sizeof(V);
+    return ((per_nnz * (T + 8) + 4 * (T / 32 + 8)) + 15) & ~15;
 }
 
-// First row in [lo, hi) whose end is after position k (s_re ascends; the
-// sentinel s_re[hi] is larger than any position).
-__device__ __forceinline__ int rows_ending_by(const int *s_re, int lo, int hi, int k) {
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_re[mid] <= k) lo = mid + 1;
-        else hi = mid;
+// ---------------------------------------------------------------- cp.async
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_small(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Copy elements [b, e) of a global array into shared memory (element b at
+// dst), b a multiple of 4.  VEC: 16-byte chunks (the array is 16-byte
+// aligned) and element-sized copies for the last partial chunk only.
+template <typename E, bool VEC>
+__device__ __forceinline__ void warp_copy(E *dst, const E *src, int b, int e, int lane) {
+    const int n = e - b;
+    if (n <= 0) return;
+    const uint32_t d = smem_addr(dst);
+    if (VEC) {
+        constexpr int EPC = 16 / sizeof(E);
+        const int nfull = n / EPC;
+        for (int c = lane; c < nfull; c += 32) cp_async16(d + 16u * c, src + b + c * EPC);
+        const int done = nfull * EPC;
+        if (lane < n - done) cp_async_small<sizeof(E)>(d + sizeof(E) * (done + lane), src + b + done + lane);
+    } else {
+        for (int q = lane; q < n; q += 32) cp_async_small<sizeof(E)>(d + sizeof(E) * q, src + b + q);
     }
-    return lo;
 }
-
-template <typename V>
-struct TileSmem {
-    V warp_sum[kWarps];
-    int warp_flag[kWarps];
-    V warp_prefix[kWarps];
-    V red[kWarps];
-    long long run_first[2];
-    long long run_last[2];
-    int run_row[2];
-    int run_finish[2];
-};
 
 template <typename V>
 __device__ __forceinline__ V finish_row(V s, V alpha, V beta, int mode, const V *y, int row) {
@@ -106,157 +124,115 @@ __device__ __forceinline__ V finish_row(V s, V alpha, V beta, int mode, const V 
     }
 }
 
-// Sum of the partials of one cut row, by the tile that arrived last.
+// Cut rows: store this tile's partial, count in; the last to arrive adds all
+// partials (tiles first..last-1 as tails, tile last as head) and writes y.
+// Called by the whole warp; `lane_with_value` holds the partial.
 template <typename V>
-__device__ void finish_cut_row(V *red, int32_t row, long long first_tile, long long last_tile,
-                               const MPParams<V> &p) {
-    const int tid = threadIdx.x;
+__device__ void cut_row(const MPParams<V> &p, int lane, int lane_with_value, V partial, bool as_head, long long me,
+                        int row, long long first, long long last) {
+    int finisher = 0;
+    if (lane == lane_with_value) {
+        if (as_head) p.head_partial[me] = partial;
+        else p.tail_partial[me] = partial;
+        __threadfence();
+        const int before = atomicAdd(p.arrivals + last, 1);
+        finisher = before == (int)(last - first);
+        if (finisher) __threadfence();
+    }
+    if (!__shfl_sync(0xffffffffu, finisher, lane_with_value)) return;
     V s = V(0);
-    for (long long t = first_tile + tid; t < last_tile; t += kThreads) s += __ldcg(p.tail_partial + t);
+    for (long long t = first + lane; t < last; t += 32) s += __ldcg(p.tail_partial + t);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if ((tid & 31) == 0) red[tid >> 5] = s;
-    __syncthreads();
-    if (tid == 0) {
-        V total = red[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) total += red[w];
-        total += __ldcg(p.head_partial + last_tile);
-        p.y[row] = finish_row(total, p.alpha, p.beta, p.mode, p.y, row);
-        p.arrivals[last_tile] = 0;  // ready for the next product
+    if (lane == 0) {
+        s += __ldcg(p.head_partial + last);
+        p.y[row] = finish_row(s, p.alpha, p.beta, p.mode, p.y, row);
+        p.arrivals[last] = 0;  // ready for the next product
     }
-    __syncthreads();
 }
 
-template <typename V, int IPT, bool VEC>
+template <typename V, int IPL, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 merge_path_spmv_kernel(const MPParams<V> p) {
     constexpr bool F64 = sizeof(V) == 8;
-    constexpr int T = kThreads * IPT;
+    constexpr int T = 32 * IPL;
     extern __shared__ __align__(16) unsigned char dsm[];
-    __shared__ TileSmem<V> sm;
 
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const long long tile = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const long long tile = (long long)blockIdx.x * kWarps + warp;
+    if (tile >= p.num_tiles) return;  // warps never wait for each other
 
     const int2 c0 = p.part[tile];
     const int2 c1 = p.part[tile + 1];
     const int i0 = c0.x, j0 = c0.y, i1 = c1.x, j1 = c1.y;
     const int nrows = i1 - i0;
     const int nnzt = j1 - j0;
-    const int base = VEC ? (j0 & ~3) : j0;  // staged nonzero g sits at index g - base
-    const int sh = j0 - base;               // tile nonzero k sits at index k + sh
-    const int nslots = (sh + nnzt + 4) & ~3;
-    V *s_a = reinterpret_cast<V *>(dsm);                  // fp32 products / fp64 values
-    V *s_b = F64 ? s_a + nslots : s_a;                    // fp64 gathered x
-    int *s_re = reinterpret_cast<int *>(F64 ? s_b + nslots : s_a + nslots);
+    const int base = j0 & ~3;  // staged nonzero g sits at index g - base
+    const int sh = j0 - base;  // tile nonzero k sits at index k + sh
+    const int ns = (sh + nnzt + 4) & ~3;
+
+    unsigned char *region = dsm + warp * warp_region_bytes<V, IPL>();
+    int *s_col = reinterpret_cast<int *>(region);
+    V *s_val = reinterpret_cast<V *>(s_col + ns);
+    int *s_re = reinterpret_cast<int *>(s_val + ns);  // absolute row ends
+    unsigned *s_bm = reinterpret_cast<unsigned *>(s_re + nrows);
+    const int nwords = (nnzt + 31) >> 5;
 
     // ---- 1. stage
-    for (int r = tid; r < nrows; r += kThreads) s_re[r] = ld_stream(p.row_ptr + i0 + 1 + r) - j0;
-    if (tid == 0) s_re[nrows] = INT_MAX;
-    if (VEC) {
-        constexpr int CH = ((T + 6) / 4 + kThreads - 1) / kThreads;
-        const int nch = (j1 - base + 3) >> 2;
-        int4 cc[CH];
-        V vv[CH][4];
-#pragma unroll
-        for (int u = 0; u < CH; ++u) {
-            const int c = tid + u * kThreads;
-            const int g = base + 4 * c;
-            if (c < nch && g + 4 <= p.nnz) {
-                cc[u] = ld_stream(reinterpret_cast<const int4 *>(p.col_idx + g));
-                if constexpr (F64) {
-                    const double2 v01 = ld_stream(reinterpret_cast<const double2 *>(p.vals + g));
-                    const double2 v23 = ld_stream(reinterpret_cast<const double2 *>(p.vals + g) + 1);
-                    vv[u][0] = v01.x; vv[u][1] = v01.y; vv[u][2] = v23.x; vv[u][3] = v23.y;
-                } else {
-                    const float4 v = ld_stream(reinterpret_cast<const float4 *>(p.vals + g));
-                    vv[u][0] = v.x; vv[u][1] = v.y; vv[u][2] = v.z; vv[u][3] = v.w;
-                }
-            } else if (c < nch) {  // the array's last, partial chunk
-                int ci[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool ok = g + e < j1;
-                    ci[e] = ok ? ld_stream(p.col_idx + g + e) : 0;
-                    vv[u][e] = ok ? ld_stream(p.vals + g + e) : V(0);
-                }
-                cc[u] = make_int4(ci[0], ci[1], ci[2], ci[3]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < CH; ++u) {
-            const int c = tid + u * kThreads;
-            if (c < nch) {
-                const int g = base + 4 * c;
-                const int ci[4] = {cc[u].x, cc[u].y, cc[u].z, cc[u].w};
-                V xv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) xv[e] = (g + e >= j0 && g + e < j1) ? ld_gather(p.x + ci[e]) : V(0);
-                if constexpr (F64) {
-                    reinterpret_cast<double2 *>(s_a)[2 * c] = make_double2(vv[u][0], vv[u][1]);
-                    reinterpret_cast<double2 *>(s_a)[2 * c + 1] = make_double2(vv[u][2], vv[u][3]);
-                    reinterpret_cast<double2 *>(s_b)[2 * c] = make_double2(xv[0], xv[1]);
-                    reinterpret_cast<double2 *>(s_b)[2 * c + 1] = make_double2(xv[2], xv[3]);
-                } else {
-                    reinterpret_cast<float4 *>(s_a)[c] =
-                        make_float4(vv[u][0] * xv[0], vv[u][1] * xv[1], vv[u][2] * xv[2], vv[u][3] * xv[3]);
-                }
-            }
-        }
-    } else {
-        for (int k = tid; k < nnzt; k += kThreads) {
-            const V xv = ld_gather(p.x + ld_stream(p.col_idx + j0 + k));
-            const V v = ld_stream(p.vals + j0 + k);
-            if constexpr (F64) {
-                s_a[k] = v;
-                s_b[k] = xv;
-            } else {
-                s_a[k] = v * xv;
-            }
-        }
-    }
-    __syncthreads();
+    warp_copy<int, VEC>(s_col, p.col_idx, base, j1, lane);
+    warp_copy<V, VEC>(s_val, p.vals, base, j1, lane);
+    for (int w = lane; w < nwords + 2; w += 32) s_bm[w] = 0u;  // two spare words
+    for (int r = lane; r < nrows; r += 32) s_re[r] = ld_stream(p.row_ptr + i0 + 1 + r);
+    cp_async_wait_all();
+    __syncwarp();
 
-    // ---- 2. this thread's nonzeros [k0, k1) and the first row it meets
-    const int k0 = (tid * nnzt) >> 8;
-    const int k1 = ((tid + 1) * nnzt) >> 8;
-    // Rows ending at or before k0 were closed by earlier threads; thread 0
-    // closes the rows that end before the tile's first nonzero (the first of
-    // them takes the carry into the tile, which is zero here).
-    int r = rows_ending_by(s_re, 0, nrows, k0);
-    int re = s_re[r];
+    // ---- 2. mark each row's last nonzero in the tile
+    for (int r = lane; r < nrows; r += 32) {
+        const int e = s_re[r] - j0;
+        const int ep = r == 0 ? 0 : s_re[r - 1] - j0;
+        if (e > ep) atomicOr(s_bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
+    }
+
+    __syncwarp();
+
+    // ---- 3. this lane's run of nonzeros [k0, k0 + q) and its x values
+    int Q = (nnzt + 31) >> 5;
+    Q |= 1;  // odd stride: lanes read distinct banks
+    const int k0 = min(lane * Q, nnzt);
+    const int run = min(Q, nnzt - k0);
+    V xr[IPL + 1];
+#pragma unroll
+    for (int i = 0; i <= IPL; ++i) xr[i] = i < run ? ld_gather(p.x + s_col[k0 + i + sh]) : V(0);
+    // bits of this run: bit i set when nonzero k0 + i is a row's last one
+    const unsigned long long two = ((unsigned long long)s_bm[(k0 >> 5) + 1] << 32) | s_bm[k0 >> 5];
+    unsigned long long bits = two >> (k0 & 31);
+
+    // ---- 4. add the run up, closing rows where the bitmap says
     V acc = V(0);
     V first_val = V(0);
-    int first_pos = INT_MIN;  // slot of the first closed row's last nonzero
-    bool ended = tid == 0 && r > 0;
-    if (ended) first_pos = -1;
-    for (int k = k0; k < k1; ++k) {
-        if constexpr (F64) acc = fma(s_a[k + sh], s_b[k + sh], acc);
-        else acc += s_a[k + sh];
-        if (re == k + 1) {  // row r ends after nonzero k; empty rows may follow it
-            if (!ended) {
-                ended = true;
-                first_val = acc;
-                first_pos = k;
-            } else {
-                s_a[k + sh] = acc;  // only this thread touches slot k
+    int first_pos = -1;
+#pragma unroll
+    for (int i = 0; i <= IPL; ++i) {
+        if (i < run) {
+            const int k = k0 + i;
+            acc = fma(s_val[k + sh], xr[i], acc);
+            if (bits & 1ull) {
+                if (first_pos < 0) {
+                    first_val = acc;
+                    first_pos = k;
+                } else {
+                    s_val[k + sh] = acc;
+                }
+                acc = V(0);
             }
-            acc = V(0);
-            ++r;
-            re = s_re[r];
-            if (re == k + 1) {  // skip the empty rows in one search
-                r = rows_ending_by(s_re, r, nrows, k + 1);
-                re = s_re[r];
-            }
+            bits >>= 1;
         }
     }
 
-    // ---- 3. segmented inclusive scan of (row closed, running sum)
+    // ---- 5. segmented inclusive scan of (row closed, running sum)
     V v = acc;
-    int f = ended;
+    int f = first_pos >= 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         if (!__any_sync(0xffffffffu, !f && lane >= off)) break;
@@ -267,101 +243,49 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             f = pf;
         }
     }
-    if (lane == 31) {
-        sm.warp_sum[warp] = v;
-        sm.warp_flag[warp] = f;
-    }
-    __syncthreads();
-    if (warp == 0) {  // segmented exclusive scan over the warps' totals
-        V ws = lane < kWarps ? sm.warp_sum[lane] : V(0);
-        int wf = lane < kWarps ? sm.warp_flag[lane] : 1;
-#pragma unroll
-        for (int off = 1; off < kWarps; off <<= 1) {
-            if (!__any_sync(0xffffffffu, !wf && lane >= off && lane < kWarps)) break;
-            const V pv = __shfl_up_sync(0xffffffffu, ws, off);
-            const int pf = __shfl_up_sync(0xffffffffu, wf, off);
-            if (lane >= off && !wf) {
-                ws = pv + ws;
-                wf = pf;
-            }
-        }
-        const V ex = __shfl_up_sync(0xffffffffu, ws, 1);
-        if (lane < kWarps) sm.warp_prefix[lane] = lane == 0 ? V(0) : ex;
-    }
-    __syncthreads();
-    const V wprefix = sm.warp_prefix[warp];
-    V incl = v;
-    if (warp > 0 && __any_sync(0xffffffffu, !f)) {
-        if (!f) incl = wprefix + v;
-    }
-    V carry_in = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) carry_in = wprefix;
-    if (first_pos >= 0) s_a[first_pos + sh] = carry_in + first_val;
-    __syncthreads();
+    V carry_in = __shfl_up_sync(0xffffffffu, v, 1);
+    if (lane == 0) carry_in = V(0);
+    if (first_pos >= 0) s_val[first_pos + sh] = carry_in + first_val;
+    __syncwarp();
 
-    // ---- 4. rows that start and end in this tile: the sum sits in the slot
-    // of the row's last nonzero in the tile (no nonzero here: the sum is 0)
+    // ---- 6. rows that start and end in this tile
     const int32_t rp_i0 = p.row_ptr[i0];
     const bool head_cut = nrows > 0 && rp_i0 < j0;
-    for (int q = tid; q < nrows; q += kThreads) {
-        const int e = s_re[q];
-        const int ep = q == 0 ? 0 : s_re[q - 1];
-        const V s = e > ep ? s_a[e - 1 + sh] : V(0);
+    V head_val = V(0);
+    for (int q = lane; q < nrows; q += 32) {
+        const int e = s_re[q] - j0;
+        const int ep = q == 0 ? 0 : s_re[q - 1] - j0;
+        const V s = e > ep ? s_val[e - 1 + sh] : V(0);
         if (q == 0 && head_cut) {
-            sm.run_finish[0] = 0;
-            const long long first = ((long long)rp_i0 + i0) / T;
-            p.head_partial[tile] = s;
-            __threadfence();
-            const int before = atomicAdd(p.arrivals + tile, 1);
-            if (before == (int)(tile - first)) {
-                __threadfence();
-                sm.run_finish[0] = 1;
-                sm.run_row[0] = i0;
-                sm.run_first[0] = first;
-                sm.run_last[0] = tile;
-            }
+            head_val = s;
         } else {
             const int row = i0 + q;
             p.y[row] = finish_row(s, p.alpha, p.beta, p.mode, p.y, row);
         }
     }
-    if (tid == 0 && !head_cut) sm.run_finish[0] = 0;
+    if (head_cut)
+        cut_row<V>(p, lane, 0, head_val, true, tile, i0, ((long long)rp_i0 + i0) / T, tile);
 
     // ---- the row open at the tile's end
-    if (tid == kThreads - 1) {
-        sm.run_finish[1] = 0;
-        if (i1 < p.m) {
-            const int32_t rp_i1 = nrows > 0 ? s_re[nrows - 1] + j0 : rp_i0;
-            if (j1 > max(rp_i1, j0)) {  // the open row has nonzeros in this tile
-                const long long first = ((long long)rp_i1 + i1) / T;
-                const long long last = ((long long)p.row_ptr[i1 + 1] + i1) / T;
-                p.tail_partial[tile] = incl;
-                __threadfence();
-                const int before = atomicAdd(p.arrivals + last, 1);
-                if (before == (int)(last - first)) {
-                    __threadfence();
-                    sm.run_finish[1] = 1;
-                    sm.run_row[1] = i1;
-                    sm.run_first[1] = first;
-                    sm.run_last[1] = last;
-                }
-            }
+    if (i1 < p.m) {
+        const int32_t rp_i1 = nrows > 0 ? s_re[nrows - 1] : rp_i0;
+        if (j1 > max(rp_i1, j0)) {  // it has nonzeros in this tile
+            const long long first = ((long long)rp_i1 + i1) / T;
+            const long long last = ((long long)p.row_ptr[i1 + 1] + i1) / T;
+            cut_row<V>(p, lane, 31, v, false, tile, i1, first, last);
         }
     }
-    __syncthreads();
-    if (sm.run_finish[0]) finish_cut_row<V>(sm.red, sm.run_row[0], sm.run_first[0], sm.run_last[0], p);
-    if (sm.run_finish[1]) finish_cut_row<V>(sm.red, sm.run_row[1], sm.run_first[1], sm.run_last[1], p);
 }
 
-template <typename V, int IPT, bool VEC>
+template <typename V, int IPL, bool VEC>
 cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     if (a.num_tiles <= 0) return cudaSuccess;
-    constexpr size_t smem = tile_smem_bytes<V, IPT>();
+    constexpr size_t smem = (size_t)kWarps * warp_region_bytes<V, IPL>();
     static unsigned long long configured = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (!((configured >> (dev & 63)) & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(merge_path_spmv_kernel<V, IPT, VEC>,
+        cudaError_t e = cudaFuncSetAttribute(merge_path_spmv_kernel<V, IPL, VEC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured |= 1ull << (dev & 63);
@@ -378,41 +302,42 @@ cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     p.beta = static_cast<V>(a.beta);
     p.mode = (p.alpha != V(1) ? 1 : 0) | (p.beta != V(0) ? 2 : 0);
     p.part = a.part;
+    p.num_tiles = a.num_tiles;
     p.tail_partial = static_cast<V *>(a.tail_partial);
     p.head_partial = static_cast<V *>(a.head_partial);
     p.arrivals = a.arrivals;
-    merge_path_spmv_kernel<V, IPT, VEC><<<(unsigned)a.num_tiles, kThreads, smem, stream>>>(p);
+    const long long grid = (a.num_tiles + kWarps - 1) / kWarps;
+    merge_path_spmv_kernel<V, IPL, VEC><<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 template <typename V, bool VEC>
-cudaError_t launch_ipt(int ipt, const MergePathArgs &a, cudaStream_t stream) {
-    switch (ipt) {
-    case 5: return launch_typed<V, 5, VEC>(a, stream);
-    case 7: return launch_typed<V, 7, VEC>(a, stream);
-    case 9: return launch_typed<V, 9, VEC>(a, stream);
-    case 11: return launch_typed<V, 11, VEC>(a, stream);
-    case 13: return launch_typed<V, 13, VEC>(a, stream);
-    case 15: return launch_typed<V, 15, VEC>(a, stream);
+cudaError_t launch_ipl(int ipl, const MergePathArgs &a, cudaStream_t stream) {
+    switch (ipl) {
+    case 8: return launch_typed<V, 8, VEC>(a, stream);
+    case 12: return launch_typed<V, 12, VEC>(a, stream);
+    case 16: return launch_typed<V, 16, VEC>(a, stream);
+    case 24: return launch_typed<V, 24, VEC>(a, stream);
+    case 32: return launch_typed<V, 32, VEC>(a, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-bool merge_path_supported(int ipt) {
-    return ipt == 5 || ipt == 7 || ipt == 9 || ipt == 11 || ipt == 13 || ipt == 15;
-}
+bool merge_path_supported(int ipl) { return ipl == 8 || ipl == 12 || ipl == 16 || ipl == 24 || ipl == 32; }
 
-int merge_path_threads() { return kThreads; }
+int merge_path_threads() { return 32; }
 
-cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipt, const MergePathArgs &a, cudaStream_t stream) {
-    // 16-byte staging needs col_idx and vals 16-byte aligned
+int merge_path_default_items(spmv_dtype_t dtype) { return dtype == SPMV_F64 ? 8 : 16; }
+
+cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
+    // 16-byte copies need col_idx and vals 16-byte aligned
     const bool vec = (reinterpret_cast<uintptr_t>(a.col_idx) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.vals) % 16 == 0);
     if (dtype == SPMV_F64)
-        return vec ? launch_ipt<double, true>(ipt, a, stream) : launch_ipt<double, false>(ipt, a, stream);
-    return vec ? launch_ipt<float, true>(ipt, a, stream) : launch_ipt<float, false>(ipt, a, stream);
+        return vec ? launch_ipl<double, true>(ipl, a, stream) : launch_ipl<double, false>(ipl, a, stream);
+    return vec ? launch_ipl<float, true>(ipl, a, stream) : launch_ipl<float, false>(ipl, a, stream);
 }
 
 }  // namespace lbcsr

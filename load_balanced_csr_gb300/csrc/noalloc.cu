@@ -18,10 +18,10 @@
 namespace lbcsr {
 namespace {
 
-// Up to this many merge-path tiles: m + nnz <= kNoAllocMaxTiles * T, where T
-// = 256 * items per thread (2,816 for fp32, 1,792 for fp64), i.e. about 184M
-// (fp32) or 117M (fp64) rows plus nonzeros.
-constexpr int64_t kNoAllocMaxTiles = 65536;
+// Tiles of 1,024 units (32 items per lane), up to this many of them:
+// m + nnz <= 262,144 * 1,024 = 268,435,456 rows plus nonzeros.
+constexpr int kNoAllocItemsPerLane = 32;
+constexpr int64_t kNoAllocMaxTiles = 262144;
 
 struct NoAllocLayout {
     int2 part[kNoAllocMaxTiles + 1];
@@ -30,7 +30,7 @@ struct NoAllocLayout {
     int32_t arrivals[kNoAllocMaxTiles];
 };
 
-// Scratch of spmv_execute_noalloc (about 1.8 MB).  Host code must not pass
+// Scratch of spmv_execute_noalloc (about 7.3 MB).  Host code must not pass
 // this name to a kernel: on the host it is only a stand-in for the symbol.
 // The device address comes from cudaGetSymbolAddress, once per device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocLayout)];
@@ -54,7 +54,7 @@ extern "C" spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz,
     if (!row_ptr || !y) return SPMV_ERR_INVALID_ARG;
     if (nnz > 0 && (!col_idx || !vals || !x)) return SPMV_ERR_INVALID_ARG;
 
-    const int ipt = dtype == SPMV_F64 ? 7 : 11;
+    const int ipt = kNoAllocItemsPerLane;
     const int64_t T = (int64_t)merge_path_threads() * ipt;
     const int64_t P = ((int64_t)m + nnz + T - 1) / T;
     if (P > kNoAllocMaxTiles) return SPMV_ERR_INVALID_ARG;  // beyond the fixed scratch

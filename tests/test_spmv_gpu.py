@@ -54,12 +54,13 @@ def test_random_matrices(dtype, alpha, beta, kernel):
         assert_close_to_oracle(A, x, y, alpha, beta, y0, label=f"{kernel} {dtype} m={m}")
 
 
-@pytest.mark.parametrize("ipt", [5, 7, 9, 11, 13, 15])
+@pytest.mark.parametrize("ipt", [8, 12, 16, 24, 32])
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
 def test_items_per_thread_variants(ipt, dtype):
     A, x, y0 = inputs(30000, 25000, 15, ipt, dtype)
     y, info = run(A, x, y0, 1.5, 0.5, kernel="merge_path", ipt=ipt)
-    assert info["items_per_thread"] == ipt and info["items_per_tile"] == 256 * ipt
+    assert info["items_per_thread"] == ipt
+    assert info["items_per_tile"] == info["threads_per_tile"] * ipt
     assert_close_to_oracle(A, x, y, 1.5, 0.5, y0, label=f"ipt={ipt}")
 
 
@@ -111,17 +112,24 @@ def test_degenerate_shapes(dtype):
         assert_close_to_oracle(A, x, y, 1.0, 0.0, None, label=f"1x1 {kernel}")
 
 
-@pytest.mark.parametrize("pattern", ["leading_trailing_empty", "tile_aligned_rows", "alternating"])
+@pytest.mark.parametrize("pattern", ["leading_trailing_empty", "tile_aligned_rows", "alternating",
+                                     "empty_block"])
 def test_adversarial_row_patterns(pattern):
-    T = 256 * 7
+    T = 32 * 8  # fp64 default tile
     if pattern == "leading_trailing_empty":
         lens = np.full(30000, 4, np.int32)
         lens[:5000] = 0
         lens[-7000:] = 0
     elif pattern == "tile_aligned_rows":
         lens = np.full(60, T - 1, np.int32)  # each row plus its end fills a tile exactly
-    else:
+    elif pattern == "alternating":
         lens = np.tile(np.array([0, 2 * T + 5, 0, 1], np.int32), 50)
+    else:  # a block of empty rows longer than several tiles, between two rows
+        lens = np.zeros(20000, np.int32)
+        lens[0] = 7
+        lens[3] = 2 * T
+        lens[19000] = 5
+        lens[-1] = 3
     A = synth.fill_random(lens, 100000, dist=synth.DIST_NORMAL, seed=9, dtype="f64")
     x = synth.vector(A.n, synth.DIST_NORMAL, 9, synth.STREAM_X, "f64")
     y0 = synth.vector(A.m, synth.DIST_NORMAL, 9, synth.STREAM_Y, "f64")
@@ -161,7 +169,7 @@ def test_deterministic_and_reusable_plan():
         np.testing.assert_array_equal(y.cpu().numpy(), outs[0] * 2)
 
 
-@pytest.mark.parametrize("T_ipt", [5, 7, 13])
+@pytest.mark.parametrize("T_ipt", [8, 16, 32])
 def test_partition_bit_exact(T_ipt):
     import load_balanced_csr_gb300 as lb
     for seed, lens in enumerate([

@@ -65,8 +65,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     import load_balanced_csr_gb300 as lb
     L = lb.lib()
     fake = ctypes.c_void_p(0x1000)
-    # 65536 tiles of 1,792 units (fp64) is the limit: one more unit is refused
-    m = 65536 * 1792 + 1
+    # 262,144 tiles of 1,024 units is the limit: one more unit is refused
+    m = 262144 * 1024 + 1
     assert L.spmv_execute_noalloc(m, 1, 0, fake, None, None, 1, 1.0, None, 0.0, fake, None) == 1
     assert L.spmv_execute_noalloc(-1, 1, 0, fake, None, None, 0, 1.0, None, 0.0, fake, None) == 1
     assert L.spmv_execute_noalloc(0, 1, 0, None, None, None, 0, 1.0, None, 0.0, None, None) == 0
