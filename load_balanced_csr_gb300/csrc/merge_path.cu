@@ -1,4 +1,5 @@
-// Merge-path CSR SpMV on warp-sized tiles, with a fused carry-out fix-up.
+// Merge-path CSR SpMV: persistent warps over warp-sized tiles, with a fused
+// carry-out fix-up.
 //
 // Schedule: "A GPU load-balancing programming model" (Osama, Porumbescu,
 // Owens), section 5.2.1 -- every row end and every nonzero is one unit of
@@ -6,40 +7,42 @@
 // worker finds where its share starts by a search over (row ends, nonzero
 // indices).  The plan computes the tile splits once (plan_kernels.cu).
 //
-// Here a tile belongs to one warp (T = 32 * IPL units) and the warps of a
-// CTA never wait for each other, so a stalled warp never holds up its
-// neighbours.  For each tile the warp:
+// A tile here is T = 32 * IPL units and belongs to one warp.  Each warp owns
+// a contiguous run of tiles (all tiles cost the same, so equal runs balance
+// the GPU) and never waits for another warp.  Per tile it
 //
-//  1. copies the tile's col_idx, vals and row ends row_ptr[i0+1 .. i1] into
-//     its own shared-memory region with 16-byte cp.async copies;
-//  2. marks in a bitmap, for every row that has a nonzero in the tile, the
+//  1. has the tile's col_idx, vals and row ends row_ptr[i0+1 .. i1] copied
+//     into its own shared-memory stage with cp.async -- the next tile's copy
+//     is always in flight while the current one is processed;
+//  2. marks in a bitmap, for every row with a nonzero in the tile, the
 //     position of its last one;
 //  3. splits the tile's nonzeros over the 32 lanes in runs of Q = the odd
-//     number nearest above nnz/32 (odd, so the lanes' shared-memory reads
-//     hit distinct banks); each lane first gathers x for its whole run into
-//     registers through the read-only path, so all of its gathers are in
-//     flight at once;
-//  4. then adds its run up in order (one fused multiply-add per nonzero)
-//     and, where the bitmap marks a row's last nonzero, closes the row and
-//     keeps its sum in that nonzero's slot (no other lane reads it).  Row
-//     ends cost no floating-point work, so every lane of every warp-wide FMA
-//     does useful work -- this matters on GB300, whose fp64 unit runs 2 lanes
-//     per clock per SM and charges a warp instruction the same for 1 or 32
+//     number nearest above nnz/32 (odd, so the lanes' shared-memory reads hit
+//     distinct banks); each lane gathers x for its whole run into registers
+//     through the read-only path, so all its gathers are in flight at once;
+//  4. adds its run up in order (one fused multiply-add per nonzero) and,
+//     where the bitmap marks a row's last nonzero, closes the row and keeps
+//     its sum in that nonzero's slot (no other lane reads it).  Row ends cost
+//     no floating-point work, so every lane of every warp-wide FMA does
+//     useful work -- this matters on GB300, whose fp64 unit runs 2 lanes per
+//     clock per SM and charges a warp instruction the same for 1 or 32
 //     lanes;
 //  5. a segmented warp scan adds the sum carried into each lane's first
 //     closed row (it stops once every open segment has reached its start);
-//  6. writes the rows that start and end in the tile to y, coalesced.  A
-//     row with no nonzero in the tile contributes 0.
+//     the sum still open at the tile's end is carried to the warp's next
+//     tile in a register;
+//  6. writes the finished rows to y, coalesced.  A row with no nonzero in
+//     the tile contributes 0.
 //
-// Rows cut by a tile boundary ("partial tiles" in the section) are finished
-// without a second kernel and without any waiting: each tile holding part of
-// such a row stores its partial sum, then counts itself in on the row's
-// arrival counter; the tile that arrives last (the counter says how many to
-// expect: the tiles from the one holding the row's first nonzero to the one
-// holding its end) adds the partials in tile order with a tree and writes y.
-// The order of the sum does not depend on which tile arrives last, so
-// results are deterministic.  (The CUB implementation the paper compares
-// with runs a separate fix-up step for these rows.)
+// Rows cut by the boundary between two warps' runs ("partial tiles" in the
+// section) are finished without a second kernel and without any waiting:
+// each warp holding part of such a row stores its partial sum, then counts
+// itself in on the row's arrival counter; the warp that arrives last (the
+// counter says how many to expect: the warps from the one holding the row's
+// first nonzero to the one holding its end) adds the partials in warp order
+// with a tree and writes y.  The order of the sum does not depend on which
+// warp arrives last, so results are deterministic.  (The CUB implementation
+// the paper compares with runs a separate fix-up step for these rows.)
 #include <climits>
 
 #include "internal.cuh"
@@ -50,6 +53,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kStages = 2;
 
 template <typename V>
 struct MPParams {
@@ -64,54 +68,129 @@ struct MPParams {
     V beta;
     int mode;  // bit0: alpha != 1, bit1: beta != 0
     const int2 *part;
-    long long num_tiles;
-    V *tail_partial;
-    V *head_partial;
-    int32_t *arrivals;
+    long long num_tiles;  // P
+    long long num_warps;  // W <= P: warps with a run of tiles
+    V *tail_partial;      // per warp
+    V *head_partial;      // per warp
+    int32_t *arrivals;    // per warp, zero between products
 };
 
-// Per-warp shared memory for a tile with n nonzeros and r row ends
-// (n + r <= T), laid out as
-//   col[ns] | val[ns] | row_end[r] | bitmap[(n + 31) / 32 + 2]
-// with ns = (sh + n + 4) & ~3 <= n + 7 slots.  The size grows with n, so
-// it is largest for n = T, r = 0:
+// One stage of a warp's shared memory, for a tile with n nonzeros and r row
+// ends (n + r <= T):
+//   col[ns] | val[ns] | row_ends[rs] | bitmap[(n + 31) / 32 + 2]
+// ns = (sh + n + 4) & ~3 <= n + 7 and rs = (rsh + r + 4) & ~3 <= r + 7
+// slots (sh, rsh < 4 are the alignment shifts of the 16-byte copies).  The
+// size grows with n, so it is largest for n = T, r = 0:
 template <typename V, int IPL>
-__host__ __device__ constexpr int warp_region_bytes() {
+__host__ __device__ constexpr int stage_bytes() {
     constexpr int T = 32 * IPL;
     constexpr int per_nnz = sizeof(int) + sizeof(V);
-    return ((per_nnz * (T + 8) + 4 * (T / 32 + 8)) + 15) & ~15;
+    return ((per_nnz * (T + 8) + 4 * (T / 32 + 16)) + 15) & ~15;
 }
 
 // ---------------------------------------------------------------- cp.async
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// The matrix is read once per product: its copies carry the L2 evict-first
+// hint, and x is gathered with evict-last, so the stream does not push x
+// out of L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
 }
 template <int N>
-__device__ __forceinline__ void cp_async_small(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(N) : "memory");
+__device__ __forceinline__ void cp_async_small(uint32_t dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(N),
+                 "l"(pol)
+                 : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ float gather_keep(const float *p, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ double gather_keep(const double *p, uint64_t pol) {
+    double v;
+    asm volatile("ld.global.nc.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Copy elements [b, e) of a global array into shared memory (element b at
 // dst), b a multiple of 4.  VEC: 16-byte chunks (the array is 16-byte
 // aligned) and element-sized copies for the last partial chunk only.
 template <typename E, bool VEC>
-__device__ __forceinline__ void warp_copy(E *dst, const E *src, int b, int e, int lane) {
+__device__ __forceinline__ void warp_copy(E *dst, const E *src, int b, int e, int lane, uint64_t pol) {
     const int n = e - b;
     if (n <= 0) return;
     const uint32_t d = smem_addr(dst);
     if (VEC) {
         constexpr int EPC = 16 / sizeof(E);
         const int nfull = n / EPC;
-        for (int c = lane; c < nfull; c += 32) cp_async16(d + 16u * c, src + b + c * EPC);
+        for (int c = lane; c < nfull; c += 32) cp_async16(d + 16u * c, src + b + c * EPC, pol);
         const int done = nfull * EPC;
-        if (lane < n - done) cp_async_small<sizeof(E)>(d + sizeof(E) * (done + lane), src + b + done + lane);
+        if (lane < n - done)
+            cp_async_small<sizeof(E)>(d + sizeof(E) * (done + lane), src + b + done + lane, pol);
     } else {
-        for (int q = lane; q < n; q += 32) cp_async_small<sizeof(E)>(d + sizeof(E) * q, src + b + q);
+        for (int q = lane; q < n; q += 32) cp_async_small<sizeof(E)>(d + sizeof(E) * q, src + b + q, pol);
     }
+}
+
+// Where a tile's arrays sit in its stage.
+template <typename V>
+struct StageView {
+    int *col;      // col[k + sh]: the tile's nonzero k
+    V *val;        // val[k + sh]
+    int *re;       // re[r]: absolute end of row i0 + r
+    unsigned *bm;  // bitmap over the tile's nonzeros
+};
+
+template <typename V>
+__device__ __forceinline__ StageView<V> stage_view(unsigned char *stage, int4 t) {
+    const int i0 = t.x, j0 = t.y, i1 = t.z, j1 = t.w;
+    const int sh = j0 & 3;
+    const int ns = (sh + (j1 - j0) + 4) & ~3;
+    const int rsh = (i0 + 1) & 3;
+    const int rs = (rsh + (i1 - i0) + 4) & ~3;
+    StageView<V> v;
+    v.col = reinterpret_cast<int *>(stage);
+    v.val = reinterpret_cast<V *>(v.col + ns);
+    int *re_raw = reinterpret_cast<int *>(v.val + ns);
+    v.re = re_raw + rsh;
+    v.bm = reinterpret_cast<unsigned *>(re_raw + rs);
+    return v;
+}
+
+template <typename V, bool VEC>
+__device__ __forceinline__ void issue_tile(const MPParams<V> &p, unsigned char *stage, int4 t, int lane,
+                                           uint64_t pol) {
+    const StageView<V> v = stage_view<V>(stage, t);
+    const int base = t.y & ~3;
+    warp_copy<int, VEC>(v.col, p.col_idx, base, t.w, lane, pol);
+    warp_copy<V, VEC>(v.val, p.vals, base, t.w, lane, pol);
+    const int rb = (t.x + 1) & ~3;
+    warp_copy<int, VEC>(v.re - ((t.x + 1) - rb), p.row_ptr, rb, t.z + 1, lane, pol);
+}
+
+__device__ __forceinline__ int4 tile_bounds(const int2 *part, long long t) {
+    const int2 a = part[t];
+    const int2 b = part[t + 1];
+    return make_int4(a.x, a.y, b.x, b.y);
 }
 
 template <typename V>
@@ -124,8 +203,12 @@ __device__ __forceinline__ V finish_row(V s, V alpha, V beta, int mode, const V 
     }
 }
 
-// Cut rows: store this tile's partial, count in; the last to arrive adds all
-// partials (tiles first..last-1 as tails, tile last as head) and writes y.
+__device__ __forceinline__ long long warp_of_tile(long long t, long long P, long long W) {
+    return ((t + 1) * W - 1) / P;  // warp w owns tiles [w*P/W, (w+1)*P/W)
+}
+
+// Cut rows: store this warp's partial, count in; the last to arrive adds all
+// partials (warps first..last-1 as tails, warp last as head) and writes y.
 // Called by the whole warp; `lane_with_value` holds the partial.
 template <typename V>
 __device__ void cut_row(const MPParams<V> &p, int lane, int lane_with_value, V partial, bool as_head, long long me,
@@ -154,142 +237,180 @@ __device__ void cut_row(const MPParams<V> &p, int lane, int lane_with_value, V p
 template <typename V, int IPL, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 merge_path_spmv_kernel(const MPParams<V> p) {
-    constexpr bool F64 = sizeof(V) == 8;
     constexpr int T = 32 * IPL;
     extern __shared__ __align__(16) unsigned char dsm[];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const long long tile = (long long)blockIdx.x * kWarps + warp;
-    if (tile >= p.num_tiles) return;  // warps never wait for each other
+    const long long me = (long long)blockIdx.x * kWarps + warp;
+    if (me >= p.num_warps) return;  // warps never wait for each other
+    const long long P = p.num_tiles;
+    const long long W = p.num_warps;
+    const long long t_begin = me * P / W;
+    const long long t_end = (me + 1) * P / W;  // non-empty: W <= P
+    unsigned char *stages = dsm + (size_t)warp * kStages * stage_bytes<V, IPL>();
+    const uint64_t stream_pol = l2_policy_evict_first();
+    const uint64_t x_pol = l2_policy_evict_last();
 
-    const int2 c0 = p.part[tile];
-    const int2 c1 = p.part[tile + 1];
-    const int i0 = c0.x, j0 = c0.y, i1 = c1.x, j1 = c1.y;
-    const int nrows = i1 - i0;
-    const int nnzt = j1 - j0;
-    const int base = j0 & ~3;  // staged nonzero g sits at index g - base
-    const int sh = j0 - base;  // tile nonzero k sits at index k + sh
-    const int ns = (sh + nnzt + 4) & ~3;
+    // the warp's run starts inside a row whose beginning belongs to an earlier warp
+    const int4 first_tile = tile_bounds(p.part, t_begin);
+    bool head_pending = first_tile.x < p.m && p.row_ptr[first_tile.x] < first_tile.y;
 
-    unsigned char *region = dsm + warp * warp_region_bytes<V, IPL>();
-    int *s_col = reinterpret_cast<int *>(region);
-    V *s_val = reinterpret_cast<V *>(s_col + ns);
-    int *s_re = reinterpret_cast<int *>(s_val + ns);  // absolute row ends
-    unsigned *s_bm = reinterpret_cast<unsigned *>(s_re + nrows);
-    const int nwords = (nnzt + 31) >> 5;
-
-    // ---- 1. stage
-    warp_copy<int, VEC>(s_col, p.col_idx, base, j1, lane);
-    warp_copy<V, VEC>(s_val, p.vals, base, j1, lane);
-    for (int w = lane; w < nwords + 2; w += 32) s_bm[w] = 0u;  // two spare words
-    for (int r = lane; r < nrows; r += 32) s_re[r] = ld_stream(p.row_ptr + i0 + 1 + r);
-    cp_async_wait_all();
-    __syncwarp();
-
-    // ---- 2. mark each row's last nonzero in the tile
-    for (int r = lane; r < nrows; r += 32) {
-        const int e = s_re[r] - j0;
-        const int ep = r == 0 ? 0 : s_re[r - 1] - j0;
-        if (e > ep) atomicOr(s_bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
+    int4 cur = first_tile;
+    int4 nxt = make_int4(0, 0, 0, 0);
+    issue_tile<V, VEC>(p, stages, cur, lane, stream_pol);
+    cp_async_commit();
+    if (t_begin + 1 < t_end) {
+        nxt = tile_bounds(p.part, t_begin + 1);
+        issue_tile<V, VEC>(p, stages + stage_bytes<V, IPL>(), nxt, lane, stream_pol);
     }
+    cp_async_commit();
 
-    __syncwarp();
+    V carry = V(0);  // sum of the row open at the previous tile's end
+    for (long long t = t_begin; t < t_end; ++t) {
+        const int s = (int)((t - t_begin) & 1);
+        unsigned char *stage = stages + s * stage_bytes<V, IPL>();
+        const int i0 = cur.x, j0 = cur.y, i1 = cur.z, j1 = cur.w;
+        const int nrows = i1 - i0;
+        const int nnzt = j1 - j0;
+        const int sh = j0 & 3;
+        const StageView<V> sv = stage_view<V>(stage, cur);
+        const int nwords = (nnzt + 31) >> 5;
 
-    // ---- 3. this lane's run of nonzeros [k0, k0 + q) and its x values
-    int Q = (nnzt + 31) >> 5;
-    Q |= 1;  // odd stride: lanes read distinct banks
-    const int k0 = min(lane * Q, nnzt);
-    const int run = min(Q, nnzt - k0);
-    V xr[IPL + 1];
+        cp_async_wait<1>();  // this tile's copies are done (the next tile's may not be)
+        for (int w = lane; w < nwords + 2; w += 32) sv.bm[w] = 0u;
+        __syncwarp();
+        // The carried sum belongs to row i0.  If that row ends before the
+        // tile's first nonzero, it takes the carry and nothing flows on.
+        const bool row0_ends_first = nrows > 0 && sv.re[0] == j0;
+        const V carry_row0 = row0_ends_first ? carry : V(0);
+        if (row0_ends_first) carry = V(0);
+
+        // ---- 2. mark each row's last nonzero in the tile
+        for (int r = lane; r < nrows; r += 32) {
+            const int e = sv.re[r] - j0;
+            const int ep = r == 0 ? 0 : sv.re[r - 1] - j0;
+            if (e > ep) atomicOr(sv.bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
+        }
+        __syncwarp();
+
+        // ---- 3. this lane's run [k0, k0 + run) and its x values
+        const int Q = ((nnzt + 31) >> 5) | 1;
+        const int k0 = min(lane * Q, nnzt);
+        const int run = min(Q, nnzt - k0);
+        V xr[IPL + 1];
 #pragma unroll
-    for (int i = 0; i <= IPL; ++i) xr[i] = i < run ? ld_gather(p.x + s_col[k0 + i + sh]) : V(0);
-    // bits of this run: bit i set when nonzero k0 + i is a row's last one
-    const unsigned long long two = ((unsigned long long)s_bm[(k0 >> 5) + 1] << 32) | s_bm[k0 >> 5];
-    unsigned long long bits = two >> (k0 & 31);
+        for (int i = 0; i <= IPL; ++i) xr[i] = i < run ? gather_keep(p.x + sv.col[k0 + i + sh], x_pol) : V(0);
+        const unsigned long long two = ((unsigned long long)sv.bm[(k0 >> 5) + 1] << 32) | sv.bm[k0 >> 5];
+        unsigned long long bits = two >> (k0 & 31);
 
-    // ---- 4. add the run up, closing rows where the bitmap says
-    V acc = V(0);
-    V first_val = V(0);
-    int first_pos = -1;
+        // ---- 4. add the run up, closing rows where the bitmap says
+        V acc = V(0);
+        V first_val = V(0);
+        int first_pos = -1;
 #pragma unroll
-    for (int i = 0; i <= IPL; ++i) {
-        if (i < run) {
-            const int k = k0 + i;
-            acc = fma(s_val[k + sh], xr[i], acc);
-            if (bits & 1ull) {
-                if (first_pos < 0) {
-                    first_val = acc;
-                    first_pos = k;
-                } else {
-                    s_val[k + sh] = acc;
+        for (int i = 0; i <= IPL; ++i) {
+            if (i < run) {
+                const int k = k0 + i;
+                acc = fma(sv.val[k + sh], xr[i], acc);
+                if (bits & 1ull) {
+                    if (first_pos < 0) {
+                        first_val = acc;
+                        first_pos = k;
+                    } else {
+                        sv.val[k + sh] = acc;
+                    }
+                    acc = V(0);
                 }
-                acc = V(0);
+                bits >>= 1;
             }
-            bits >>= 1;
         }
-    }
 
-    // ---- 5. segmented inclusive scan of (row closed, running sum)
-    V v = acc;
-    int f = first_pos >= 0;
+        // ---- 5. segmented inclusive scan of (row closed, running sum)
+        V v = acc;
+        int f = first_pos >= 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        if (!__any_sync(0xffffffffu, !f && lane >= off)) break;
-        const V pv = __shfl_up_sync(0xffffffffu, v, off);
-        const int pf = __shfl_up_sync(0xffffffffu, f, off);
-        if (lane >= off && !f) {
-            v = pv + v;
-            f = pf;
+        for (int off = 1; off < 32; off <<= 1) {
+            if (!__any_sync(0xffffffffu, !f && lane >= off)) break;
+            const V pv = __shfl_up_sync(0xffffffffu, v, off);
+            const int pf = __shfl_up_sync(0xffffffffu, f, off);
+            if (lane >= off && !f) {
+                v = pv + v;
+                f = pf;
+            }
         }
-    }
-    V carry_in = __shfl_up_sync(0xffffffffu, v, 1);
-    if (lane == 0) carry_in = V(0);
-    if (first_pos >= 0) s_val[first_pos + sh] = carry_in + first_val;
-    __syncwarp();
-
-    // ---- 6. rows that start and end in this tile
-    const int32_t rp_i0 = p.row_ptr[i0];
-    const bool head_cut = nrows > 0 && rp_i0 < j0;
-    V head_val = V(0);
-    for (int q = lane; q < nrows; q += 32) {
-        const int e = s_re[q] - j0;
-        const int ep = q == 0 ? 0 : s_re[q - 1] - j0;
-        const V s = e > ep ? s_val[e - 1 + sh] : V(0);
-        if (q == 0 && head_cut) {
-            head_val = s;
-        } else {
-            const int row = i0 + q;
-            p.y[row] = finish_row(s, p.alpha, p.beta, p.mode, p.y, row);
+        if (__any_sync(0xffffffffu, !f)) {
+            if (!f) v = carry + v;  // the segment reaches back into the previous tile
         }
-    }
-    if (head_cut)
-        cut_row<V>(p, lane, 0, head_val, true, tile, i0, ((long long)rp_i0 + i0) / T, tile);
+        V carry_in = __shfl_up_sync(0xffffffffu, v, 1);
+        if (lane == 0) carry_in = carry;
+        if (first_pos >= 0) sv.val[first_pos + sh] = carry_in + first_val;
+        carry = __shfl_sync(0xffffffffu, v, 31);
+        __syncwarp();
 
-    // ---- the row open at the tile's end
-    if (i1 < p.m) {
-        const int32_t rp_i1 = nrows > 0 ? s_re[nrows - 1] : rp_i0;
-        if (j1 > max(rp_i1, j0)) {  // it has nonzeros in this tile
-            const long long first = ((long long)rp_i1 + i1) / T;
-            const long long last = ((long long)p.row_ptr[i1 + 1] + i1) / T;
-            cut_row<V>(p, lane, 31, v, false, tile, i1, first, last);
+        // ---- 6. finished rows; the warp's first row end may be a cut row
+        const bool cut_head = head_pending && nrows > 0;
+        V head_val = V(0);
+        for (int q = lane; q < nrows; q += 32) {
+            const int e = sv.re[q] - j0;
+            const int ep = q == 0 ? 0 : sv.re[q - 1] - j0;
+            const V sum = e > ep ? sv.val[e - 1 + sh] : (q == 0 ? carry_row0 : V(0));
+            if (q == 0 && cut_head) {
+                head_val = sum;
+            } else {
+                const int row = i0 + q;
+                p.y[row] = finish_row(sum, p.alpha, p.beta, p.mode, p.y, row);
+            }
+        }
+        if (cut_head) {
+            head_pending = false;
+            const long long first = warp_of_tile(((long long)p.row_ptr[i0] + i0) / T, P, W);
+            cut_row<V>(p, lane, 0, head_val, true, me, i0, first, me);
+        }
+        __syncwarp();  // this stage may now be refilled
+
+        // ---- next tile: tile t + 2 goes into this stage
+        cur = nxt;
+        if (t + 2 < t_end) {
+            nxt = tile_bounds(p.part, t + 2);
+            issue_tile<V, VEC>(p, stage, nxt, lane, stream_pol);
+        }
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // ---- the row open at the end of the warp's run, if it has nonzeros here
+    const int4 last_tile = tile_bounds(p.part, t_end - 1);
+    const int ie = last_tile.z, je = last_tile.w;
+    if (ie < p.m) {
+        const int32_t rp_ie = p.row_ptr[ie];
+        if (je > max(rp_ie, first_tile.y)) {
+            const long long first = warp_of_tile(((long long)rp_ie + ie) / T, P, W);
+            const long long last = warp_of_tile(((long long)p.row_ptr[ie + 1] + ie) / T, P, W);
+            cut_row<V>(p, lane, 0, carry, false, me, ie, first, last);
         }
     }
 }
 
+int g_ctas_per_sm[2][33][2][64];  // occupancy per (type, IPL, VEC, device)
+
 template <typename V, int IPL, bool VEC>
 cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     if (a.num_tiles <= 0) return cudaSuccess;
-    constexpr size_t smem = (size_t)kWarps * warp_region_bytes<V, IPL>();
-    static unsigned long long configured = 0;  // one bit per device
+    constexpr size_t smem = (size_t)kWarps * kStages * stage_bytes<V, IPL>();
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!((configured >> (dev & 63)) & 1ull)) {
+    int &per_sm = g_ctas_per_sm[sizeof(V) == 8][IPL][VEC][dev & 63];
+    if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(merge_path_spmv_kernel<V, IPL, VEC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured |= 1ull << (dev & 63);
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, merge_path_spmv_kernel<V, IPL, VEC>, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        per_sm = nb > 0 ? nb : 1;
     }
+    const long long max_warps = (long long)per_sm * device_sm_count() * kWarps;
     MPParams<V> p;
     p.m = a.m;
     p.nnz = a.nnz;
@@ -303,11 +424,12 @@ cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     p.mode = (p.alpha != V(1) ? 1 : 0) | (p.beta != V(0) ? 2 : 0);
     p.part = a.part;
     p.num_tiles = a.num_tiles;
+    p.num_warps = a.num_tiles < max_warps ? a.num_tiles : max_warps;
     p.tail_partial = static_cast<V *>(a.tail_partial);
     p.head_partial = static_cast<V *>(a.head_partial);
     p.arrivals = a.arrivals;
-    const long long grid = (a.num_tiles + kWarps - 1) / kWarps;
-    merge_path_spmv_kernel<V, IPL, VEC><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    const unsigned grid = (unsigned)((p.num_warps + kWarps - 1) / kWarps);
+    merge_path_spmv_kernel<V, IPL, VEC><<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -332,8 +454,9 @@ int merge_path_threads() { return 32; }
 int merge_path_default_items(spmv_dtype_t dtype) { return dtype == SPMV_F64 ? 8 : 16; }
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
-    // 16-byte copies need col_idx and vals 16-byte aligned
-    const bool vec = (reinterpret_cast<uintptr_t>(a.col_idx) % 16 == 0) &&
+    // 16-byte copies need row_ptr, col_idx and vals 16-byte aligned
+    const bool vec = (reinterpret_cast<uintptr_t>(a.row_ptr) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(a.col_idx) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.vals) % 16 == 0);
     if (dtype == SPMV_F64)
         return vec ? launch_ipl<double, true>(ipl, a, stream) : launch_ipl<double, false>(ipl, a, stream);
