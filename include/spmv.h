@@ -213,6 +213,14 @@ spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz, const int3
                                    double alpha, const void *x, double beta, void *y,
                                    spmv_stream_t stream);
 
+/*
+ * Kernel-side failure flags of a plan (HOST *flags; waits for the device).
+ * 0 = no failure.  Bit 0: a kernel's wait for its tile copies ran past its
+ * time limit (about a second); the kernel then stopped that part of the work
+ * instead of waiting forever, so the y of that product is incomplete.
+ */
+spmv_status_t spmv_plan_device_status(spmv_plan_t plan, int32_t *flags);
+
 /* Static text for a status code. */
 const char *spmv_status_string(spmv_status_t status);
 

@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "spmv_plan_destroy": [vp],
             "spmv_plan_info": [vp, ctypes.POINTER(PlanInfo)],
             "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
+            "spmv_plan_device_status": [vp, ctypes.POINTER(i32)],
             "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
         }
         for name, args in sigs.items():
@@ -181,6 +182,12 @@ class Plan:
                         "min_len": s.min_len, "max_len": s.max_len, "n_empty": s.n_empty, "flags": s.flags}
         out["kernel_name"] = KERNEL_NAMES.get(inf.kernel, str(inf.kernel))
         return out
+
+    def device_status(self) -> int:
+        """Kernel-side failure flags (0 = none); waits for the device."""
+        flags = ctypes.c_int32(0)
+        check(lib().spmv_plan_device_status(self._h, ctypes.byref(flags)), "spmv_plan_device_status")
+        return flags.value
 
     def export(self, what: str):
         import numpy as np

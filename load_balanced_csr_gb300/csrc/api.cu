@@ -37,6 +37,7 @@ struct spmv_plan_s {
     void *tail_partial = nullptr;
     void *head_partial = nullptr;
     int32_t *arrivals = nullptr;
+    int32_t *device_error = nullptr;  // set by kernels whose copies time out
 
     spmv_row_stats_t stats{};
 };
@@ -186,6 +187,8 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     off = align_up(off + vs * P, 256);
     const size_t off_arr = off;
     off = align_up(off + sizeof(int32_t) * P, 256);
+    const size_t off_err = off;
+    off = align_up(off + sizeof(int32_t), 256);
     p->arena_bytes = off;
     e = cudaMalloc(&p->arena, p->arena_bytes);
     if (e != cudaSuccess) {
@@ -200,9 +203,10 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     p->tail_partial = base + off_tail;
     p->head_partial = base + off_head;
     p->arrivals = reinterpret_cast<int32_t *>(base + off_arr);
+    p->device_error = reinterpret_cast<int32_t *>(base + off_err);
 
     // ---- analysis: statistics + validity, read back once
-    e = cudaMemsetAsync(p->arrivals, 0, sizeof(int32_t) * P, stream);
+    e = cudaMemsetAsync(p->arrivals, 0, off_err + sizeof(int32_t) - off_arr, stream);
     if (e == cudaSuccess) e = launch_row_stats(m, n, nnz, row_ptr, col_idx, partials, stats_ctas, d_stats, stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(&p->stats, d_stats, sizeof(spmv_row_stats_t), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -263,6 +267,7 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
         a.tail_partial = p->tail_partial;
         a.head_partial = p->head_partial;
         a.arrivals = p->arrivals;
+        a.error = p->device_error;
         e = launch_merge_path_spmv(p->dtype, p->ipt, a, stream);
         break;
     }
@@ -301,6 +306,14 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->launches_per_execute = p->m > 0 ? 1 : 0;
     info->workspace_bytes = (int64_t)p->arena_bytes;
     info->stats = p->stats;
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_plan_device_status(spmv_plan_t p, int32_t *flags) {
+    if (!p || !flags) return fail(SPMV_ERR_INVALID_ARG, "plan or flags is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(flags, p->device_error, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_device_status");
     return SPMV_OK;
 }
 

@@ -64,6 +64,7 @@ struct MergePathArgs {
     void *tail_partial;    // [num_tiles] value type: partial of the row open at a tile's end
     void *head_partial;    // [num_tiles] value type: partial of a split row finished in a tile
     int32_t *arrivals;     // [num_tiles] zero between executions
+    int32_t *error = nullptr;  // device word: bit 0 set if a copy never completed
 };
 
 bool merge_path_supported(int items_per_thread);

@@ -12,8 +12,11 @@
 // the GPU) and never waits for another warp.  Per tile it
 //
 //  1. has the tile's col_idx, vals and row ends row_ptr[i0+1 .. i1] copied
-//     into its own shared-memory stage with cp.async -- the next tile's copy
-//     is always in flight while the current one is processed;
+//     into its own shared-memory stage by the Tensor Memory Accelerator (one
+//     bulk copy per array, issued by one lane, completion signalled on an
+//     mbarrier) -- the next tile's copy is always in flight while the current
+//     one is processed.  A copy must start and end on 16-byte boundaries, so
+//     the up-to-3 elements after the last boundary are loaded by lanes;
 //  2. marks in a bitmap, for every row with a nonzero in the tile, the
 //     position of its last one;
 //  3. splits the tile's nonzeros over the 32 lanes in runs of Q = the odd
@@ -73,6 +76,7 @@ struct MPParams {
     V *tail_partial;      // per warp
     V *head_partial;      // per warp
     int32_t *arrivals;    // per warp, zero between products
+    int32_t *error;       // bit 0 set if a copy never completed (may be null)
 };
 
 // One stage of a warp's shared memory, for a tile with n nonzeros and r row
@@ -87,11 +91,52 @@ __host__ __device__ constexpr int stage_bytes() {
     constexpr int per_nnz = sizeof(int) + sizeof(V);
     return ((per_nnz * (T + 8) + 4 * (T / 32 + 16)) + 15) & ~15;
 }
+// A warp's region: two mbarriers (16 bytes), then its two stages.
+template <typename V, int IPL>
+__host__ __device__ constexpr int warp_region_bytes() {
+    return 16 + kStages * stage_bytes<V, IPL>();
+}
 
-// ---------------------------------------------------------------- cp.async
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+// ---------------------------------------------------------------- TMA bulk copies
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Wait for phase `parity` of a copy barrier, giving up after about a second
+// (2^31 SM clocks) instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - start > (1ll << 31)) return false;
+    return true;
+}
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- cp.async
 // The matrix is read once per product: its copies carry the L2 evict-first
 // hint, and x is gathered with evict-last, so the stream does not push x
 // out of L2.
@@ -105,16 +150,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint64_t pol) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
-                 : "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_small(uint32_t dst, const void *src, uint64_t pol) {
-    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(N),
-                 "l"(pol)
-                 : "memory");
-}
 __device__ __forceinline__ float gather_keep(const float *p, uint64_t pol) {
     float v;
     asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
@@ -124,31 +159,6 @@ __device__ __forceinline__ double gather_keep(const double *p, uint64_t pol) {
     double v;
     asm volatile("ld.global.nc.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v) : "l"(p), "l"(pol));
     return v;
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Copy elements [b, e) of a global array into shared memory (element b at
-// dst), b a multiple of 4.  VEC: 16-byte chunks (the array is 16-byte
-// aligned) and element-sized copies for the last partial chunk only.
-template <typename E, bool VEC>
-__device__ __forceinline__ void warp_copy(E *dst, const E *src, int b, int e, int lane, uint64_t pol) {
-    const int n = e - b;
-    if (n <= 0) return;
-    const uint32_t d = smem_addr(dst);
-    if (VEC) {
-        constexpr int EPC = 16 / sizeof(E);
-        const int nfull = n / EPC;
-        for (int c = lane; c < nfull; c += 32) cp_async16(d + 16u * c, src + b + c * EPC, pol);
-        const int done = nfull * EPC;
-        if (lane < n - done)
-            cp_async_small<sizeof(E)>(d + sizeof(E) * (done + lane), src + b + done + lane, pol);
-    } else {
-        for (int q = lane; q < n; q += 32) cp_async_small<sizeof(E)>(d + sizeof(E) * q, src + b + q, pol);
-    }
 }
 
 // Where a tile's arrays sit in its stage.
@@ -176,15 +186,42 @@ __device__ __forceinline__ StageView<V> stage_view(unsigned char *stage, int4 t)
     return v;
 }
 
+// Copy elements [b, e) of an array to shared memory (element b at dst), b a
+// multiple of 4.  VEC: the 16-byte-aligned bulk [b, e & ~3) by one TMA copy
+// (lane 0), the rest by lanes tail_lane0.. with plain loads.  Otherwise
+// every element by plain loads.
+template <typename E, bool VEC>
+__device__ __forceinline__ void stage_range(E *dst, const E *src, int b, int e, int lane, int tail_lane0,
+                                            uint64_t *bar, uint64_t pol) {
+    if (VEC) {
+        const int bulk_end = max(b, e & ~3);
+        const uint32_t bytes = (uint32_t)(bulk_end - b) * sizeof(E);
+        if (lane == 0 && bytes) bulk_copy(dst, src + b, bytes, bar, pol);
+        const int t = lane - tail_lane0;
+        if (t >= 0 && bulk_end + t < e) dst[bulk_end - b + t] = ld_stream(src + bulk_end + t);
+    } else {
+        for (int q = b + lane; q < e; q += 32) dst[q - b] = ld_stream(src + q);
+    }
+}
+
+// Start the copies of tile t into a stage.  Lane 0 first fences the generic
+// proxy (lanes may have written this stage) against the asynchronous one.
 template <typename V, bool VEC>
-__device__ __forceinline__ void issue_tile(const MPParams<V> &p, unsigned char *stage, int4 t, int lane,
-                                           uint64_t pol) {
+__device__ __forceinline__ void issue_tile(const MPParams<V> &p, unsigned char *stage, uint64_t *bar, int4 t,
+                                           int lane, uint64_t pol) {
     const StageView<V> v = stage_view<V>(stage, t);
     const int base = t.y & ~3;
-    warp_copy<int, VEC>(v.col, p.col_idx, base, t.w, lane, pol);
-    warp_copy<V, VEC>(v.val, p.vals, base, t.w, lane, pol);
     const int rb = (t.x + 1) & ~3;
-    warp_copy<int, VEC>(v.re - ((t.x + 1) - rb), p.row_ptr, rb, t.z + 1, lane, pol);
+    if (VEC && lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the bytes the three bulk copies below will deliver
+        const uint32_t nb = (uint32_t)(max(base, t.w & ~3) - base);
+        const uint32_t rbytes = 4u * (uint32_t)(max(rb, (t.z + 1) & ~3) - rb);
+        mbar_expect_tx(bar, nb * (4u + sizeof(V)) + rbytes);
+    }
+    stage_range<int, VEC>(v.col, p.col_idx, base, t.w, lane, 1, bar, pol);
+    stage_range<V, VEC>(v.val, p.vals, base, t.w, lane, 4, bar, pol);
+    stage_range<int, VEC>(v.re - ((t.x + 1) - rb), p.row_ptr, rb, t.z + 1, lane, 8, bar, pol);
 }
 
 __device__ __forceinline__ int4 tile_bounds(const int2 *part, long long t) {
@@ -248,9 +285,19 @@ merge_path_spmv_kernel(const MPParams<V> p) {
     const long long W = p.num_warps;
     const long long t_begin = me * P / W;
     const long long t_end = (me + 1) * P / W;  // non-empty: W <= P
-    unsigned char *stages = dsm + (size_t)warp * kStages * stage_bytes<V, IPL>();
+    unsigned char *region = dsm + (size_t)warp * warp_region_bytes<V, IPL>();
+    uint64_t *bars = reinterpret_cast<uint64_t *>(region);
+    unsigned char *stages = region + 16;
     const uint64_t stream_pol = l2_policy_evict_first();
     const uint64_t x_pol = l2_policy_evict_last();
+    if (VEC) {
+        if (lane == 0) {
+            mbar_init(bars);
+            mbar_init(bars + 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+    }
 
     // the warp's run starts inside a row whose beginning belongs to an earlier warp
     const int4 first_tile = tile_bounds(p.part, t_begin);
@@ -258,13 +305,11 @@ merge_path_spmv_kernel(const MPParams<V> p) {
 
     int4 cur = first_tile;
     int4 nxt = make_int4(0, 0, 0, 0);
-    issue_tile<V, VEC>(p, stages, cur, lane, stream_pol);
-    cp_async_commit();
+    issue_tile<V, VEC>(p, stages, bars, cur, lane, stream_pol);
     if (t_begin + 1 < t_end) {
         nxt = tile_bounds(p.part, t_begin + 1);
-        issue_tile<V, VEC>(p, stages + stage_bytes<V, IPL>(), nxt, lane, stream_pol);
+        issue_tile<V, VEC>(p, stages + stage_bytes<V, IPL>(), bars + 1, nxt, lane, stream_pol);
     }
-    cp_async_commit();
 
     V carry = V(0);  // sum of the row open at the previous tile's end
     for (long long t = t_begin; t < t_end; ++t) {
@@ -277,7 +322,17 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const StageView<V> sv = stage_view<V>(stage, cur);
         const int nwords = (nnzt + 31) >> 5;
 
-        cp_async_wait<1>();  // this tile's copies are done (the next tile's may not be)
+        if (VEC) {  // this tile's copies are done (the next tile's may not be)
+            const uint32_t parity = (uint32_t)(((t - t_begin) >> 1) & 1);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + s, parity));
+            if (!ok) {  // a copy never completed: report it and stop this warp
+                if (lane == 0 && p.error) atomicOr(p.error, 1);
+                mbar_wait_bounded(bars + s, parity);
+                if (t + 1 < t_end) mbar_wait_bounded(bars + (s ^ 1), (uint32_t)(((t + 1 - t_begin) >> 1) & 1));
+                return;
+            }
+        }
+        __syncwarp();  // the lanes' tail loads are visible too
         for (int w = lane; w < nwords + 2; w += 32) sv.bm[w] = 0u;
         __syncwarp();
         // The carried sum belongs to row i0.  If that row ends before the
@@ -373,11 +428,9 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         cur = nxt;
         if (t + 2 < t_end) {
             nxt = tile_bounds(p.part, t + 2);
-            issue_tile<V, VEC>(p, stage, nxt, lane, stream_pol);
+            issue_tile<V, VEC>(p, stage, bars + s, nxt, lane, stream_pol);
         }
-        cp_async_commit();
     }
-    cp_async_wait<0>();
 
     // ---- the row open at the end of the warp's run, if it has nonzeros here
     const int4 last_tile = tile_bounds(p.part, t_end - 1);
@@ -397,7 +450,7 @@ int g_ctas_per_sm[2][33][2][64];  // occupancy per (type, IPL, VEC, device)
 template <typename V, int IPL, bool VEC>
 cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     if (a.num_tiles <= 0) return cudaSuccess;
-    constexpr size_t smem = (size_t)kWarps * kStages * stage_bytes<V, IPL>();
+    constexpr size_t smem = (size_t)kWarps * warp_region_bytes<V, IPL>();
     int dev = 0;
     cudaGetDevice(&dev);
     int &per_sm = g_ctas_per_sm[sizeof(V) == 8][IPL][VEC][dev & 63];
@@ -428,6 +481,7 @@ cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     p.tail_partial = static_cast<V *>(a.tail_partial);
     p.head_partial = static_cast<V *>(a.head_partial);
     p.arrivals = a.arrivals;
+    p.error = a.error;
     const unsigned grid = (unsigned)((p.num_warps + kWarps - 1) / kWarps);
     merge_path_spmv_kernel<V, IPL, VEC><<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
@@ -454,7 +508,7 @@ int merge_path_threads() { return 32; }
 int merge_path_default_items(spmv_dtype_t dtype) { return dtype == SPMV_F64 ? 8 : 16; }
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
-    // 16-byte copies need row_ptr, col_idx and vals 16-byte aligned
+    // bulk copies need row_ptr, col_idx and vals 16-byte aligned
     const bool vec = (reinterpret_cast<uintptr_t>(a.row_ptr) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.col_idx) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.vals) % 16 == 0);

@@ -47,4 +47,5 @@ def test_argument_errors_need_no_device():
     assert L.spmv_plan_info(None, None) == 1
     assert L.spmv_plan_export(None, 0, None, 0, None) == 1
     assert L.spmv_plan_update_values(None, fake, None) == 1
+    assert L.spmv_plan_device_status(None, None) == 1
     assert L.spmv_plan_destroy(None) == 0

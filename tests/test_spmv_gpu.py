@@ -28,6 +28,7 @@ def run(A, x, y0, alpha, beta, kernel="auto", ipt=0, fill_nan=False):
     plan(xd, yd, alpha, beta)
     torch.cuda.synchronize()
     info = plan.info()
+    assert plan.device_status() == 0
     plan.close()
     return yd.cpu().numpy(), info
 
