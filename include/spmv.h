@@ -70,7 +70,7 @@ typedef struct {
     int32_t kernel;           /* spmv_kernel_t; SPMV_KERNEL_AUTO (0) = choose */
     int32_t items_per_thread; /* merge-path work items (rows + nonzeros) per
                                  thread; a tile is one warp, T = 32 * items.
-                                 0 = default (16 for fp32, 8 for fp64).
+                                 0 = default (12 for fp32, 8 for fp64).
                                  Allowed: 8, 12, 16, 24, 32 */
     int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = default.
                                  Allowed: 32, 64, 128, 256 */

@@ -15,14 +15,17 @@
 //     into its own shared-memory stage by the Tensor Memory Accelerator (one
 //     bulk copy per array, issued by one lane, completion signalled on an
 //     mbarrier) -- the next tile's copy is always in flight while the current
-//     one is processed.  A copy must start and end on 16-byte boundaries, so
-//     the up-to-3 elements after the last boundary are loaded by lanes;
+//     one is processed.  When beta != 0 the tile's slice of y comes along.
+//     A copy must start and end on 16-byte boundaries: it is rounded out to
+//     them wherever that stays inside the array, and only at an array's end
+//     do lanes load the last few elements;
 //  2. marks in a bitmap, for every row with a nonzero in the tile, the
 //     position of its last one;
 //  3. splits the tile's nonzeros over the 32 lanes in runs of Q = the odd
 //     number nearest above nnz/32 (odd, so the lanes' shared-memory reads hit
-//     distinct banks); each lane gathers x for its whole run into registers
-//     through the read-only path, so all its gathers are in flight at once;
+//     distinct banks); each lane loads its run's values and gathers its x
+//     values into registers through the read-only path -- all at once, and
+//     before the bitmap is built, so their latency overlaps that work;
 //  4. adds its run up in order (one fused multiply-add per nonzero) and,
 //     where the bitmap marks a row's last nonzero, closes the row and keeps
 //     its sum in that nonzero's slot (no other lane reads it).  Row ends cost
@@ -81,15 +84,16 @@ struct MPParams {
 
 // One stage of a warp's shared memory, for a tile with n nonzeros and r row
 // ends (n + r <= T):
-//   col[ns] | val[ns] | row_ends[rs] | bitmap[(n + 31) / 32 + 2]
-// ns = (sh + n + 4) & ~3 <= n + 7 and rs = (rsh + r + 4) & ~3 <= r + 7
-// slots (sh, rsh < 4 are the alignment shifts of the 16-byte copies).  The
-// size grows with n, so it is largest for n = T, r = 0:
+//   col[ns] | val[ns] | row_ends[rs] | y_old[ys] (beta != 0 only) | bitmap
+// ns = (sh + n + 4) & ~3 <= n + 7, rs and ys likewise <= r + 7 slots (sh and
+// the other shifts < 4 align the 16-byte copies), bitmap (n + 31) / 32 + 2
+// words.  With 4 + sizeof(V) bytes per nonzero and at most 4 + sizeof(V) per
+// row this is bounded by:
 template <typename V, int IPL>
 __host__ __device__ constexpr int stage_bytes() {
     constexpr int T = 32 * IPL;
-    constexpr int per_nnz = sizeof(int) + sizeof(V);
-    return ((per_nnz * (T + 8) + 4 * (T / 32 + 16)) + 15) & ~15;
+    constexpr int per_unit = sizeof(int) + sizeof(V);
+    return ((per_unit * (T + 16) + 4 * (T / 32 + 16)) + 15) & ~15;
 }
 // A warp's region: two mbarriers (16 bytes), then its two stages.
 template <typename V, int IPL>
@@ -167,61 +171,87 @@ struct StageView {
     int *col;      // col[k + sh]: the tile's nonzero k
     V *val;        // val[k + sh]
     int *re;       // re[r]: absolute end of row i0 + r
+    V *yo;         // yo[r] = y[i0 + r] before the product (beta != 0)
     unsigned *bm;  // bitmap over the tile's nonzeros
 };
 
 template <typename V>
-__device__ __forceinline__ StageView<V> stage_view(unsigned char *stage, int4 t) {
+__device__ __forceinline__ StageView<V> stage_view(unsigned char *stage, int4 t, bool with_y) {
     const int i0 = t.x, j0 = t.y, i1 = t.z, j1 = t.w;
-    const int sh = j0 & 3;
-    const int ns = (sh + (j1 - j0) + 4) & ~3;
+    const int ns = ((j0 & 3) + (j1 - j0) + 4) & ~3;
     const int rsh = (i0 + 1) & 3;
     const int rs = (rsh + (i1 - i0) + 4) & ~3;
+    const int ysh = i0 & 3;
+    const int ys = with_y ? (ysh + (i1 - i0) + 4) & ~3 : 0;
     StageView<V> v;
     v.col = reinterpret_cast<int *>(stage);
     v.val = reinterpret_cast<V *>(v.col + ns);
     int *re_raw = reinterpret_cast<int *>(v.val + ns);
     v.re = re_raw + rsh;
-    v.bm = reinterpret_cast<unsigned *>(re_raw + rs);
+    V *y_raw = reinterpret_cast<V *>(re_raw + rs);
+    v.yo = y_raw + ysh;
+    v.bm = reinterpret_cast<unsigned *>(y_raw + ys);
     return v;
 }
 
-// Copy elements [b, e) of an array to shared memory (element b at dst), b a
-// multiple of 4.  VEC: the 16-byte-aligned bulk [b, e & ~3) by one TMA copy
-// (lane 0), the rest by lanes tail_lane0.. with plain loads.  Otherwise
-// every element by plain loads.
-template <typename E, bool VEC>
-__device__ __forceinline__ void stage_range(E *dst, const E *src, int b, int e, int lane, int tail_lane0,
-                                            uint64_t *bar, uint64_t pol) {
-    if (VEC) {
-        const int bulk_end = max(b, e & ~3);
-        const uint32_t bytes = (uint32_t)(bulk_end - b) * sizeof(E);
-        if (lane == 0 && bytes) bulk_copy(dst, src + b, bytes, bar, pol);
-        const int t = lane - tail_lane0;
-        if (t >= 0 && bulk_end + t < e) dst[bulk_end - b + t] = ld_stream(src + bulk_end + t);
-    } else {
-        for (int q = b + lane; q < e; q += 32) dst[q - b] = ld_stream(src + q);
-    }
+// The bulk-copied part of elements [b, e) of an array of n elements, b a
+// multiple of 4: rounded up to a 16-byte boundary when that stays inside the
+// array, else down (the few elements left are loaded by lanes).
+__device__ __forceinline__ int bulk_end(int b, int e, long long n) {
+    const int up = (e + 3) & ~3;
+    return max(b, (long long)up <= n ? up : (e & ~3));
+}
+
+// Lanes tail_lane0.. load the elements [from, e) the bulk copy left out.
+template <typename E>
+__device__ __forceinline__ void stage_tail(E *dst, const E *src, int b, int from, int e, int lane, int tail_lane0) {
+    const int t = lane - tail_lane0;
+    if (t >= 0 && from + t < e) dst[from - b + t] = ld_stream(src + from + t);
 }
 
 // Start the copies of tile t into a stage.  Lane 0 first fences the generic
-// proxy (lanes may have written this stage) against the asynchronous one.
+// proxy (lanes may have written this stage) against the asynchronous one,
+// announces the bytes to the stage's barrier and issues one copy per array.
 template <typename V, bool VEC>
 __device__ __forceinline__ void issue_tile(const MPParams<V> &p, unsigned char *stage, uint64_t *bar, int4 t,
                                            int lane, uint64_t pol) {
-    const StageView<V> v = stage_view<V>(stage, t);
-    const int base = t.y & ~3;
-    const int rb = (t.x + 1) & ~3;
-    if (VEC && lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        // the bytes the three bulk copies below will deliver
-        const uint32_t nb = (uint32_t)(max(base, t.w & ~3) - base);
-        const uint32_t rbytes = 4u * (uint32_t)(max(rb, (t.z + 1) & ~3) - rb);
-        mbar_expect_tx(bar, nb * (4u + sizeof(V)) + rbytes);
+    const bool with_y = p.mode & 2;
+    const StageView<V> v = stage_view<V>(stage, t, with_y);
+    const int i0 = t.x, j0 = t.y, i1 = t.z, j1 = t.w;
+    const int base = j0 & ~3;
+    const int rb = (i0 + 1) & ~3;
+    const int yb = i0 & ~3;
+    int *re_raw = v.re - ((i0 + 1) - rb);
+    V *y_raw = v.yo - (i0 - yb);
+    if (!VEC) {
+        for (int q = base + lane; q < j1; q += 32) {
+            v.col[q - base] = ld_stream(p.col_idx + q);
+            v.val[q - base] = ld_stream(p.vals + q);
+        }
+        for (int q = rb + lane; q < i1 + 1; q += 32) re_raw[q - rb] = ld_stream(p.row_ptr + q);
+        if (with_y)
+            for (int q = yb + lane; q < i1; q += 32) y_raw[q - yb] = p.y[q];
+        return;
     }
-    stage_range<int, VEC>(v.col, p.col_idx, base, t.w, lane, 1, bar, pol);
-    stage_range<V, VEC>(v.val, p.vals, base, t.w, lane, 4, bar, pol);
-    stage_range<int, VEC>(v.re - ((t.x + 1) - rb), p.row_ptr, rb, t.z + 1, lane, 8, bar, pol);
+    const int ne = bulk_end(base, j1, p.nnz);
+    const int re_end = bulk_end(rb, i1 + 1, (long long)p.m + 1);
+    const int ye = with_y ? bulk_end(yb, i1, p.m) : yb;
+    if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t nb = (uint32_t)(ne - base), rbytes = 4u * (uint32_t)(re_end - rb);
+        const uint32_t ybytes = (uint32_t)sizeof(V) * (uint32_t)(ye - yb);
+        mbar_expect_tx(bar, nb * (4u + sizeof(V)) + rbytes + ybytes);
+        if (nb) {
+            bulk_copy(v.col, p.col_idx + base, 4u * nb, bar, pol);
+            bulk_copy(v.val, p.vals + base, (uint32_t)sizeof(V) * nb, bar, pol);
+        }
+        if (rbytes) bulk_copy(re_raw, p.row_ptr + rb, rbytes, bar, pol);
+        if (ybytes) bulk_copy(y_raw, p.y + yb, ybytes, bar, pol);
+    }
+    stage_tail<int>(v.col, p.col_idx, base, ne, j1, lane, 1);
+    stage_tail<V>(v.val, p.vals, base, ne, j1, lane, 4);
+    stage_tail<int>(re_raw, p.row_ptr, rb, re_end, i1 + 1, lane, 8);
+    if (with_y) stage_tail<V>(y_raw, p.y, yb, ye, i1, lane, 12);
 }
 
 __device__ __forceinline__ int4 tile_bounds(const int2 *part, long long t) {
@@ -311,6 +341,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         issue_tile<V, VEC>(p, stages + stage_bytes<V, IPL>(), bars + 1, nxt, lane, stream_pol);
     }
 
+    const bool with_y = p.mode & 2;
     V carry = V(0);  // sum of the row open at the previous tile's end
     for (long long t = t_begin; t < t_end; ++t) {
         const int s = (int)((t - t_begin) & 1);
@@ -319,8 +350,10 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const int nrows = i1 - i0;
         const int nnzt = j1 - j0;
         const int sh = j0 & 3;
-        const StageView<V> sv = stage_view<V>(stage, cur);
+        const StageView<V> sv = stage_view<V>(stage, cur, with_y);
         const int nwords = (nnzt + 31) >> 5;
+        // bounds of the tile that goes into this stage next (load early)
+        const int4 after = t + 2 < t_end ? tile_bounds(p.part, t + 2) : cur;
 
         if (VEC) {  // this tile's copies are done (the next tile's may not be)
             const uint32_t parity = (uint32_t)(((t - t_begin) >> 1) & 1);
@@ -333,6 +366,19 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             }
         }
         __syncwarp();  // the lanes' tail loads are visible too
+
+        // ---- this lane's run [k0, k0 + run): values and x into registers
+        const int Q = ((nnzt + 31) >> 5) | 1;
+        const int k0 = min(lane * Q, nnzt);
+        const int run = min(Q, nnzt - k0);
+        V xr[IPL + 1], vr[IPL + 1];
+#pragma unroll
+        for (int i = 0; i <= IPL; ++i) {
+            xr[i] = i < run ? gather_keep(p.x + sv.col[k0 + i + sh], x_pol) : V(0);
+            vr[i] = i < run ? sv.val[k0 + i + sh] : V(0);
+        }
+
+        // ---- mark each row's last nonzero in the tile (while the gathers fly)
         for (int w = lane; w < nwords + 2; w += 32) sv.bm[w] = 0u;
         __syncwarp();
         // The carried sum belongs to row i0.  If that row ends before the
@@ -340,40 +386,29 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const bool row0_ends_first = nrows > 0 && sv.re[0] == j0;
         const V carry_row0 = row0_ends_first ? carry : V(0);
         if (row0_ends_first) carry = V(0);
-
-        // ---- 2. mark each row's last nonzero in the tile
         for (int r = lane; r < nrows; r += 32) {
             const int e = sv.re[r] - j0;
             const int ep = r == 0 ? 0 : sv.re[r - 1] - j0;
             if (e > ep) atomicOr(sv.bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
         }
         __syncwarp();
-
-        // ---- 3. this lane's run [k0, k0 + run) and its x values
-        const int Q = ((nnzt + 31) >> 5) | 1;
-        const int k0 = min(lane * Q, nnzt);
-        const int run = min(Q, nnzt - k0);
-        V xr[IPL + 1];
-#pragma unroll
-        for (int i = 0; i <= IPL; ++i) xr[i] = i < run ? gather_keep(p.x + sv.col[k0 + i + sh], x_pol) : V(0);
         const unsigned long long two = ((unsigned long long)sv.bm[(k0 >> 5) + 1] << 32) | sv.bm[k0 >> 5];
         unsigned long long bits = two >> (k0 & 31);
 
-        // ---- 4. add the run up, closing rows where the bitmap says
+        // ---- add the run up, closing rows where the bitmap says
         V acc = V(0);
         V first_val = V(0);
         int first_pos = -1;
 #pragma unroll
         for (int i = 0; i <= IPL; ++i) {
             if (i < run) {
-                const int k = k0 + i;
-                acc = fma(sv.val[k + sh], xr[i], acc);
+                acc = fma(vr[i], xr[i], acc);
                 if (bits & 1ull) {
                     if (first_pos < 0) {
                         first_val = acc;
-                        first_pos = k;
+                        first_pos = k0 + i;
                     } else {
-                        sv.val[k + sh] = acc;
+                        sv.val[k0 + i + sh] = acc;  // only this lane touches the slot
                     }
                     acc = V(0);
                 }
@@ -381,7 +416,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             }
         }
 
-        // ---- 5. segmented inclusive scan of (row closed, running sum)
+        // ---- segmented inclusive scan of (row closed, running sum)
         V v = acc;
         int f = first_pos >= 0;
 #pragma unroll
@@ -403,7 +438,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         carry = __shfl_sync(0xffffffffu, v, 31);
         __syncwarp();
 
-        // ---- 6. finished rows; the warp's first row end may be a cut row
+        // ---- finished rows; the warp's first row end may be a cut row
         const bool cut_head = head_pending && nrows > 0;
         V head_val = V(0);
         for (int q = lane; q < nrows; q += 32) {
@@ -413,8 +448,10 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             if (q == 0 && cut_head) {
                 head_val = sum;
             } else {
-                const int row = i0 + q;
-                p.y[row] = finish_row(sum, p.alpha, p.beta, p.mode, p.y, row);
+                V res = sum;
+                if (p.mode & 1) res = p.alpha * res;
+                if (with_y) res = fma(p.beta, sv.yo[q], res);
+                p.y[i0 + q] = res;
             }
         }
         if (cut_head) {
@@ -424,10 +461,10 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         }
         __syncwarp();  // this stage may now be refilled
 
-        // ---- next tile: tile t + 2 goes into this stage
+        // ---- tile t + 2 goes into this stage
         cur = nxt;
         if (t + 2 < t_end) {
-            nxt = tile_bounds(p.part, t + 2);
+            nxt = after;
             issue_tile<V, VEC>(p, stage, bars + s, nxt, lane, stream_pol);
         }
     }
@@ -505,7 +542,7 @@ bool merge_path_supported(int ipl) { return ipl == 8 || ipl == 12 || ipl == 16 |
 
 int merge_path_threads() { return 32; }
 
-int merge_path_default_items(spmv_dtype_t dtype) { return dtype == SPMV_F64 ? 8 : 16; }
+int merge_path_default_items(spmv_dtype_t dtype) { return dtype == SPMV_F64 ? 8 : 12; }
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
     // bulk copies need row_ptr, col_idx and vals 16-byte aligned
