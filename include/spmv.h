@@ -70,7 +70,7 @@ typedef struct {
     int32_t kernel;           /* spmv_kernel_t; SPMV_KERNEL_AUTO (0) = choose */
     int32_t items_per_thread; /* merge-path work items (rows + nonzeros) per
                                  thread; a tile is one warp, T = 32 * items.
-                                 0 = default (12 for fp32, 8 for fp64).
+                                 0 = chosen from the statistics (8-16).
                                  Allowed: 8, 12, 16, 24, 32 */
     int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = default.
                                  Allowed: 32, 64, 128, 256 */
@@ -83,8 +83,9 @@ typedef struct {
  * length falls in class k: class 0 = empty rows, class k >= 1 = lengths in
  * [2^(k-1), 2^k).  rg_slots[g] = storage (slots) a Row-grouped CSR layout
  * with group size 32 << g would need (each group padded to its longest
- * row).  flags: bit0 row_ptr[0] != 0, bit1 row_ptr decreases, bit2
- * row_ptr[m] != nnz, bit3 a column index outside [0, n).
+ * row).  bandwidth: the largest |column - row| over every row's first and
+ * last stored nonzero.  flags: bit0 row_ptr[0] != 0, bit1 row_ptr
+ * decreases, bit2 row_ptr[m] != nnz, bit3 a column index outside [0, n).
  */
 typedef struct {
     int64_t hist[32];
@@ -94,6 +95,8 @@ typedef struct {
     int32_t max_len;
     int32_t n_empty;
     int32_t flags;
+    int32_t bandwidth;
+    int32_t reserved;
 } spmv_row_stats_t;
 
 typedef struct {

@@ -39,7 +39,7 @@ class Options(ctypes.Structure):
 class RowStats(ctypes.Structure):
     _fields_ = [("hist", ctypes.c_int64 * 32), ("sum_len", ctypes.c_int64), ("rg_slots", ctypes.c_int64 * 4),
                 ("min_len", ctypes.c_int32), ("max_len", ctypes.c_int32), ("n_empty", ctypes.c_int32),
-                ("flags", ctypes.c_int32)]
+                ("flags", ctypes.c_int32), ("bandwidth", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -179,7 +179,8 @@ class Plan:
         out = {f: getattr(inf, f) for f, _ in PlanInfo._fields_ if f != "stats"}
         s = inf.stats
         out["stats"] = {"hist": list(s.hist), "sum_len": s.sum_len, "rg_slots": list(s.rg_slots),
-                        "min_len": s.min_len, "max_len": s.max_len, "n_empty": s.n_empty, "flags": s.flags}
+                        "min_len": s.min_len, "max_len": s.max_len, "n_empty": s.n_empty, "flags": s.flags,
+                        "bandwidth": s.bandwidth}
         out["kernel_name"] = KERNEL_NAMES.get(inf.kernel, str(inf.kernel))
         return out
 

@@ -141,9 +141,8 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
         return fail(SPMV_ERR_INVALID_ARG, "unknown kernel option");
     if (forced == SPMV_KERNEL_RGCSR || forced == SPMV_KERNEL_LONG_ROWS)
         return fail(SPMV_ERR_UNSUPPORTED, "kernel not built in this version");
-    int ipt = opt.items_per_thread ? opt.items_per_thread
-                                   : env_int("SPMV_ITEMS_PER_THREAD", merge_path_default_items(dtype));
-    if (!merge_path_supported(ipt))
+    const int ipt_forced = opt.items_per_thread ? opt.items_per_thread : env_int("SPMV_ITEMS_PER_THREAD", 0);
+    if (ipt_forced && !merge_path_supported(ipt_forced))
         return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 8, 12, 16, 24 or 32");
 
     int dev = 0;
@@ -165,15 +164,16 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     p->row_ptr = row_ptr;
     p->col_idx = col_idx;
     p->vals = vals;
-    p->ipt = ipt;
-    p->tile = (int64_t)merge_path_threads() * ipt;
+    // the tile size is chosen after the analysis: size the arena for the
+    // smallest one
     const int64_t total = (int64_t)m + nnz;
-    p->num_tiles = total > 0 ? (total + p->tile - 1) / p->tile : 1;
+    const int64_t min_tile = (int64_t)merge_path_threads() * (ipt_forced ? ipt_forced : merge_path_min_items());
+    const int64_t max_tiles = total > 0 ? (total + min_tile - 1) / min_tile : 1;
 
     // ---- one arena: analysis scratch + merge-path schedule and carry state
     const int stats_ctas = stats_num_ctas(m, nnz);
     const size_t vs = value_size(dtype);
-    const size_t P = (size_t)p->num_tiles;
+    const size_t P = (size_t)max_tiles;
     size_t off = 0;
     const size_t off_partials = off;
     off = align_up(off + sizeof(StatsPartial) * stats_ctas, 256);
@@ -226,6 +226,9 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
 
     // ---- kernel choice and schedule
     p->kernel = forced != SPMV_KERNEL_AUTO ? forced : choose_kernel(*p);
+    p->ipt = ipt_forced ? ipt_forced : merge_path_choose_items(dtype, n, p->stats);
+    p->tile = (int64_t)merge_path_threads() * p->ipt;
+    p->num_tiles = total > 0 ? (total + p->tile - 1) / p->tile : 1;
     if (p->kernel == SPMV_KERNEL_MERGE_PATH && m > 0) {
         e = launch_merge_path_partition(m, nnz, row_ptr, p->tile, p->num_tiles, p->part, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);

@@ -37,6 +37,7 @@ struct StatsPartial {
     int32_t max_len;
     int32_t n_empty;
     int32_t flags;
+    int32_t bandwidth;
 };
 
 int stats_num_ctas(int32_t m, int32_t nnz);
@@ -69,7 +70,8 @@ struct MergePathArgs {
 
 bool merge_path_supported(int items_per_thread);
 int merge_path_threads();                       // threads per merge-path tile
-int merge_path_default_items(spmv_dtype_t dtype);  // items per thread by default
+int merge_path_min_items();                     // smallest supported items per thread
+int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_t &stats);
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int items_per_thread, const MergePathArgs &a,
                                    cudaStream_t stream);
 

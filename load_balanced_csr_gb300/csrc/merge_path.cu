@@ -374,6 +374,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         V xr[IPL + 1], vr[IPL + 1];
 #pragma unroll
         for (int i = 0; i <= IPL; ++i) {
+            if (sizeof(V) == 8 && i >= Q) break;  // Q is the same for all lanes
             xr[i] = i < run ? gather_keep(p.x + sv.col[k0 + i + sh], x_pol) : V(0);
             vr[i] = i < run ? sv.val[k0 + i + sh] : V(0);
         }
@@ -401,6 +402,9 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         int first_pos = -1;
 #pragma unroll
         for (int i = 0; i <= IPL; ++i) {
+            // fp64: every warp-wide FMA costs the fp64 unit the same, so stop
+            // at Q (the same for all lanes); fp32 runs fully predicated
+            if (sizeof(V) == 8 && i >= Q) break;
             if (i < run) {
                 acc = fma(vr[i], xr[i], acc);
                 if (bits & 1ull) {
@@ -542,7 +546,19 @@ bool merge_path_supported(int ipl) { return ipl == 8 || ipl == 12 || ipl == 16 |
 
 int merge_path_threads() { return 32; }
 
-int merge_path_default_items(spmv_dtype_t dtype) { return dtype == SPMV_F64 ? 8 : 12; }
+int merge_path_min_items() { return 8; }
+
+// Tile size from the row statistics.  Measured on GB300: matrices whose
+// nonzeros stay near the diagonal (the gathers of a tile hit few cache lines)
+// run best with larger tiles, which spread the per-tile work over more
+// nonzeros; scattered columns run best with smaller ones, which keep fewer
+// gathers outstanding per SM (too many of them stall the whole memory
+// pipeline).  fp32: 16 items per lane when the bandwidth is below n/64, else
+// 12.  fp64: 12 when the bandwidth is below 4096, else 8.
+int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_t &s) {
+    if (dtype == SPMV_F64) return s.bandwidth <= 4096 ? 12 : 8;
+    return (int64_t)s.bandwidth * 64 <= (int64_t)n ? 16 : 12;
+}
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
     // bulk copies need row_ptr, col_idx and vals 16-byte aligned

@@ -31,7 +31,7 @@ row_stats_kernel(int32_t m, int32_t n, int32_t nnz, const int32_t *__restrict__ 
                  const int32_t *__restrict__ col_idx, int64_t nnz_per_cta,
                  StatsPartial *__restrict__ partials) {
     __shared__ int s_hist[32];
-    __shared__ int s_min, s_max, s_empty, s_flags;
+    __shared__ int s_min, s_max, s_empty, s_flags, s_bw;
     __shared__ int s_wmax[kStatsThreads / 32];
     __shared__ long long s_rg[4];
     const int tid = threadIdx.x;
@@ -42,6 +42,7 @@ row_stats_kernel(int32_t m, int32_t n, int32_t nnz, const int32_t *__restrict__ 
         s_max = 0;
         s_empty = 0;
         s_flags = 0;
+        s_bw = 0;
     }
     __syncthreads();
 
@@ -62,6 +63,13 @@ row_stats_kernel(int32_t m, int32_t n, int32_t nnz, const int32_t *__restrict__ 
             atomicMin(&s_min, len);
             atomicMax(&s_max, len);
             if (len == 0) atomicAdd(&s_empty, 1);
+            // distance of the row's outermost stored entries from the diagonal
+            // (read only when the row's range lies inside col_idx)
+            if (len > 0 && a >= 0 && b <= nnz) {
+                const long long d0 = (long long)col_idx[a] - i, d1 = (long long)col_idx[b - 1] - i;
+                const long long d = max(d0 < 0 ? -d0 : d0, d1 < 0 ? -d1 : d1);
+                atomicMax(&s_bw, (int)min(d, (long long)INT_MAX));
+            }
         }
         // Row-grouped CSR storage: groups of G = 32, 64, 128, 256 rows, each
         // padded to its longest row (rows past m count as empty).
@@ -111,6 +119,7 @@ row_stats_kernel(int32_t m, int32_t n, int32_t nnz, const int32_t *__restrict__ 
         out->max_len = s_max;
         out->n_empty = s_empty;
         out->flags = s_flags;
+        out->bandwidth = s_bw;
     }
 }
 
@@ -147,6 +156,11 @@ stats_reduce_kernel(int num, const StatsPartial *__restrict__ partials, int32_t 
         int v = 0;
         for (int b = 0; b < num; ++b) v |= partials[b].flags;
         out->flags = v;
+    } else if (tid == 41) {
+        int v = 0;
+        for (int b = 0; b < num; ++b) v = max(v, partials[b].bandwidth);
+        out->bandwidth = m > 0 ? v : 0;
+        out->reserved = 0;
     }
 }
 

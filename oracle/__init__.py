@@ -44,7 +44,8 @@ def build(force: bool = False) -> str:
 class _Stats(ctypes.Structure):
     _fields_ = [("hist", ctypes.c_int64 * 32), ("sum_len", ctypes.c_int64),
                 ("rg_slots", ctypes.c_int64 * 4), ("min_len", ctypes.c_int32),
-                ("max_len", ctypes.c_int32), ("n_empty", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("max_len", ctypes.c_int32), ("n_empty", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("bandwidth", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -172,7 +173,8 @@ def row_stats(row_ptr, col_idx, n: int, nnz: int | None = None) -> dict:
     if lib().oracle_row_stats(m, n, nnz, _p(row_ptr), _p(col_idx), ctypes.byref(s)):
         raise ValueError("oracle_row_stats: bad arguments")
     return {"hist": list(s.hist), "sum_len": s.sum_len, "rg_slots": list(s.rg_slots),
-            "min_len": s.min_len, "max_len": s.max_len, "n_empty": s.n_empty, "flags": s.flags}
+            "min_len": s.min_len, "max_len": s.max_len, "n_empty": s.n_empty, "flags": s.flags,
+            "bandwidth": s.bandwidth}
 
 
 def rgcsr_layout(row_ptr, G: int):

@@ -121,6 +121,8 @@ int oracle_row_stats(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
     out->max_len = 0;
     out->n_empty = 0;
     out->flags = 0;
+    out->bandwidth = 0;
+    out->reserved = 0;
 
     if (row_ptr[0] != 0) out->flags |= 1;
     for (int32_t i = 0; i < m; ++i)
@@ -138,6 +140,14 @@ int oracle_row_stats(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
         if (i == 0 || len < out->min_len) out->min_len = len;
         if (i == 0 || len > out->max_len) out->max_len = len;
         if (len == 0) out->n_empty += 1;
+        if (len > 0) {
+            int64_t d_first = (int64_t)col_idx[row_ptr[i]] - i;
+            int64_t d_last = (int64_t)col_idx[row_ptr[i + 1] - 1] - i;
+            if (d_first < 0) d_first = -d_first;
+            if (d_last < 0) d_last = -d_last;
+            if (d_first > out->bandwidth) out->bandwidth = (int32_t)d_first;
+            if (d_last > out->bandwidth) out->bandwidth = (int32_t)d_last;
+        }
     }
     for (int g = 0; g < 4; ++g) {
         int32_t G = 32 << g;

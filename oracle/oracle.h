@@ -68,6 +68,9 @@ int oracle_merge_path_partition(int32_t m, int32_t nnz, const int32_t *row_ptr, 
  * with group size 32 << g needs ([RgCSR] section 3: each group of G rows is
  * padded to its longest row): sum over groups of G * max length, the last
  * partial group padded with empty rows.
+ * bandwidth = the largest |column - row| over every row's first and last
+ * stored nonzero (the distance of a sorted row's outermost entries from the
+ * diagonal; 0 for a matrix without nonzeros).
  * Flags: bit0 row_ptr[0] != 0, bit1 row_ptr decreases somewhere,
  * bit2 row_ptr[m] != nnz, bit3 a column index outside [0, n).
  * Statistics are computed only if no row_ptr flag (bits 0-2) is set.
@@ -80,6 +83,8 @@ typedef struct {
     int32_t max_len;
     int32_t n_empty;
     int32_t flags;
+    int32_t bandwidth;
+    int32_t reserved;
 } oracle_stats_t;
 
 int oracle_row_stats(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,

@@ -250,9 +250,15 @@ def brute_stats(rp, col, n):
         padded = np.zeros(-(-m // G) * G, dtype=np.int64)
         padded[:m] = lens
         slots.append(int(G * padded.reshape(-1, G).max(axis=1).sum()) if m else 0)
+    bw = 0
+    for i in range(m):
+        seg = np.asarray(col[rp[i]:rp[i + 1]], dtype=np.int64)
+        if len(seg):
+            bw = max(bw, int(abs(seg[0] - i)), int(abs(seg[-1] - i)))
     return {"hist": hist.tolist(), "sum_len": int(lens.sum()), "rg_slots": slots,
             "min_len": int(lens.min()) if m else 0, "max_len": int(lens.max()) if m else 0,
-            "n_empty": int((lens == 0).sum()), "flags": int(bool(np.any((col < 0) | (col >= n)))) * 8}
+            "n_empty": int((lens == 0).sum()), "flags": int(bool(np.any((col < 0) | (col >= n)))) * 8,
+            "bandwidth": bw}
 
 
 @pytest.mark.parametrize("seed", range(4))
@@ -279,6 +285,19 @@ def test_row_stats_flags():
     assert oracle.row_stats(rp, np.array([0, 4, 1], np.int32), 4)["flags"] == 8
     assert oracle.row_stats(rp, np.array([0, -1, 1], np.int32), 4)["flags"] == 8
     assert oracle.row_stats(rp, np.array([0, 3, 1], np.int32), 4)["flags"] == 0
+
+
+def test_bandwidth_of_known_matrices():
+    """5-point Laplacian on an nx-wide grid: outermost entries at +-nx; a
+    band-limited random matrix stays within its band; the identity has 0."""
+    A = synth.laplace2d(16, 9, "f64")
+    assert oracle.row_stats(A.row_ptr, A.col_idx, A.n)["bandwidth"] == 16
+    B = synth.fill_random(synth.lengths_uniform(5000, 1, 6, 3), 5000, band=37, seed=3)
+    bw = oracle.row_stats(B.row_ptr, B.col_idx, B.n)["bandwidth"]
+    assert 30 <= bw <= 37
+    rp = np.arange(11, dtype=np.int32)
+    assert oracle.row_stats(rp, np.arange(10, dtype=np.int32), 10)["bandwidth"] == 0
+    assert oracle.row_stats(rp, np.arange(10, dtype=np.int32)[::-1].copy(), 10)["bandwidth"] == 9
 
 
 def test_length_class_boundaries():
