@@ -393,32 +393,28 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             if (e > ep) atomicOr(sv.bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
         }
         __syncwarp();
+        // bit i of `bits`: nonzero k0 + i is the last of a row in this tile
+        // (Q <= 33 and only the run's bits are kept)
         const unsigned long long two = ((unsigned long long)sv.bm[(k0 >> 5) + 1] << 32) | sv.bm[k0 >> 5];
-        unsigned long long bits = two >> (k0 & 31);
+        const unsigned long long shifted = two >> (k0 & 31);
+        const unsigned long long run_mask = run >= 64 ? ~0ull : ((1ull << run) - 1);
+        const unsigned long long bits = shifted & run_mask;
 
-        // ---- add the run up, closing rows where the bitmap says
+        // ---- add the run up; a row's sum goes to the slot of its last nonzero
+        // (the first closed row's slot gets the carry from earlier lanes below)
         V acc = V(0);
-        V first_val = V(0);
-        int first_pos = -1;
 #pragma unroll
         for (int i = 0; i <= IPL; ++i) {
             // fp64: every warp-wide FMA costs the fp64 unit the same, so stop
             // at Q (the same for all lanes); fp32 runs fully predicated
             if (sizeof(V) == 8 && i >= Q) break;
-            if (i < run) {
-                acc = fma(vr[i], xr[i], acc);
-                if (bits & 1ull) {
-                    if (first_pos < 0) {
-                        first_val = acc;
-                        first_pos = k0 + i;
-                    } else {
-                        sv.val[k0 + i + sh] = acc;  // only this lane touches the slot
-                    }
-                    acc = V(0);
-                }
-                bits >>= 1;
+            acc = fma(vr[i], xr[i], acc);  // vr[i] = 0 past the run
+            if ((bits >> i) & 1ull) {
+                sv.val[k0 + i + sh] = acc;  // only this lane touches the slot
+                acc = V(0);
             }
         }
+        const int first_pos = bits ? k0 + (__ffsll((long long)bits) - 1) : -1;
 
         // ---- segmented inclusive scan of (row closed, running sum)
         V v = acc;
@@ -438,7 +434,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         }
         V carry_in = __shfl_up_sync(0xffffffffu, v, 1);
         if (lane == 0) carry_in = carry;
-        if (first_pos >= 0) sv.val[first_pos + sh] = carry_in + first_val;
+        if (first_pos >= 0) sv.val[first_pos + sh] = carry_in + sv.val[first_pos + sh];
         carry = __shfl_sync(0xffffffffu, v, 31);
         __syncwarp();
 
