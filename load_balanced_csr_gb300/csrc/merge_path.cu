@@ -248,10 +248,13 @@ __device__ __forceinline__ void issue_tile(const MPParams<V> &p, unsigned char *
         if (rbytes) bulk_copy(re_raw, p.row_ptr + rb, rbytes, bar, pol);
         if (ybytes) bulk_copy(y_raw, p.y + yb, ybytes, bar, pol);
     }
-    stage_tail<int>(v.col, p.col_idx, base, ne, j1, lane, 1);
-    stage_tail<V>(v.val, p.vals, base, ne, j1, lane, 4);
-    stage_tail<int>(re_raw, p.row_ptr, rb, re_end, i1 + 1, lane, 8);
-    if (with_y) stage_tail<V>(y_raw, p.y, yb, ye, i1, lane, 12);
+    // elements past the last 16-byte boundary, only at an array's end
+    if (ne < j1 || re_end < i1 + 1 || ye < (with_y ? i1 : yb)) {
+        stage_tail<int>(v.col, p.col_idx, base, ne, j1, lane, 1);
+        stage_tail<V>(v.val, p.vals, base, ne, j1, lane, 4);
+        stage_tail<int>(re_raw, p.row_ptr, rb, re_end, i1 + 1, lane, 8);
+        if (with_y) stage_tail<V>(y_raw, p.y, yb, ye, i1, lane, 12);
+    }
 }
 
 __device__ __forceinline__ int4 tile_bounds(const int2 *part, long long t) {
@@ -546,14 +549,14 @@ int merge_path_min_items() { return 8; }
 
 // Tile size from the row statistics.  Measured on GB300: matrices whose
 // nonzeros stay near the diagonal (the gathers of a tile hit few cache lines)
-// run best with larger tiles, which spread the per-tile work over more
+// run best with large tiles, which spread the per-tile work over more
 // nonzeros; scattered columns run best with smaller ones, which keep fewer
 // gathers outstanding per SM (too many of them stall the whole memory
-// pipeline).  fp32: 16 items per lane when the bandwidth is below n/64, else
+// pipeline).  fp32: 24 items per lane when the bandwidth is below n/64, else
 // 12.  fp64: 12 when the bandwidth is below 4096, else 8.
 int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_t &s) {
     if (dtype == SPMV_F64) return s.bandwidth <= 4096 ? 12 : 8;
-    return (int64_t)s.bandwidth * 64 <= (int64_t)n ? 16 : 12;
+    return (int64_t)s.bandwidth * 64 <= (int64_t)n ? 24 : 12;
 }
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
