@@ -44,12 +44,13 @@ SPEC_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def compulsory_bytes(A) -> int:
-    """nnz*(4+s) + (m+1)*4 + n*s + 2*m*s: every index and value once, x once,
-    y read and written once (the bytes-per-nonzero model of the Row-grouped
-    CSR page, section 3, extended by row_ptr, x and y)."""
+def compulsory_bytes(A, beta: float) -> int:
+    """nnz*(4+s) + (m+1)*4 + n*s + m*s (+ m*s when beta != 0): every index and
+    value once, x once, y written once and read once only when beta != 0 (the
+    bytes-per-nonzero model of the Row-grouped CSR page, section 3, extended
+    by row_ptr, x and y)."""
     s = A.vals.dtype.itemsize
-    return A.nnz * (4 + s) + (A.m + 1) * 4 + A.n * s + 2 * A.m * s
+    return A.nnz * (4 + s) + (A.m + 1) * 4 + A.n * s + (2 if beta != 0 else 1) * A.m * s
 
 
 def measured_peak():
@@ -259,7 +260,7 @@ def run_gpu(args, workload_name: str) -> dict | None:
         return None
 
     ms_step = total_ms / K
-    bc = compulsory_bytes(A)
+    bc = compulsory_bytes(A, W.beta)
     gflops = 2.0 * A.nnz / (ms_step * 1e-3) / 1e9 * world
     mean_us = float(per.mean())
     achieved = bc / (mean_us * 1e-6) / 1e9
