@@ -185,7 +185,8 @@ def run_gpu(args, workload_name: str) -> dict | None:
 
     torch.cuda.synchronize(dev)
     t = time.perf_counter()
-    plan = lb.Plan(rp, col, val, A.n, kernel=args.kernel, items_per_thread=args.ipt)
+    plan = lb.Plan(rp, col, val, A.n, kernel=args.kernel, items_per_thread=args.ipt, rgcsr_group=args.group,
+                   long_row_min=args.long_min)
     torch.cuda.synchronize(dev)
     plan_ms = (time.perf_counter() - t) * 1e3
     info = plan.info()
@@ -390,6 +391,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="auto")
     ap.add_argument("--ipt", type=int, default=0)
+    ap.add_argument("--group", type=int, default=0, help="Row-grouped CSR group size (0 = plan's choice)")
+    ap.add_argument("--long-min", type=int, default=0, help="long-row threshold (0 = plan's default)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

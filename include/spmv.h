@@ -59,10 +59,12 @@ typedef enum {
 /* Kernels a plan can run. */
 typedef enum {
     SPMV_KERNEL_AUTO = 0,       /* let the plan choose from the row-length statistics */
-    SPMV_KERNEL_MERGE_PATH = 1, /* equal shares of rows + nonzeros per CTA, carry-out fix-up */
+    SPMV_KERNEL_MERGE_PATH = 1, /* equal shares of rows + nonzeros per warp tile, fused carry-out fix-up */
     SPMV_KERNEL_THREAD_ROW = 2, /* one thread per row */
-    SPMV_KERNEL_RGCSR = 3,      /* Row-grouped CSR (interleaved copy of A built by the plan) */
-    SPMV_KERNEL_LONG_ROWS = 4   /* long rows by warp/CTA kernels, the rest by merge path */
+    SPMV_KERNEL_RGCSR = 3,      /* Row-grouped CSR (interleaved copy of A built by the plan);
+                                   long rows, if any, by the long-row kernel */
+    SPMV_KERNEL_LONG_ROWS = 4   /* long rows by the long-row kernel (one warp per segment of
+                                   4096 nonzeros), the other rows one thread per row */
 } spmv_kernel_t;
 
 /* Options for spmv_plan_create_ex; zero-initialise and set what you need. */
@@ -70,12 +72,16 @@ typedef struct {
     int32_t kernel;           /* spmv_kernel_t; SPMV_KERNEL_AUTO (0) = choose */
     int32_t items_per_thread; /* merge-path work items (rows + nonzeros) per
                                  thread; a tile is one warp, T = 32 * items.
-                                 0 = chosen from the statistics (8-16).
+                                 0 = chosen from the statistics (8-24).
                                  Allowed: 8, 12, 16, 24, 32 */
-    int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = default.
+    int32_t rgcsr_group;      /* Row-grouped CSR group size G; 0 = chosen from
+                                 the statistics (the largest G whose padding
+                                 is at most 10 %, else the least padded).
                                  Allowed: 32, 64, 128, 256 */
-    int32_t long_row_min;     /* rows with at least this many nonzeros count as
-                                 long (SPMV_KERNEL_LONG_ROWS); 0 = default */
+    int32_t long_row_min;     /* Row-grouped CSR and long-row kernels: rows with
+                                 at least this many nonzeros count as long and
+                                 go to the long-row kernel; 0 = default (512).
+                                 Allowed: 0 or >= 32 */
 } spmv_options_t;
 
 /*
@@ -112,16 +118,21 @@ typedef struct {
     int32_t launches_per_execute; /* kernel launches one spmv_execute issues */
     int64_t workspace_bytes;      /* device memory the plan owns */
     spmv_row_stats_t stats;
+    int32_t long_row_min;         /* threshold of the long-row kernel (0 if unused) */
+    int32_t long_segment_nnz;     /* nonzeros per long-row segment (one warp each) */
+    int64_t num_long_segments;    /* segments over all long rows */
+    int64_t rgcsr_slots;          /* slots of the Row-grouped copy (group_ptr[last]) */
 } spmv_plan_info_t;
 
 /* What spmv_plan_export copies out. */
 typedef enum {
     SPMV_EXPORT_PARTITION = 0,   /* int32 pairs (row, nonzero), num_tiles + 1 of them */
     SPMV_EXPORT_RG_GROUP_PTR = 1,/* int64[ceil(m/G) + 1] */
-    SPMV_EXPORT_RG_ROW_LEN = 2,  /* int32[m] */
+    SPMV_EXPORT_RG_ROW_LEN = 2,  /* int32[m]: row length, -1 for a row left to the long-row kernel */
     SPMV_EXPORT_RG_COL = 3,      /* int32[group_ptr[last]] */
     SPMV_EXPORT_RG_VAL = 4,      /* value type [group_ptr[last]] */
-    SPMV_EXPORT_LONG_ROWS = 5    /* int32[num_long_rows], ascending */
+    SPMV_EXPORT_LONG_ROWS = 5,   /* int32[num_long_rows], ascending */
+    SPMV_EXPORT_LONG_SEG_BEGIN = 6 /* int64[num_long_rows + 1]: first segment of each long row */
 } spmv_export_t;
 
 /*
@@ -134,8 +145,10 @@ typedef enum {
  * spmv_plan_update_values is called afterwards).  The plan OWNS one device
  * workspace, allocated here and freed by spmv_plan_destroy.
  * Synchronisation: runs its analysis kernels on `stream` and waits for that
- * stream once (to read the ~0.4 KB statistics back).  Results are
- * synchronous.
+ * stream once (to read the ~0.4 KB statistics back) -- three times for the
+ * Row-grouped CSR and long-row kernels, whose layouts are sized on the
+ * device (long-row count, segment count, Row-grouped slots) before their
+ * last allocation.  Results are synchronous.
  * Errors: INVALID_ARG for bad sizes/pointers; INVALID_CSR when the analysis
  * finds a malformed row_ptr or a column index outside [0, n); ALLOC; CUDA;
  * UNSUPPORTED when the current device is not compute capability 10.3.

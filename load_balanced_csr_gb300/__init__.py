@@ -20,7 +20,8 @@ __all__ = ["Plan", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
 
 KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
-EXPORTS = {"partition": 0, "rg_group_ptr": 1, "rg_row_len": 2, "rg_col": 3, "rg_val": 4, "long_rows": 5}
+EXPORTS = {"partition": 0, "rg_group_ptr": 1, "rg_row_len": 2, "rg_col": 3, "rg_val": 4, "long_rows": 5,
+           "long_seg_begin": 6}
 STATUS = {0: "ok", 1: "invalid argument", 2: "invalid CSR matrix", 3: "allocation failed", 4: "CUDA error",
           5: "unsupported"}
 
@@ -48,7 +49,9 @@ class PlanInfo(ctypes.Structure):
                 ("items_per_thread", ctypes.c_int32), ("rgcsr_group", ctypes.c_int32),
                 ("items_per_tile", ctypes.c_int64), ("num_tiles", ctypes.c_int64),
                 ("num_long_rows", ctypes.c_int32), ("launches_per_execute", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("stats", RowStats)]
+                ("workspace_bytes", ctypes.c_int64), ("stats", RowStats),
+                ("long_row_min", ctypes.c_int32), ("long_segment_nnz", ctypes.c_int32),
+                ("num_long_segments", ctypes.c_int64), ("rgcsr_slots", ctypes.c_int64)]
 
 
 _lib = None
@@ -196,7 +199,7 @@ class Plan:
         need = ctypes.c_size_t(0)
         check(lib().spmv_plan_export(self._h, code, None, 0, ctypes.byref(need)), "spmv_plan_export")
         dtype = {"partition": np.int32, "rg_group_ptr": np.int64, "rg_row_len": np.int32, "rg_col": np.int32,
-                 "long_rows": np.int32,
+                 "long_rows": np.int32, "long_seg_begin": np.int64,
                  "rg_val": np.float64 if str(self.dtype) == "torch.float64" else np.float32}[what]
         buf = np.empty(need.value // np.dtype(dtype).itemsize, dtype=dtype)
         check(lib().spmv_plan_export(self._h, code, buf.ctypes.data if buf.size else None, need.value, None),

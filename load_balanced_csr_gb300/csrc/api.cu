@@ -39,6 +39,26 @@ struct spmv_plan_s {
     int32_t *arrivals = nullptr;
     int32_t *device_error = nullptr;  // set by kernels whose copies time out
 
+    // Row-grouped CSR and long-row kernels (a second allocation, `aux`, and
+    // the interleaved copy of A, `rg`)
+    void *aux = nullptr;
+    size_t aux_bytes = 0;
+    int32_t long_min = 0;            // rows this long go to the long-row kernel (0: none)
+    int32_t *long_rows = nullptr;    // [num_long_rows]
+    int64_t *seg_begin = nullptr;    // [num_long_rows + 1]
+    int64_t num_segs = 0;
+    void *seg_partial = nullptr;     // [num_segs]
+    int32_t *long_arrivals = nullptr;  // [num_long_rows]
+    int g_log2 = 0;
+    int64_t ngroups = 0;
+    int64_t rg_slots = 0;
+    int64_t *group_ptr = nullptr;    // [ngroups + 1]
+    int32_t *row_len = nullptr;      // [m]
+    void *rg = nullptr;
+    size_t rg_bytes = 0;
+    int32_t *rg_col = nullptr;       // [rg_slots]
+    void *rg_val = nullptr;          // [rg_slots]
+
     spmv_row_stats_t stats{};
 };
 
@@ -90,10 +110,172 @@ spmv_kernel_t choose_kernel(const spmv_plan_s &p) {
     return SPMV_KERNEL_MERGE_PATH;
 }
 
+// Row-grouped CSR group size: the largest G in {32, 64, 128, 256} whose
+// padding (rg_slots / nnz - 1, measured over all rows) is at most 10 %, else
+// the least padded one.  The Row-grouped CSR page found G >= 32 needed for
+// coalescing and 128 best on its hardware (section 4); larger groups mean
+// fewer group offsets but more padding.
+int choose_rgcsr_group(const spmv_row_stats_t &s, int64_t nnz) {
+    if (nnz <= 0) return 128;
+    for (int g = 3; g >= 0; --g)
+        if ((double)s.rg_slots[g] <= 1.1 * (double)nnz) return 32 << g;
+    int best = 0;
+    for (int g = 1; g < 4; ++g)
+        if (s.rg_slots[g] < s.rg_slots[best]) best = g;
+    return 32 << best;
+}
+
+// Rows in length classes that can hold a row of at least `len` nonzeros:
+// an upper bound on the number of long rows.
+int64_t rows_at_least(const spmv_row_stats_t &s, int32_t len) {
+    int c = 0;
+    while (c < 31 && (len >> c) != 0) ++c;  // class of len
+    int64_t r = 0;
+    for (int k = c; k < 32; ++k) r += s.hist[k];
+    return r;
+}
+
 void destroy_plan(spmv_plan_s *p) {
     if (!p) return;
+    if (p->rg) cudaFree(p->rg);
+    if (p->aux) cudaFree(p->aux);
     if (p->arena) cudaFree(p->arena);
     delete p;
+}
+
+constexpr int32_t kDefaultLongRowMin = 512;
+
+// The long-row list and, for the Row-grouped kernel, its layout and copy of
+// A.  Two passes over row_ptr per structure, sized on the host from the
+// statistics where they bound it, read back where they do not.
+spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaStream_t stream) {
+    const int32_t m = p->m;
+    const bool rgcsr = p->kernel == SPMV_KERNEL_RGCSR;
+    p->long_min = opt.long_row_min ? opt.long_row_min : kDefaultLongRowMin;
+    const bool has_long = m > 0 && p->stats.max_len >= p->long_min;
+    const size_t vs = value_size(p->dtype);
+
+    const int nc = long_rows_num_chunks(m);
+    const int64_t long_ub = has_long ? rows_at_least(p->stats, p->long_min) : 0;
+    const int64_t segs_ub = has_long ? (int64_t)p->nnz / kLongSegmentNnz + long_ub : 0;
+    if (rgcsr) {
+        const int G = opt.rgcsr_group ? opt.rgcsr_group : choose_rgcsr_group(p->stats, p->nnz);
+        p->rgcsr_group = G;
+        p->g_log2 = 0;
+        while ((1 << p->g_log2) < G) ++p->g_log2;
+        p->ngroups = ((int64_t)m + G - 1) / G;
+    }
+    const int64_t scan_n = rgcsr && p->ngroups > nc ? p->ngroups : nc;
+
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t o_long = take(sizeof(int32_t) * long_ub);
+    const size_t o_segb = take(sizeof(int64_t) * (long_ub + 1));
+    const size_t o_segp = take(vs * segs_ub);
+    const size_t o_larr = take(sizeof(int32_t) * long_ub);
+    const size_t o_crow = take(sizeof(int64_t) * nc);
+    const size_t o_cseg = take(sizeof(int64_t) * nc);
+    const size_t o_crow_off = take(sizeof(int64_t) * (nc + 1));
+    const size_t o_cseg_off = take(sizeof(int64_t) * (nc + 1));
+    const size_t o_rlen = take(rgcsr ? sizeof(int32_t) * m : 0);
+    const size_t o_gsize = take(rgcsr ? sizeof(int64_t) * p->ngroups : 0);
+    const size_t o_gp = take(rgcsr ? sizeof(int64_t) * (p->ngroups + 1) : 0);
+    const size_t o_scr = take(sizeof(int64_t) * scan_scratch_elems(scan_n));
+    p->aux_bytes = off;
+    cudaError_t e = cudaMalloc(&p->aux, p->aux_bytes);
+    if (e != cudaSuccess) {
+        p->aux = nullptr;
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the row-kernel workspace: ") + cudaGetErrorString(e));
+    }
+    char *base = static_cast<char *>(p->aux);
+    p->long_rows = reinterpret_cast<int32_t *>(base + o_long);
+    p->seg_begin = reinterpret_cast<int64_t *>(base + o_segb);
+    p->seg_partial = base + o_segp;
+    p->long_arrivals = reinterpret_cast<int32_t *>(base + o_larr);
+    int64_t *chunk_rows = reinterpret_cast<int64_t *>(base + o_crow);
+    int64_t *chunk_segs = reinterpret_cast<int64_t *>(base + o_cseg);
+    int64_t *chunk_row_off = reinterpret_cast<int64_t *>(base + o_crow_off);
+    int64_t *chunk_seg_off = reinterpret_cast<int64_t *>(base + o_cseg_off);
+    int64_t *gsize = reinterpret_cast<int64_t *>(base + o_gsize);
+    int64_t *scratch = reinterpret_cast<int64_t *>(base + o_scr);
+    if (rgcsr) {
+        p->row_len = reinterpret_cast<int32_t *>(base + o_rlen);
+        p->group_ptr = reinterpret_cast<int64_t *>(base + o_gp);
+    }
+
+    // sizes read back: long rows, segments, Row-grouped slots
+    int64_t sizes[3] = {0, 0, 0};
+    if (long_ub > 0) e = cudaMemsetAsync(p->long_arrivals, 0, sizeof(int32_t) * long_ub, stream);
+    if (e == cudaSuccess && has_long) {
+        e = launch_long_rows_count(m, p->row_ptr, p->long_min, chunk_rows, chunk_segs, stream);
+        if (e == cudaSuccess) e = launch_exclusive_scan(chunk_rows, nc, chunk_row_off, scratch, stream);
+        if (e == cudaSuccess) e = launch_exclusive_scan(chunk_segs, nc, chunk_seg_off, scratch, stream);
+        if (e == cudaSuccess)
+            e = launch_long_rows_scatter(m, p->row_ptr, p->long_min, chunk_row_off, chunk_seg_off, p->long_rows,
+                                         p->seg_begin, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(&sizes[0], chunk_row_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(&sizes[1], chunk_seg_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    }
+    if (e == cudaSuccess && rgcsr && m > 0) {
+        e = launch_rgcsr_lengths(m, p->row_ptr, p->g_log2, has_long ? p->long_min : 0, p->row_len, gsize, stream);
+        if (e == cudaSuccess) e = launch_exclusive_scan(gsize, p->ngroups, p->group_ptr, scratch, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(&sizes[2], p->group_ptr + p->ngroups, sizeof(int64_t), cudaMemcpyDeviceToHost,
+                                stream);
+    } else if (e == cudaSuccess && rgcsr) {
+        e = cudaMemsetAsync(p->group_ptr, 0, sizeof(int64_t), stream);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "row-kernel layout");
+    p->num_long_rows = (int32_t)sizes[0];
+    p->num_segs = sizes[1];
+    p->rg_slots = sizes[2];
+    if (p->num_long_rows > long_ub || p->num_segs > segs_ub)
+        return fail(SPMV_ERR_CUDA, "long-row count exceeds its bound");
+
+    if (rgcsr && p->rg_slots > 0) {
+        const size_t col_bytes = align_up(sizeof(int32_t) * (size_t)p->rg_slots, 256);
+        p->rg_bytes = col_bytes + vs * (size_t)p->rg_slots;
+        e = cudaMalloc(&p->rg, p->rg_bytes);
+        if (e != cudaSuccess) {
+            p->rg = nullptr;
+            return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the Row-grouped copy: ") + cudaGetErrorString(e));
+        }
+        p->rg_col = static_cast<int32_t *>(p->rg);
+        p->rg_val = static_cast<char *>(p->rg) + col_bytes;
+        e = cudaMemsetAsync(p->rg, 0, p->rg_bytes, stream);  // pads: column 0, value 0
+        if (e == cudaSuccess)
+            e = launch_rgcsr_pack(p->dtype, m, p->row_ptr, p->col_idx, p->vals, p->g_log2, p->group_ptr, p->row_len,
+                                  p->rg_col, p->rg_val, true, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "Row-grouped copy");
+    }
+    return SPMV_OK;
+}
+
+cudaError_t launch_long_part(const spmv_plan_s *p, const void *x, void *y, double alpha, double beta,
+                             cudaStream_t stream) {
+    LongRowsArgs a;
+    a.row_ptr = p->row_ptr;
+    a.col_idx = p->col_idx;
+    a.vals = p->vals;
+    a.x = x;
+    a.y = y;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.long_rows = p->long_rows;
+    a.seg_begin = p->seg_begin;
+    a.num_long = p->num_long_rows;
+    a.num_segs = p->num_segs;
+    a.seg_partial = p->seg_partial;
+    a.arrivals = p->long_arrivals;
+    return launch_long_rows_spmv(p->dtype, a, stream);
 }
 
 }  // namespace
@@ -139,8 +321,11 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     if (forced == SPMV_KERNEL_AUTO) forced = env_kernel();
     if (forced < SPMV_KERNEL_AUTO || forced > SPMV_KERNEL_LONG_ROWS)
         return fail(SPMV_ERR_INVALID_ARG, "unknown kernel option");
-    if (forced == SPMV_KERNEL_RGCSR || forced == SPMV_KERNEL_LONG_ROWS)
-        return fail(SPMV_ERR_UNSUPPORTED, "kernel not built in this version");
+    if (opt.rgcsr_group && opt.rgcsr_group != 32 && opt.rgcsr_group != 64 && opt.rgcsr_group != 128 &&
+        opt.rgcsr_group != 256)
+        return fail(SPMV_ERR_INVALID_ARG, "rgcsr_group must be 32, 64, 128 or 256");
+    if (opt.long_row_min != 0 && opt.long_row_min < 32)
+        return fail(SPMV_ERR_INVALID_ARG, "long_row_min must be 0 or at least 32");
     const int ipt_forced = opt.items_per_thread ? opt.items_per_thread : env_int("SPMV_ITEMS_PER_THREAD", 0);
     if (ipt_forced && !merge_path_supported(ipt_forced))
         return fail(SPMV_ERR_INVALID_ARG, "items_per_thread must be 8, 12, 16, 24 or 32");
@@ -237,6 +422,13 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
             return cuda_fail(e, "merge-path partition");
         }
     }
+    if (p->kernel == SPMV_KERNEL_RGCSR || p->kernel == SPMV_KERNEL_LONG_ROWS) {
+        const spmv_status_t st = build_row_layouts(p, opt, stream);
+        if (st != SPMV_OK) {
+            destroy_plan(p);
+            return st;
+        }
+    }
     *out = p;
     return SPMV_OK;
 }
@@ -251,7 +443,20 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     cudaError_t e = cudaSuccess;
     switch (p->kernel) {
     case SPMV_KERNEL_THREAD_ROW:
-        e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, stream);
+        e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, 0, stream);
+        break;
+    case SPMV_KERNEL_LONG_ROWS:
+        // long rows first (they take longest), then the others
+        if (p->num_long_rows > 0) e = launch_long_part(p, x, y, alpha, beta, stream);
+        if (e == cudaSuccess)
+            e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta,
+                                      p->num_long_rows > 0 ? p->long_min : 0, stream);
+        break;
+    case SPMV_KERNEL_RGCSR:
+        if (p->num_long_rows > 0) e = launch_long_part(p, x, y, alpha, beta, stream);
+        if (e == cudaSuccess)
+            e = launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->rg_col, p->rg_val, x, y,
+                                  alpha, beta, stream);
         break;
     case SPMV_KERNEL_MERGE_PATH:
     default: {
@@ -279,10 +484,17 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     return SPMV_OK;
 }
 
-spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stream_t) {
+spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stream_t stream_handle) {
     if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
     if (!vals && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "vals is NULL");
     p->vals = vals;
+    if (p->kernel == SPMV_KERNEL_RGCSR && p->rg_slots > 0) {
+        // the pattern is unchanged: only the values move into the copy
+        const cudaError_t e = launch_rgcsr_pack(p->dtype, p->m, p->row_ptr, p->col_idx, vals, p->g_log2, p->group_ptr,
+                                                p->row_len, p->rg_col, p->rg_val, false,
+                                                reinterpret_cast<cudaStream_t>(stream_handle));
+        if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_update_values");
+    }
     return SPMV_OK;
 }
 
@@ -306,9 +518,13 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->items_per_tile = p->tile;
     info->num_tiles = p->num_tiles;
     info->num_long_rows = p->num_long_rows;
-    info->launches_per_execute = p->m > 0 ? 1 : 0;
-    info->workspace_bytes = (int64_t)p->arena_bytes;
+    info->launches_per_execute = p->m > 0 ? 1 + (p->num_long_rows > 0 ? 1 : 0) : 0;
+    info->workspace_bytes = (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes);
     info->stats = p->stats;
+    info->long_row_min = p->num_long_rows > 0 ? p->long_min : 0;
+    info->long_segment_nnz = kLongSegmentNnz;
+    info->num_long_segments = p->num_segs;
+    info->rgcsr_slots = p->rg_slots;
     return SPMV_OK;
 }
 
@@ -329,6 +545,37 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
         if (p->kernel != SPMV_KERNEL_MERGE_PATH) return fail(SPMV_ERR_INVALID_ARG, "plan has no merge-path partition");
         src = p->part;
         size = sizeof(int2) * (size_t)(p->num_tiles + 1);
+        break;
+    case SPMV_EXPORT_RG_GROUP_PTR:
+    case SPMV_EXPORT_RG_ROW_LEN:
+    case SPMV_EXPORT_RG_COL:
+    case SPMV_EXPORT_RG_VAL:
+        if (p->kernel != SPMV_KERNEL_RGCSR) return fail(SPMV_ERR_INVALID_ARG, "plan has no Row-grouped copy");
+        if (what == SPMV_EXPORT_RG_GROUP_PTR) {
+            src = p->group_ptr;
+            size = sizeof(int64_t) * (size_t)(p->ngroups + 1);
+        } else if (what == SPMV_EXPORT_RG_ROW_LEN) {
+            src = p->row_len;
+            size = sizeof(int32_t) * (size_t)p->m;
+        } else if (what == SPMV_EXPORT_RG_COL) {
+            src = p->rg_col;
+            size = sizeof(int32_t) * (size_t)p->rg_slots;
+        } else {
+            src = p->rg_val;
+            size = value_size(p->dtype) * (size_t)p->rg_slots;
+        }
+        break;
+    case SPMV_EXPORT_LONG_ROWS:
+    case SPMV_EXPORT_LONG_SEG_BEGIN:
+        if (p->kernel != SPMV_KERNEL_RGCSR && p->kernel != SPMV_KERNEL_LONG_ROWS)
+            return fail(SPMV_ERR_INVALID_ARG, "plan has no long-row list");
+        if (what == SPMV_EXPORT_LONG_ROWS) {
+            src = p->long_rows;
+            size = sizeof(int32_t) * (size_t)p->num_long_rows;
+        } else {
+            src = p->seg_begin;
+            size = p->num_long_rows > 0 ? sizeof(int64_t) * (size_t)(p->num_long_rows + 1) : 0;
+        }
         break;
     default: return fail(SPMV_ERR_INVALID_ARG, "plan does not hold this array");
     }

@@ -75,10 +75,64 @@ int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int items_per_thread, const MergePathArgs &a,
                                    cudaStream_t stream);
 
+// ---------------------------------------------------------------- plan-time layouts
+// Exclusive prefix sum of n int64 values: out[0..n] (out[n] = total).
+// scratch holds scan_scratch_elems(n) int64.
+int64_t scan_scratch_elems(int64_t n);
+cudaError_t launch_exclusive_scan(const int64_t *in, int64_t n, int64_t *out, int64_t *scratch,
+                                  cudaStream_t stream);
+
+// Long rows (length >= min_len), after OpSparse's two-pass binning: pass 1
+// counts per chunk of kStatsRowsPerCta rows the long rows and their
+// segments of kLongSegmentNnz nonzeros; after prefix sums over the chunks,
+// pass 2 writes the row ids in ascending order and each row's first segment.
+constexpr int kLongSegmentNnz = 4096;
+int long_rows_num_chunks(int32_t m);
+cudaError_t launch_long_rows_count(int32_t m, const int32_t *row_ptr, int32_t min_len, int64_t *chunk_rows,
+                                   int64_t *chunk_segs, cudaStream_t stream);
+cudaError_t launch_long_rows_scatter(int32_t m, const int32_t *row_ptr, int32_t min_len,
+                                     const int64_t *chunk_row_off, const int64_t *chunk_seg_off,
+                                     int32_t *long_rows, int64_t *seg_begin, cudaStream_t stream);
+
+// Row-grouped CSR layout: row_len[i] (-1 for rows of length >= long_min when
+// long_min > 0: those rows are left to the long-row kernel), group sizes
+// gsize[g] = G * (longest remaining row of group g); after a prefix sum,
+// group_ptr; then the interleaved copy (pads must be zero beforehand).
+cudaError_t launch_rgcsr_lengths(int32_t m, const int32_t *row_ptr, int g_log2, int32_t long_min,
+                                 int32_t *row_len, int64_t *gsize, cudaStream_t stream);
+cudaError_t launch_rgcsr_pack(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
+                              const void *vals, int g_log2, const int64_t *group_ptr, const int32_t *row_len,
+                              int32_t *rg_col, void *rg_val, bool pack_cols, cudaStream_t stream);
+
 // ---------------------------------------------------------------- row kernels
+// Thread per row; rows of length >= skip_min_len (when > 0) are skipped.
 cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr,
                                   const int32_t *col_idx, const void *vals, const void *x, void *y,
-                                  double alpha, double beta, cudaStream_t stream);
+                                  double alpha, double beta, int32_t skip_min_len, cudaStream_t stream);
+
+// Row-grouped CSR, thread per row (rows with row_len < 0 are skipped).
+cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const int64_t *group_ptr,
+                              const int32_t *row_len, const int32_t *rg_col, const void *rg_val,
+                              const void *x, void *y, double alpha, double beta, cudaStream_t stream);
+
+// Long rows: one warp per segment of kLongSegmentNnz nonzeros; rows with
+// several segments are finished by the last segment to arrive.
+struct LongRowsArgs {
+    const int32_t *row_ptr;
+    const int32_t *col_idx;
+    const void *vals;
+    const void *x;
+    void *y;
+    double alpha;
+    double beta;
+    const int32_t *long_rows;  // [num_long] ascending
+    const int64_t *seg_begin;  // [num_long + 1]
+    int32_t num_long;
+    int64_t num_segs;
+    void *seg_partial;         // [num_segs] value type
+    int32_t *arrivals;         // [num_long] zero between products
+};
+cudaError_t launch_long_rows_spmv(spmv_dtype_t dtype, const LongRowsArgs &a, cudaStream_t stream);
 
 int device_sm_count();
 

@@ -560,10 +560,13 @@ int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_
 }
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
-    // bulk copies need row_ptr, col_idx and vals 16-byte aligned
+    // bulk copies need row_ptr, col_idx, vals and (when it is read) y 16-byte
+    // aligned
+    const bool reads_y = dtype == SPMV_F64 ? a.beta != 0.0 : (float)a.beta != 0.0f;
     const bool vec = (reinterpret_cast<uintptr_t>(a.row_ptr) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.col_idx) % 16 == 0) &&
-                     (reinterpret_cast<uintptr_t>(a.vals) % 16 == 0);
+                     (reinterpret_cast<uintptr_t>(a.vals) % 16 == 0) &&
+                     (!reads_y || reinterpret_cast<uintptr_t>(a.y) % 16 == 0);
     if (dtype == SPMV_F64)
         return vec ? launch_ipl<double, true>(ipl, a, stream) : launch_ipl<double, false>(ipl, a, stream);
     return vec ? launch_ipl<float, true>(ipl, a, stream) : launch_ipl<float, false>(ipl, a, stream);

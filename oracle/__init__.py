@@ -103,6 +103,7 @@ def _bind(cdll):
         "oracle_rgcsr_layout": [i32, vp, i32, vp, vp],
         "oracle_rgcsr_pack_f64": [i32, vp, vp, vp, i32, vp, vp, vp],
         "oracle_rgcsr_pack_f32": [i32, vp, vp, vp, i32, vp, vp, vp],
+        "oracle_long_rows": [i32, vp, i32, i32, vp, vp, ctypes.POINTER(i64)],
     }
     for name, argtypes in sig.items():
         f = getattr(cdll, name)
@@ -203,3 +204,18 @@ def rgcsr_pack(row_ptr, col_idx, vals, G: int):
     if fn(m, _p(row_ptr), _p(col_idx), _p(vals), G, _p(gp), _p(rg_col), _p(rg_val)):
         raise ValueError("oracle_rgcsr_pack: bad arguments")
     return gp, rl, rg_col, rg_val
+
+
+def long_rows(row_ptr, min_len: int, seg_nnz: int):
+    """(ids, seg_begin): rows with at least min_len nonzeros, ascending, and
+    the first segment of each (segments of seg_nnz nonzeros)."""
+    row_ptr = _i32(row_ptr)
+    m = len(row_ptr) - 1
+    count = ctypes.c_int64(0)
+    if lib().oracle_long_rows(m, _p(row_ptr), min_len, seg_nnz, None, None, ctypes.byref(count)):
+        raise ValueError("oracle_long_rows: bad arguments")
+    ids = np.empty(count.value, dtype=np.int32)
+    seg_begin = np.empty(count.value + 1, dtype=np.int64)
+    if lib().oracle_long_rows(m, _p(row_ptr), min_len, seg_nnz, _p(ids), _p(seg_begin), ctypes.byref(count)):
+        raise ValueError("oracle_long_rows: bad arguments")
+    return ids, seg_begin

@@ -219,3 +219,22 @@ int oracle_rgcsr_pack_f32(int32_t m, const int32_t *row_ptr, const int32_t *col_
     }
     return 0;
 }
+
+/* [OpSparse] section 5.1: a row belongs to the bin when its length reaches
+ * the bin's lower bound; the rows are listed in the order they are met. */
+int oracle_long_rows(int32_t m, const int32_t *row_ptr, int32_t min_len, int32_t seg_nnz, int32_t *ids,
+                     int64_t *seg_begin, int64_t *count) {
+    if (!check_row_ptr_basic(m, row_ptr) || min_len < 1 || seg_nnz < 1 || count == NULL) return 1;
+    int64_t t = 0, segs = 0;
+    if (seg_begin) seg_begin[0] = 0;
+    for (int32_t i = 0; i < m; ++i) {
+        int32_t len = row_ptr[i + 1] - row_ptr[i];
+        if (len < min_len) continue;
+        segs += ((int64_t)len + seg_nnz - 1) / seg_nnz;
+        if (ids) ids[t] = i;
+        if (seg_begin) seg_begin[t + 1] = segs;
+        ++t;
+    }
+    *count = t;
+    return 0;
+}

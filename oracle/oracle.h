@@ -109,6 +109,19 @@ int oracle_rgcsr_pack_f32(int32_t m, const int32_t *row_ptr, const int32_t *col_
                           const float *vals, int32_t G, const int64_t *group_ptr,
                           int32_t *rg_col, float *rg_val);
 
+/*
+ * Long rows: the bin of rows with at least min_len nonzeros ([OpSparse]
+ * section 5.1 bins rows by length; the order inside a bin and the segment
+ * size are this library's choice, as the pages fix neither).  ids[] gets the
+ * long rows in ascending order; seg_begin[t] (count + 1 entries) is the
+ * number of seg_nnz-nonzero segments of the long rows before ids[t]:
+ * seg_begin[0] = 0, seg_begin[t+1] = seg_begin[t] + ceil(len(ids[t]) / seg_nnz).
+ * *count gets the number of long rows; ids and seg_begin may be NULL to
+ * count only.  Returns 0, or 1 on bad arguments (min_len < 1, seg_nnz < 1).
+ */
+int oracle_long_rows(int32_t m, const int32_t *row_ptr, int32_t min_len, int32_t seg_nnz, int32_t *ids,
+                     int64_t *seg_begin, int64_t *count);
+
 #ifdef __cplusplus
 }
 #endif

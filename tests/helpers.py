@@ -37,3 +37,6 @@ def assert_close_to_oracle(A, x, y_gpu, alpha, beta, y_old, rows=None, label="")
         t = np.float64 if A.dtype == "f64" else np.float32
         want = (t(beta) * y_old[sel][empty]).astype(t) if beta != 0 else np.zeros(empty.sum(), t)
         np.testing.assert_array_equal(got[empty], want, err_msg=f"{label}: empty rows")
+        # and the sign of a zero (alpha * +0 is -0 for alpha < 0), as the oracle has it
+        np.testing.assert_array_equal(np.signbit(got[empty]), np.signbit(ref[empty]),
+                                      err_msg=f"{label}: sign of empty rows")

@@ -27,6 +27,10 @@ MUTATIONS = [
     ("rgcsr row-major instead of interleaved", "rg_col[base + (int64_t)k * G] = col_idx[row_ptr[i] + k];\n            rg_val[base + (int64_t)k * G] = vals[row_ptr[i] + k];\n        }\n    }\n    return 0;\n}\n\nint oracle_rgcsr_pack_f32",
      "rg_col[group_ptr[i / G] + (i % G) * (group_ptr[i / G + 1] - group_ptr[i / G]) / G + k] = col_idx[row_ptr[i] + k];\n            rg_val[group_ptr[i / G] + (i % G) * (group_ptr[i / G + 1] - group_ptr[i / G]) / G + k] = vals[row_ptr[i] + k];\n        }\n    }\n    return 0;\n}\n\nint oracle_rgcsr_pack_f32",
      [pins.test_rgcsr_pack_decodes_back_to_csr]),
+    ("long-row bin excludes its bound", "if (len < min_len) continue;", "if (len <= min_len) continue;",
+     [pins.test_long_rows_worked_example]),
+    ("segment count rounds wrongly", "segs += ((int64_t)len + seg_nnz - 1) / seg_nnz;",
+     "segs += (int64_t)len / seg_nnz + 1;", [pins.test_long_rows_worked_example]),
 ]
 
 

@@ -345,3 +345,41 @@ def test_rgcsr_pack_decodes_back_to_csr(G):
     s = oracle.row_stats(A.row_ptr, A.col_idx, A.n)
     if G in (32, 128):
         assert gp[-1] == s["rg_slots"][{32: 0, 128: 2}[G]]
+
+
+# ---------------------------------------------------------------- long rows
+
+
+def test_long_rows_worked_example():
+    """Lengths 0, 5, 40, 4096, 4097, 12000, 31, 32 with the bin starting at 32
+    and segments of 4096: rows 2, 3, 4, 5, 7 are long, with 1, 1, 2, 3, 1
+    segments (counted by hand)."""
+    lens = np.array([0, 5, 40, 4096, 4097, 12000, 31, 32], dtype=np.int64)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ids, seg_begin = oracle.long_rows(rp, 32, 4096)
+    assert ids.tolist() == [2, 3, 4, 5, 7]
+    assert seg_begin.tolist() == [0, 1, 2, 4, 7, 8]
+    ids, seg_begin = oracle.long_rows(rp, 4097, 1000)
+    assert ids.tolist() == [4, 5] and seg_begin.tolist() == [0, 5, 17]
+    ids, seg_begin = oracle.long_rows(rp, 20000, 4096)
+    assert ids.size == 0 and seg_begin.tolist() == [0]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_long_rows_cover_every_long_row_once(seed):
+    """Invariants: ascending, exactly the rows reaching the bound, and each
+    row's segments hold its nonzeros with the last one non-empty."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, 300, size=500)
+    lens[rng.integers(0, 500, size=20)] = rng.integers(300, 5000, size=20)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    S, L = 97, 150
+    ids, seg_begin = oracle.long_rows(rp, L, S)
+    assert np.all(np.diff(ids) > 0)
+    members = set(ids.tolist())
+    for i in range(500):
+        assert (i in members) == (lens[i] >= L)
+    counts = np.diff(seg_begin)
+    assert seg_begin[0] == 0
+    for t, i in enumerate(ids):
+        assert counts[t] * S >= lens[i] > (counts[t] - 1) * S

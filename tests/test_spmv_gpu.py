@@ -222,3 +222,37 @@ def test_invalid_csr_is_rejected(case):
         lb.Plan(torch.from_numpy(rp).cuda(), torch.from_numpy(col).cuda(),
                 torch.ones(nnz, dtype=torch.float32, device="cuda"), 3)
     assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("offset_what", ["matrix", "y", "x", "all"])
+def test_unaligned_pointers(dtype, offset_what):
+    """Arrays that start one element past a 16-byte boundary (slices of a
+    larger buffer): bulk copies need 16-byte aligned sources, so such
+    matrices (and y when beta != 0) take the plain-load staging path."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+
+    def shifted(a, shift):
+        t = torch.from_numpy(a).cuda()
+        if not shift:
+            return t
+        buf = torch.empty(a.size + 1, dtype=t.dtype, device="cuda")
+        buf[1:] = t
+        return buf[1:]
+
+    A, x, y0 = inputs(12000, 9000, 24, 11, dtype)
+    sm, sy, sx = (offset_what in ("matrix", "all"), offset_what in ("y", "all"), offset_what in ("x", "all"))
+    rp, col, val = shifted(A.row_ptr, sm), shifted(A.col_idx, sm), shifted(A.vals, sm)
+    assert (rp.data_ptr() % 16 != 0) == sm
+    for alpha, beta in [(1.0, 0.0), (1.5, 0.5)]:
+        for ipt in [8, 24]:
+            plan = lb.Plan(rp, col, val, A.n, kernel="merge_path", items_per_thread=ipt)
+            xd = shifted(x, sx)
+            yd = shifted(y0.copy(), sy)
+            plan(xd, yd, alpha, beta)
+            torch.cuda.synchronize()
+            assert plan.device_status() == 0
+            plan.close()
+            assert_close_to_oracle(A, x, yd.cpu().numpy(), alpha, beta, y0,
+                                   label=f"{offset_what} {dtype} ipt={ipt} beta={beta}")
