@@ -102,28 +102,28 @@ spmv_kernel_t env_kernel() {
 //  * small matrices: the same paper's rule (section 6.2) -- merge path unless
 //    (rows < 500 or columns < 500) and nnz < 10000 -- with rows capped at 256
 //    nonzeros so the sequential per-row sum stays accurate.
+//  * rows so even that a Row-grouped CSR copy with groups of 32 rows pads at
+//    most 10 % (the Row-grouped CSR page, section 4, names padding as the
+//    format's weakness): the Row-grouped kernel, which measured faster than
+//    merge path on such matrices (27-point stencil 128^3: 82.6 us against
+//    90.0 us; 5-point Laplacian 64x64: 8.2 us against 12.6 us) and 2-8x
+//    slower on irregular ones;
 //  * everything else: merge path.
 spmv_kernel_t choose_kernel(const spmv_plan_s &p) {
     const spmv_row_stats_t &s = p.stats;
     if (p.n == 1 && s.max_len <= 32) return SPMV_KERNEL_THREAD_ROW;
     if ((p.m < 500 || p.n < 500) && p.nnz < 10000 && s.max_len <= 256) return SPMV_KERNEL_THREAD_ROW;
+    if (p.nnz > 0 && (double)s.rg_slots[0] <= 1.1 * (double)p.nnz) return SPMV_KERNEL_RGCSR;
     return SPMV_KERNEL_MERGE_PATH;
 }
 
-// Row-grouped CSR group size: the largest G in {32, 64, 128, 256} whose
-// padding (rg_slots / nnz - 1, measured over all rows) is at most 10 %, else
-// the least padded one.  The Row-grouped CSR page found G >= 32 needed for
-// coalescing and 128 best on its hardware (section 4); larger groups mean
-// fewer group offsets but more padding.
-int choose_rgcsr_group(const spmv_row_stats_t &s, int64_t nnz) {
-    if (nnz <= 0) return 128;
-    for (int g = 3; g >= 0; --g)
-        if ((double)s.rg_slots[g] <= 1.1 * (double)nnz) return 32 << g;
-    int best = 0;
-    for (int g = 1; g < 4; ++g)
-        if (s.rg_slots[g] < s.rg_slots[best]) best = g;
-    return 32 << best;
-}
+// Row-grouped CSR group size: 32.  The Row-grouped CSR page needs G >= 32
+// for coalesced loads and found 128 best on its hardware (section 4), where
+// a warp read each level straight from global memory.  Here the copy is
+// staged by bulk copies and G = 32 makes a group one warp's rows, so warps
+// never synchronise; it also pads least (a group's padding is set by its
+// longest row, and smaller groups have shorter longest rows).
+int choose_rgcsr_group(const spmv_row_stats_t &, int64_t) { return 32; }
 
 // Rows in length classes that can hold a row of at least `len` nonzeros:
 // an upper bound on the number of long rows.
@@ -456,7 +456,7 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
         if (p->num_long_rows > 0) e = launch_long_part(p, x, y, alpha, beta, stream);
         if (e == cudaSuccess)
             e = launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->rg_col, p->rg_val, x, y,
-                                  alpha, beta, stream);
+                                  alpha, beta, p->device_error, stream);
         break;
     case SPMV_KERNEL_MERGE_PATH:
     default: {

@@ -111,9 +111,11 @@ cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *
                                   double alpha, double beta, int32_t skip_min_len, cudaStream_t stream);
 
 // Row-grouped CSR, thread per row (rows with row_len < 0 are skipped).
+// rg_col and rg_val must be 128-byte aligned (the plan allocates them).
 cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const int64_t *group_ptr,
                               const int32_t *row_len, const int32_t *rg_col, const void *rg_val,
-                              const void *x, void *y, double alpha, double beta, cudaStream_t stream);
+                              const void *x, void *y, double alpha, double beta, int32_t *error,
+                              cudaStream_t stream);
 
 // Long rows: one warp per segment of kLongSegmentNnz nonzeros; rows with
 // several segments are finished by the last segment to arrive.

@@ -1,5 +1,5 @@
 """The five workloads at full size, with the plan the benchmark times
-(kernel chosen automatically).  The oracle checks sampled rows one by one:
+(kernel chosen automatically) and with merge path.  The oracle checks sampled rows one by one:
 random rows, the first and last rows, the longest rows, the rows cut by
 merge-path tile boundaries and empty rows.  Two properties check every row:
 no row is skipped (y starts as NaN when beta = 0) and
@@ -28,8 +28,9 @@ def sample_rows(A, plan_info, part, seed=0):
     return np.unique(np.concatenate(pick)).astype(np.int32)
 
 
+@pytest.mark.parametrize("kernel", ["auto", "merge_path"])
 @pytest.mark.parametrize("name", synth.WORKLOADS)
-def test_full_size_workload(name):
+def test_full_size_workload(name, kernel):
     import torch
     import load_balanced_csr_gb300 as lb
     W = synth.workload(name)
@@ -40,8 +41,10 @@ def test_full_size_workload(name):
         yd = torch.from_numpy(W.y0.copy()).cuda()
     else:
         yd = torch.full((A.m,), float("nan"), dtype=val.dtype, device="cuda")
-    with lb.Plan(rp, col, val, A.n) as plan:
+    with lb.Plan(rp, col, val, A.n, kernel=kernel) as plan:
         info = plan.info()
+        if kernel == "auto" and info["kernel_name"] == "merge_path":
+            pytest.skip("the plan chose merge path: covered by the merge_path case")
         plan(xd, yd, W.alpha, W.beta)
         torch.cuda.synchronize()
         part = plan.export("partition") if info["kernel_name"] == "merge_path" else None
