@@ -63,13 +63,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the sources each product kernel is built from
+KERNEL_SOURCES = {
+    "merge_path": ["merge_path.cu", "tma.cuh", "internal.cuh"],
+    "rgcsr": ["rgcsr.cu", "long_rows.cu", "tma.cuh", "internal.cuh"],
+    "long_rows": ["long_rows.cu", "row_kernels.cu", "internal.cuh"],
+    "thread_row": ["row_kernels.cu", "internal.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of one kernel's sources (all of csrc/ when kernel is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "load_balanced_csr_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    names = KERNEL_SOURCES.get(kernel) if kernel else None
+    if names is None:
+        names = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh"))]
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -83,7 +95,7 @@ def recorded_traffic(workload: str, kernel: str):
     except Exception:
         return None, None
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None, None
     return e.get("dram_bytes_per_launch"), e.get("note")
 

@@ -101,7 +101,11 @@ spmv_kernel_t env_kernel() {
 //    (section 6.1): perfectly balanced work needs no balancing.
 //  * small matrices: the same paper's rule (section 6.2) -- merge path unless
 //    (rows < 500 or columns < 500) and nnz < 10000 -- with rows capped at 256
-//    nonzeros so the sequential per-row sum stays accurate.
+//    nonzeros so the per-row sum stays accurate; and on GB300 any matrix of
+//    at most 65,536 rows (one wave of thread-per-row CTAs) whose rows hold
+//    at most 64 nonzeros: such products are latency-bound, and one thread
+//    per row has the shortest chain (5-point Laplacian 64x64: 6.1 us, against
+//    8.1 us Row-grouped and 12.2 us merge path);
 //  * rows so even that a Row-grouped CSR copy with groups of 32 rows pads at
 //    most 10 % (the Row-grouped CSR page, section 4, names padding as the
 //    format's weakness): the Row-grouped kernel, which measured faster than
@@ -113,6 +117,7 @@ spmv_kernel_t choose_kernel(const spmv_plan_s &p) {
     const spmv_row_stats_t &s = p.stats;
     if (p.n == 1 && s.max_len <= 32) return SPMV_KERNEL_THREAD_ROW;
     if ((p.m < 500 || p.n < 500) && p.nnz < 10000 && s.max_len <= 256) return SPMV_KERNEL_THREAD_ROW;
+    if (p.m <= 65536 && s.max_len <= 64) return SPMV_KERNEL_THREAD_ROW;
     if (p.nnz > 0 && (double)s.rg_slots[0] <= 1.1 * (double)p.nnz) return SPMV_KERNEL_RGCSR;
     return SPMV_KERNEL_MERGE_PATH;
 }

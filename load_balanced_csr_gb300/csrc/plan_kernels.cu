@@ -123,44 +123,54 @@ row_stats_kernel(int32_t m, int32_t n, int32_t nnz, const int32_t *__restrict__ 
     }
 }
 
-// One CTA adds the per-CTA partials up in index order.
-__global__ void __launch_bounds__(64)
+// One CTA adds the per-CTA partials up: warp w reduces fields w, w + 32,
+// ... (0-31 the classes, 32-35 the Row-grouped slots, 36 the length sum,
+// 37 min, 38 max, 39 empty rows, 40 flags, 41 bandwidth), its lanes
+// striding over the partials.  Integer sums, minima and maxima do not
+// depend on the order.
+constexpr int kStatsFields = 42;
+
+__device__ __forceinline__ long long stats_field(const StatsPartial &q, int f) {
+    if (f < 32) return q.hist[f];
+    if (f < 36) return q.rg_slots[f - 32];
+    switch (f) {
+    case 36: return q.sum_len;
+    case 37: return q.min_len;
+    case 38: return q.max_len;
+    case 39: return q.n_empty;
+    case 40: return q.flags;
+    default: return q.bandwidth;
+    }
+}
+
+__global__ void __launch_bounds__(1024)
 stats_reduce_kernel(int num, const StatsPartial *__restrict__ partials, int32_t m,
                     spmv_row_stats_t *__restrict__ out) {
-    const int tid = threadIdx.x;
-    if (tid < 32) {
-        long long s = 0;
-        for (int b = 0; b < num; ++b) s += partials[b].hist[tid];
-        out->hist[tid] = s;
-    } else if (tid < 36) {
-        long long s = 0;
-        for (int b = 0; b < num; ++b) s += partials[b].rg_slots[tid - 32];
-        out->rg_slots[tid - 32] = s;
-    } else if (tid == 36) {
-        long long s = 0;
-        for (int b = 0; b < num; ++b) s += partials[b].sum_len;
-        out->sum_len = s;
-    } else if (tid == 37) {
-        int v = INT_MAX;
-        for (int b = 0; b < num; ++b) v = min(v, partials[b].min_len);
-        out->min_len = m > 0 ? v : 0;
-    } else if (tid == 38) {
-        int v = 0;
-        for (int b = 0; b < num; ++b) v = max(v, partials[b].max_len);
-        out->max_len = v;
-    } else if (tid == 39) {
-        int v = 0;
-        for (int b = 0; b < num; ++b) v += partials[b].n_empty;
-        out->n_empty = v;
-    } else if (tid == 40) {
-        int v = 0;
-        for (int b = 0; b < num; ++b) v |= partials[b].flags;
-        out->flags = v;
-    } else if (tid == 41) {
-        int v = 0;
-        for (int b = 0; b < num; ++b) v = max(v, partials[b].bandwidth);
-        out->bandwidth = m > 0 ? v : 0;
-        out->reserved = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int f = warp; f < kStatsFields; f += 32) {
+        const bool is_min = f == 37, is_max = f == 38 || f == 41, is_or = f == 40;
+        long long v = is_min ? (long long)INT_MAX : 0;
+        for (int b = lane; b < num; b += 32) {
+            const long long q = stats_field(partials[b], f);
+            v = is_min ? min(v, q) : is_max ? max(v, q) : is_or ? (v | q) : v + q;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const long long q = __shfl_xor_sync(0xffffffffu, v, off);
+            v = is_min ? min(v, q) : is_max ? max(v, q) : is_or ? (v | q) : v + q;
+        }
+        if (lane != 0) continue;
+        if (f < 32) out->hist[f] = v;
+        else if (f < 36) out->rg_slots[f - 32] = v;
+        else if (f == 36) out->sum_len = v;
+        else if (f == 37) out->min_len = m > 0 ? (int)v : 0;
+        else if (f == 38) out->max_len = (int)v;
+        else if (f == 39) out->n_empty = (int)v;
+        else if (f == 40) out->flags = (int)v;
+        else {
+            out->bandwidth = m > 0 ? (int)v : 0;
+            out->reserved = 0;
+        }
     }
 }
 
@@ -199,7 +209,7 @@ cudaError_t launch_row_stats(int32_t m, int32_t n, int32_t nnz, const int32_t *r
                                                              partials);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    stats_reduce_kernel<<<1, 64, 0, stream>>>(num_ctas, partials, m, out);
+    stats_reduce_kernel<<<1, 1024, 0, stream>>>(num_ctas, partials, m, out);
     return cudaGetLastError();
 }
 
