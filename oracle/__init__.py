@@ -104,6 +104,7 @@ def _bind(cdll):
         "oracle_rgcsr_pack_f64": [i32, vp, vp, vp, i32, vp, vp, vp],
         "oracle_rgcsr_pack_f32": [i32, vp, vp, vp, i32, vp, vp, vp],
         "oracle_long_rows": [i32, vp, i32, i32, vp, vp, ctypes.POINTER(i64)],
+        "oracle_window_sort": [i32, vp, i32, i32, vp, vp],
     }
     for name, argtypes in sig.items():
         f = getattr(cdll, name)
@@ -219,3 +220,14 @@ def long_rows(row_ptr, min_len: int, seg_nnz: int):
     if lib().oracle_long_rows(m, _p(row_ptr), min_len, seg_nnz, _p(ids), _p(seg_begin), ctypes.byref(count)):
         raise ValueError("oracle_long_rows: bad arguments")
     return ids, seg_begin
+
+
+def window_sort(row_ptr, window: int, long_min: int = 0):
+    """(perm, eff_len) of the window-sorted row order (quadratic: small inputs)."""
+    row_ptr = _i32(row_ptr)
+    m = len(row_ptr) - 1
+    perm = np.empty(m, dtype=np.int32)
+    eff = np.empty(m, dtype=np.int32)
+    if lib().oracle_window_sort(m, _p(row_ptr), window, long_min, _p(perm), _p(eff)):
+        raise ValueError("oracle_window_sort: bad arguments")
+    return perm, eff

@@ -238,3 +238,33 @@ int oracle_long_rows(int32_t m, const int32_t *row_ptr, int32_t min_len, int32_t
     *count = t;
     return 0;
 }
+
+/* Selection of the next row by (length descending, index ascending), one
+ * window at a time: the plainest statement of the order, quadratic in the
+ * window size. */
+int oracle_window_sort(int32_t m, const int32_t *row_ptr, int32_t window, int32_t long_min, int32_t *perm,
+                       int32_t *eff_len) {
+    if (!check_row_ptr_basic(m, row_ptr) || window < 1 || perm == NULL) return 1;
+    for (int32_t w0 = 0; w0 < m; w0 += window) {
+        int32_t w1 = w0 + window < m ? w0 + window : m;
+        for (int32_t p = w0; p < w1; ++p) perm[p] = -1;
+        for (int32_t p = w0; p < w1; ++p) {
+            int32_t best = -1, best_len = 0;
+            for (int32_t i = w0; i < w1; ++i) {
+                int taken = 0;
+                for (int32_t q = w0; q < p; ++q)
+                    if (perm[q] == i) taken = 1;
+                if (taken) continue;
+                int32_t len = row_ptr[i + 1] - row_ptr[i];
+                if (long_min > 0 && len >= long_min) len = -1;
+                if (best < 0 || len > best_len) {
+                    best = i;
+                    best_len = len;
+                }
+            }
+            perm[p] = best;
+            if (eff_len) eff_len[p] = best_len;
+        }
+    }
+    return 0;
+}

@@ -122,6 +122,19 @@ int oracle_rgcsr_pack_f32(int32_t m, const int32_t *row_ptr, const int32_t *col_
 int oracle_long_rows(int32_t m, const int32_t *row_ptr, int32_t min_len, int32_t seg_nnz, int32_t *ids,
                      int64_t *seg_begin, int64_t *count);
 
+/*
+ * Row order of the window-sorted Row-grouped layout (an extension of
+ * [RgCSR] section 3, whose weakness is the padding of a group to its
+ * longest row, section 4): inside each window of `window` consecutive rows
+ * (the last window may be shorter), rows are listed by decreasing length,
+ * equal lengths by increasing row index; rows of length >= long_min (when
+ * long_min > 0) count as length -1, i.e. they come last.  perm[p] (m
+ * entries) is the row at position p; eff_len[p] (may be NULL) its length,
+ * or -1 for a long row.  Returns 0, or 1 on bad arguments (window < 1).
+ */
+int oracle_window_sort(int32_t m, const int32_t *row_ptr, int32_t window, int32_t long_min, int32_t *perm,
+                       int32_t *eff_len);
+
 #ifdef __cplusplus
 }
 #endif

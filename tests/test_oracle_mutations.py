@@ -31,6 +31,10 @@ MUTATIONS = [
      [pins.test_long_rows_worked_example]),
     ("segment count rounds wrongly", "segs += ((int64_t)len + seg_nnz - 1) / seg_nnz;",
      "segs += (int64_t)len / seg_nnz + 1;", [pins.test_long_rows_worked_example]),
+    ("window sort ascending", "if (best < 0 || len > best_len) {", "if (best < 0 || len < best_len) {",
+     [pins.test_window_sort_worked_example]),
+    ("window sort ties by last index", "if (best < 0 || len > best_len) {", "if (best < 0 || len >= best_len) {",
+     [pins.test_window_sort_worked_example]),
 ]
 
 

@@ -383,3 +383,37 @@ def test_long_rows_cover_every_long_row_once(seed):
     assert seg_begin[0] == 0
     for t, i in enumerate(ids):
         assert counts[t] * S >= lens[i] > (counts[t] - 1) * S
+
+
+# ---------------------------------------------------------------- window-sorted rows
+
+
+def test_window_sort_worked_example():
+    """Lengths 2, 5, 0, 5, 1 | 3, 9, 3 in windows of 5, long rows from 9 on:
+    window 1 lists rows 1, 3 (length 5, by index), 0, 4, 2; window 2 lists
+    5, 7 (length 3) and then the long row 6 (sorted by hand)."""
+    lens = np.array([2, 5, 0, 5, 1, 3, 9, 3])
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    perm, eff = oracle.window_sort(rp, 5, 9)
+    assert perm.tolist() == [1, 3, 0, 4, 2, 5, 7, 6]
+    assert eff.tolist() == [5, 5, 2, 1, 0, 3, 3, -1]
+    perm, eff = oracle.window_sort(rp, 5, 0)  # no long rows
+    assert perm.tolist() == [1, 3, 0, 4, 2, 6, 5, 7]
+    perm, _ = oracle.window_sort(rp, 1, 0)  # windows of one row: identity
+    assert perm.tolist() == list(range(8))
+
+
+@pytest.mark.parametrize("window", [1, 32, 96, 1000])
+def test_window_sort_invariants(window):
+    """A permutation that never leaves its window, lengths non-increasing
+    inside a window, ties in index order."""
+    A = synth.random_csr(777, 300, max_len=9, empty_frac=0.2, seed=window)
+    perm, eff = oracle.window_sort(A.row_ptr, window, 7)
+    lens = np.diff(A.row_ptr)
+    assert sorted(perm.tolist()) == list(range(A.m))
+    for p in range(A.m):
+        assert p // window == perm[p] // window
+        want = -1 if lens[perm[p]] >= 7 else lens[perm[p]]
+        assert eff[p] == want
+        if p + 1 < A.m and (p + 1) // window == p // window:
+            assert eff[p] > eff[p + 1] or (eff[p] == eff[p + 1] and perm[p] < perm[p + 1])
