@@ -11,6 +11,7 @@
 #include "oracle.h"
 
 #include <stddef.h>
+#include <stdlib.h>
 
 static int check_row_ptr_basic(int32_t m, const int32_t *row_ptr) {
     return m >= 0 && row_ptr != NULL;
@@ -245,16 +246,15 @@ int oracle_long_rows(int32_t m, const int32_t *row_ptr, int32_t min_len, int32_t
 int oracle_window_sort(int32_t m, const int32_t *row_ptr, int32_t window, int32_t long_min, int32_t *perm,
                        int32_t *eff_len) {
     if (!check_row_ptr_basic(m, row_ptr) || window < 1 || perm == NULL) return 1;
+    char *taken = (char *)malloc((size_t)window);
+    if (!taken) return 1;
     for (int32_t w0 = 0; w0 < m; w0 += window) {
         int32_t w1 = w0 + window < m ? w0 + window : m;
-        for (int32_t p = w0; p < w1; ++p) perm[p] = -1;
+        for (int32_t i = w0; i < w1; ++i) taken[i - w0] = 0;
         for (int32_t p = w0; p < w1; ++p) {
             int32_t best = -1, best_len = 0;
             for (int32_t i = w0; i < w1; ++i) {
-                int taken = 0;
-                for (int32_t q = w0; q < p; ++q)
-                    if (perm[q] == i) taken = 1;
-                if (taken) continue;
+                if (taken[i - w0]) continue;
                 int32_t len = row_ptr[i + 1] - row_ptr[i];
                 if (long_min > 0 && len >= long_min) len = -1;
                 if (best < 0 || len > best_len) {
@@ -263,8 +263,10 @@ int oracle_window_sort(int32_t m, const int32_t *row_ptr, int32_t window, int32_
                 }
             }
             perm[p] = best;
+            taken[best - w0] = 1;
             if (eff_len) eff_len[p] = best_len;
         }
     }
+    free(taken);
     return 0;
 }
