@@ -63,8 +63,11 @@ typedef enum {
     SPMV_KERNEL_THREAD_ROW = 2, /* one thread per row */
     SPMV_KERNEL_RGCSR = 3,      /* Row-grouped CSR (interleaved copy of A built by the plan);
                                    long rows, if any, by the long-row kernel */
-    SPMV_KERNEL_LONG_ROWS = 4   /* long rows by the long-row kernel (one warp per segment of
+    SPMV_KERNEL_LONG_ROWS = 4,  /* long rows by the long-row kernel (one warp per segment of
                                    4096 nonzeros), the other rows one thread per row */
+    SPMV_KERNEL_RGCSR_SORTED = 5 /* Row-grouped CSR (groups of 32) over the rows listed, in
+                                   each window of 1024 rows, by decreasing length, which
+                                   cuts the padding; long rows by the long-row kernel */
 } spmv_kernel_t;
 
 /* Options for spmv_plan_create_ex; zero-initialise and set what you need. */
@@ -128,11 +131,13 @@ typedef struct {
 typedef enum {
     SPMV_EXPORT_PARTITION = 0,   /* int32 pairs (row, nonzero), num_tiles + 1 of them */
     SPMV_EXPORT_RG_GROUP_PTR = 1,/* int64[ceil(m/G) + 1] */
-    SPMV_EXPORT_RG_ROW_LEN = 2,  /* int32[m]: row length, -1 for a row left to the long-row kernel */
+    SPMV_EXPORT_RG_ROW_LEN = 2,  /* int32[m] by position: row length, -1 for a row left to the
+                                    long-row kernel */
     SPMV_EXPORT_RG_COL = 3,      /* int32[group_ptr[last]] */
     SPMV_EXPORT_RG_VAL = 4,      /* value type [group_ptr[last]] */
     SPMV_EXPORT_LONG_ROWS = 5,   /* int32[num_long_rows], ascending */
-    SPMV_EXPORT_LONG_SEG_BEGIN = 6 /* int64[num_long_rows + 1]: first segment of each long row */
+    SPMV_EXPORT_LONG_SEG_BEGIN = 6,/* int64[num_long_rows + 1]: first segment of each long row */
+    SPMV_EXPORT_RG_PERM = 7      /* int32[m]: the row at each position of the window-sorted copy */
 } spmv_export_t;
 
 /*

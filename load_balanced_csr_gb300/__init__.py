@@ -18,10 +18,10 @@ from . import _build
 
 __all__ = ["Plan", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
 
-KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4}
+KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4, "rgcsr_sorted": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 EXPORTS = {"partition": 0, "rg_group_ptr": 1, "rg_row_len": 2, "rg_col": 3, "rg_val": 4, "long_rows": 5,
-           "long_seg_begin": 6}
+           "long_seg_begin": 6, "rg_perm": 7}
 STATUS = {0: "ok", 1: "invalid argument", 2: "invalid CSR matrix", 3: "allocation failed", 4: "CUDA error",
           5: "unsupported"}
 
@@ -199,7 +199,7 @@ class Plan:
         need = ctypes.c_size_t(0)
         check(lib().spmv_plan_export(self._h, code, None, 0, ctypes.byref(need)), "spmv_plan_export")
         dtype = {"partition": np.int32, "rg_group_ptr": np.int64, "rg_row_len": np.int32, "rg_col": np.int32,
-                 "long_rows": np.int32, "long_seg_begin": np.int64,
+                 "long_rows": np.int32, "long_seg_begin": np.int64, "rg_perm": np.int32,
                  "rg_val": np.float64 if str(self.dtype) == "torch.float64" else np.float32}[what]
         buf = np.empty(need.value // np.dtype(dtype).itemsize, dtype=dtype)
         check(lib().spmv_plan_export(self._h, code, buf.ctypes.data if buf.size else None, need.value, None),

@@ -53,7 +53,8 @@ struct spmv_plan_s {
     int64_t ngroups = 0;
     int64_t rg_slots = 0;
     int64_t *group_ptr = nullptr;    // [ngroups + 1]
-    int32_t *row_len = nullptr;      // [m]
+    int32_t *row_len = nullptr;      // [m] by position
+    int32_t *perm = nullptr;         // [m] row at each position (window-sorted copy only)
     void *rg = nullptr;
     size_t rg_bytes = 0;
     int32_t *rg_col = nullptr;       // [rg_slots]
@@ -92,6 +93,7 @@ spmv_kernel_t env_kernel() {
     if (!std::strcmp(v, "thread_row")) return SPMV_KERNEL_THREAD_ROW;
     if (!std::strcmp(v, "rgcsr")) return SPMV_KERNEL_RGCSR;
     if (!std::strcmp(v, "long_rows")) return SPMV_KERNEL_LONG_ROWS;
+    if (!std::strcmp(v, "rgcsr_sorted")) return SPMV_KERNEL_RGCSR_SORTED;
     return SPMV_KERNEL_AUTO;
 }
 
@@ -153,9 +155,12 @@ constexpr int32_t kDefaultLongRowMin = 512;
 // The long-row list and, for the Row-grouped kernel, its layout and copy of
 // A.  Two passes over row_ptr per structure, sized on the host from the
 // statistics where they bound it, read back where they do not.
+bool is_rgcsr(spmv_kernel_t k) { return k == SPMV_KERNEL_RGCSR || k == SPMV_KERNEL_RGCSR_SORTED; }
+
 spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaStream_t stream) {
     const int32_t m = p->m;
-    const bool rgcsr = p->kernel == SPMV_KERNEL_RGCSR;
+    const bool rgcsr = is_rgcsr(p->kernel);
+    const bool sorted = p->kernel == SPMV_KERNEL_RGCSR_SORTED;
     p->long_min = opt.long_row_min ? opt.long_row_min : kDefaultLongRowMin;
     const bool has_long = m > 0 && p->stats.max_len >= p->long_min;
     const size_t vs = value_size(p->dtype);
@@ -164,7 +169,7 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
     const int64_t long_ub = has_long ? rows_at_least(p->stats, p->long_min) : 0;
     const int64_t segs_ub = has_long ? (int64_t)p->nnz / kLongSegmentNnz + long_ub : 0;
     if (rgcsr) {
-        const int G = opt.rgcsr_group ? opt.rgcsr_group : choose_rgcsr_group(p->stats, p->nnz);
+        const int G = sorted ? 32 : opt.rgcsr_group ? opt.rgcsr_group : choose_rgcsr_group(p->stats, p->nnz);
         p->rgcsr_group = G;
         p->g_log2 = 0;
         while ((1 << p->g_log2) < G) ++p->g_log2;
@@ -187,6 +192,7 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
     const size_t o_crow_off = take(sizeof(int64_t) * (nc + 1));
     const size_t o_cseg_off = take(sizeof(int64_t) * (nc + 1));
     const size_t o_rlen = take(rgcsr ? sizeof(int32_t) * m : 0);
+    const size_t o_perm = take(sorted ? sizeof(int32_t) * m : 0);
     const size_t o_gsize = take(rgcsr ? sizeof(int64_t) * p->ngroups : 0);
     const size_t o_gp = take(rgcsr ? sizeof(int64_t) * (p->ngroups + 1) : 0);
     const size_t o_scr = take(sizeof(int64_t) * scan_scratch_elems(scan_n));
@@ -211,6 +217,7 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
         p->row_len = reinterpret_cast<int32_t *>(base + o_rlen);
         p->group_ptr = reinterpret_cast<int64_t *>(base + o_gp);
     }
+    if (sorted) p->perm = reinterpret_cast<int32_t *>(base + o_perm);
 
     // sizes read back: long rows, segments, Row-grouped slots
     int64_t sizes[3] = {0, 0, 0};
@@ -228,7 +235,11 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
             e = cudaMemcpyAsync(&sizes[1], chunk_seg_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     }
     if (e == cudaSuccess && rgcsr && m > 0) {
-        e = launch_rgcsr_lengths(m, p->row_ptr, p->g_log2, has_long ? p->long_min : 0, p->row_len, gsize, stream);
+        if (sorted)
+            e = launch_window_sort(m, p->row_ptr, has_long ? p->long_min : 0, p->perm, p->row_len, gsize, stream);
+        else
+            e = launch_rgcsr_lengths(m, p->row_ptr, p->g_log2, has_long ? p->long_min : 0, p->row_len, gsize,
+                                     stream);
         if (e == cudaSuccess) e = launch_exclusive_scan(gsize, p->ngroups, p->group_ptr, scratch, stream);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(&sizes[2], p->group_ptr + p->ngroups, sizeof(int64_t), cudaMemcpyDeviceToHost,
@@ -257,7 +268,7 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
         e = cudaMemsetAsync(p->rg, 0, p->rg_bytes, stream);  // pads: column 0, value 0
         if (e == cudaSuccess)
             e = launch_rgcsr_pack(p->dtype, m, p->row_ptr, p->col_idx, p->vals, p->g_log2, p->group_ptr, p->row_len,
-                                  p->rg_col, p->rg_val, true, stream);
+                                  p->perm, p->rg_col, p->rg_val, true, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) return cuda_fail(e, "Row-grouped copy");
     }
@@ -324,7 +335,7 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     if (options) opt = *options;
     spmv_kernel_t forced = (spmv_kernel_t)opt.kernel;
     if (forced == SPMV_KERNEL_AUTO) forced = env_kernel();
-    if (forced < SPMV_KERNEL_AUTO || forced > SPMV_KERNEL_LONG_ROWS)
+    if (forced < SPMV_KERNEL_AUTO || forced > SPMV_KERNEL_RGCSR_SORTED)
         return fail(SPMV_ERR_INVALID_ARG, "unknown kernel option");
     if (opt.rgcsr_group && opt.rgcsr_group != 32 && opt.rgcsr_group != 64 && opt.rgcsr_group != 128 &&
         opt.rgcsr_group != 256)
@@ -427,7 +438,7 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
             return cuda_fail(e, "merge-path partition");
         }
     }
-    if (p->kernel == SPMV_KERNEL_RGCSR || p->kernel == SPMV_KERNEL_LONG_ROWS) {
+    if (is_rgcsr(p->kernel) || p->kernel == SPMV_KERNEL_LONG_ROWS) {
         const spmv_status_t st = build_row_layouts(p, opt, stream);
         if (st != SPMV_OK) {
             destroy_plan(p);
@@ -458,10 +469,11 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
                                       p->num_long_rows > 0 ? p->long_min : 0, stream);
         break;
     case SPMV_KERNEL_RGCSR:
+    case SPMV_KERNEL_RGCSR_SORTED:
         if (p->num_long_rows > 0) e = launch_long_part(p, x, y, alpha, beta, stream);
         if (e == cudaSuccess)
-            e = launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->rg_col, p->rg_val, x, y,
-                                  alpha, beta, p->device_error, stream);
+            e = launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->perm, p->rg_col, p->rg_val,
+                                  x, y, alpha, beta, p->device_error, stream);
         break;
     case SPMV_KERNEL_MERGE_PATH:
     default: {
@@ -493,10 +505,10 @@ spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stre
     if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
     if (!vals && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "vals is NULL");
     p->vals = vals;
-    if (p->kernel == SPMV_KERNEL_RGCSR && p->rg_slots > 0) {
+    if (is_rgcsr(p->kernel) && p->rg_slots > 0) {
         // the pattern is unchanged: only the values move into the copy
         const cudaError_t e = launch_rgcsr_pack(p->dtype, p->m, p->row_ptr, p->col_idx, vals, p->g_log2, p->group_ptr,
-                                                p->row_len, p->rg_col, p->rg_val, false,
+                                                p->row_len, p->perm, p->rg_col, p->rg_val, false,
                                                 reinterpret_cast<cudaStream_t>(stream_handle));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_update_values");
     }
@@ -555,7 +567,7 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
     case SPMV_EXPORT_RG_ROW_LEN:
     case SPMV_EXPORT_RG_COL:
     case SPMV_EXPORT_RG_VAL:
-        if (p->kernel != SPMV_KERNEL_RGCSR) return fail(SPMV_ERR_INVALID_ARG, "plan has no Row-grouped copy");
+        if (!is_rgcsr(p->kernel)) return fail(SPMV_ERR_INVALID_ARG, "plan has no Row-grouped copy");
         if (what == SPMV_EXPORT_RG_GROUP_PTR) {
             src = p->group_ptr;
             size = sizeof(int64_t) * (size_t)(p->ngroups + 1);
@@ -572,7 +584,7 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
         break;
     case SPMV_EXPORT_LONG_ROWS:
     case SPMV_EXPORT_LONG_SEG_BEGIN:
-        if (p->kernel != SPMV_KERNEL_RGCSR && p->kernel != SPMV_KERNEL_LONG_ROWS)
+        if (!is_rgcsr(p->kernel) && p->kernel != SPMV_KERNEL_LONG_ROWS)
             return fail(SPMV_ERR_INVALID_ARG, "plan has no long-row list");
         if (what == SPMV_EXPORT_LONG_ROWS) {
             src = p->long_rows;
@@ -581,6 +593,11 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
             src = p->seg_begin;
             size = p->num_long_rows > 0 ? sizeof(int64_t) * (size_t)(p->num_long_rows + 1) : 0;
         }
+        break;
+    case SPMV_EXPORT_RG_PERM:
+        if (p->kernel != SPMV_KERNEL_RGCSR_SORTED) return fail(SPMV_ERR_INVALID_ARG, "plan has no row order");
+        src = p->perm;
+        size = sizeof(int32_t) * (size_t)p->m;
         break;
     default: return fail(SPMV_ERR_INVALID_ARG, "plan does not hold this array");
     }

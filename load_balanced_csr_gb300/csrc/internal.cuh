@@ -100,9 +100,17 @@ cudaError_t launch_long_rows_scatter(int32_t m, const int32_t *row_ptr, int32_t 
 // group_ptr; then the interleaved copy (pads must be zero beforehand).
 cudaError_t launch_rgcsr_lengths(int32_t m, const int32_t *row_ptr, int g_log2, int32_t long_min,
                                  int32_t *row_len, int64_t *gsize, cudaStream_t stream);
+// Window-sorted order (windows of kSortWindow rows, groups of 32): perm[p]
+// is the row at position p, eff_len[p] its length (-1 for a long row),
+// gsize[g] = 32 * longest row of group g.
+constexpr int kSortWindow = 1024;
+cudaError_t launch_window_sort(int32_t m, const int32_t *row_ptr, int32_t long_min, int32_t *perm,
+                               int32_t *eff_len, int64_t *gsize, cudaStream_t stream);
+// perm: the row at each position (null: position = row).
 cudaError_t launch_rgcsr_pack(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
                               const void *vals, int g_log2, const int64_t *group_ptr, const int32_t *row_len,
-                              int32_t *rg_col, void *rg_val, bool pack_cols, cudaStream_t stream);
+                              const int32_t *perm, int32_t *rg_col, void *rg_val, bool pack_cols,
+                              cudaStream_t stream);
 
 // ---------------------------------------------------------------- row kernels
 // Thread per row; rows of length >= skip_min_len (when > 0) are skipped.
@@ -112,10 +120,11 @@ cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *
 
 // Row-grouped CSR, thread per row (rows with row_len < 0 are skipped).
 // rg_col and rg_val must be 128-byte aligned (the plan allocates them).
+// perm (G = 32 only): the row at each position, null for the natural order.
 cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const int64_t *group_ptr,
-                              const int32_t *row_len, const int32_t *rg_col, const void *rg_val,
-                              const void *x, void *y, double alpha, double beta, int32_t *error,
-                              cudaStream_t stream);
+                              const int32_t *row_len, const int32_t *perm, const int32_t *rg_col,
+                              const void *rg_val, const void *x, void *y, double alpha, double beta,
+                              int32_t *error, cudaStream_t stream);
 
 // Long rows: one warp per segment of kLongSegmentNnz nonzeros; rows with
 // several segments are finished by the last segment to arrive.

@@ -6,7 +6,7 @@
 // Algorithms 1 and 2): a first pass counts, a prefix sum turns the counts
 // into offsets, a second pass writes each row id to its place.  OpSparse
 // places rows with shared-memory atomics, so the order inside a bin is
-// arbitrary; here each CTA ranks its rows with warp ballots instead, which
+// arbitrary; here each CTA ranks its rows with a prefix sum instead, which
 // keeps the list in ascending row order (the same plan every time).
 //
 // Row-grouped CSR ("New Row-grouped CSR format for storing the sparse
@@ -14,6 +14,10 @@
 // are taken in groups of G; the k-th nonzeros of a group's rows are stored
 // next to each other, and every row of the group is padded to the group's
 // longest row.  The group offsets are the prefix sum of G * longest row.
+// The page names that padding as the format's weakness (section 4); the
+// window-sorted variant lists the rows of each window of kSortWindow rows
+// by decreasing length first, so that a group's rows have nearly equal
+// lengths.
 #include "internal.cuh"
 
 namespace lbcsr {
@@ -193,22 +197,66 @@ rgcsr_lengths_kernel(int32_t m, const int32_t *__restrict__ rp, int g_log2, int3
     }
 }
 
-// The interleaved copy: element k of row i goes to group_ptr[i / G] + k*G +
-// (i mod G).  One thread per row; at every k the threads of a warp write
-// neighbouring slots.
+// Window-sorted order: one CTA per window of kSortWindow rows sorts the keys
+// (length descending, row ascending; long rows count as length -1) with a
+// bitonic network in shared memory.  Keys are unique (they hold the row), so
+// the order is the same every time.  Position p gets perm[p], its length
+// eff_len[p], and the first position of every group of 32 -- the group's
+// longest row, as lengths fall inside a window -- sets the group's size.
+__global__ void __launch_bounds__(kSortWindow)
+window_sort_kernel(int32_t m, const int32_t *__restrict__ rp, int32_t long_min, int32_t *__restrict__ perm,
+                   int32_t *__restrict__ eff_len, int64_t *__restrict__ gsize) {
+    __shared__ unsigned long long keys[kSortWindow];
+    const int t = threadIdx.x;
+    const int64_t r = (int64_t)blockIdx.x * kSortWindow + t;
+    unsigned long long key = ~0ull;  // past the last row: sorts last
+    if (r < m) {
+        const int len = rp[r + 1] - rp[r];
+        const int eff = long_min > 0 && len >= long_min ? -1 : len;
+        key = ((unsigned long long)(0x7fffffffLL - eff) << 32) | (unsigned long long)(uint32_t)r;
+    }
+    keys[t] = key;
+    __syncthreads();
+    for (int k = 2; k <= kSortWindow; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int partner = t ^ j;
+            if (partner > t) {
+                const unsigned long long a = keys[t], b = keys[partner];
+                const bool ascending = (t & k) == 0;
+                if ((a > b) == ascending) {
+                    keys[t] = b;
+                    keys[partner] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (r < m) {  // positions of this window are its rows' slots
+        const unsigned long long kk = keys[t];
+        const int eff = (int)(0x7fffffffLL - (long long)(kk >> 32));
+        perm[r] = (int32_t)(kk & 0xffffffffull);
+        eff_len[r] = eff;
+        if ((t & 31) == 0) gsize[r >> 5] = 32LL * (eff > 0 ? eff : 0);
+    }
+}
+
+// The interleaved copy: element k of the row at position i goes to
+// group_ptr[i / G] + k*G + (i mod G); the row is perm[i] (i itself when perm
+// is null).  One thread per position; at every k the threads of a warp
+// write neighbouring slots.
 template <typename V>
 __global__ void __launch_bounds__(256)
 rgcsr_pack_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
                   const V *__restrict__ val, int g_log2, const int64_t *__restrict__ gp,
-                  const int32_t *__restrict__ row_len, int32_t *__restrict__ rg_col, V *__restrict__ rg_val,
-                  bool pack_cols) {
+                  const int32_t *__restrict__ row_len, const int32_t *__restrict__ perm, int32_t *__restrict__ rg_col,
+                  V *__restrict__ rg_val, bool pack_cols) {
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     if (i >= m) return;
     const int len = row_len[i];
     if (len <= 0) return;
     const int G = 1 << g_log2;
     const int64_t base = gp[i >> g_log2] + (i & (G - 1));
-    const int32_t b = rp[i];
+    const int32_t b = rp[perm ? perm[i] : i];
     for (int k = 0; k < len; ++k) {
         if (pack_cols) rg_col[base + (int64_t)k * G] = col[b + k];
         rg_val[base + (int64_t)k * G] = val[b + k];
@@ -258,18 +306,27 @@ cudaError_t launch_rgcsr_lengths(int32_t m, const int32_t *row_ptr, int g_log2, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_window_sort(int32_t m, const int32_t *row_ptr, int32_t long_min, int32_t *perm,
+                               int32_t *eff_len, int64_t *gsize, cudaStream_t stream) {
+    if (m <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)(((int64_t)m + kSortWindow - 1) / kSortWindow);
+    window_sort_kernel<<<blocks, kSortWindow, 0, stream>>>(m, row_ptr, long_min, perm, eff_len, gsize);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rgcsr_pack(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
                               const void *vals, int g_log2, const int64_t *group_ptr, const int32_t *row_len,
-                              int32_t *rg_col, void *rg_val, bool pack_cols, cudaStream_t stream) {
+                              const int32_t *perm, int32_t *rg_col, void *rg_val, bool pack_cols,
+                              cudaStream_t stream) {
     if (m <= 0) return cudaSuccess;
     const unsigned blocks = (unsigned)(((int64_t)m + 255) / 256);
     if (dtype == SPMV_F64)
         rgcsr_pack_kernel<double><<<blocks, 256, 0, stream>>>(m, row_ptr, col_idx, static_cast<const double *>(vals),
-                                                              g_log2, group_ptr, row_len, rg_col,
+                                                              g_log2, group_ptr, row_len, perm, rg_col,
                                                               static_cast<double *>(rg_val), pack_cols);
     else
         rgcsr_pack_kernel<float><<<blocks, 256, 0, stream>>>(m, row_ptr, col_idx, static_cast<const float *>(vals),
-                                                             g_log2, group_ptr, row_len, rg_col,
+                                                             g_log2, group_ptr, row_len, perm, rg_col,
                                                              static_cast<float *>(rg_val), pack_cols);
     return cudaGetLastError();
 }

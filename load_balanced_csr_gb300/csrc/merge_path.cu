@@ -393,7 +393,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
                 V res = sum;
                 if (p.mode & 1) res = p.alpha * res;
                 if (with_y) res = fma(p.beta, sv.yo[q], res);
-                p.y[i0 + q] = res;
+                store_stream(p.y + i0 + q, res, stream_pol);
             }
         }
         if (cut_head) {

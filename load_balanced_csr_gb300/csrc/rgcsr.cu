@@ -15,7 +15,8 @@
 // neighbouring columns whenever the matrix is banded.
 //
 // With G = 32 (the default: it pads least) a group is exactly one warp's
-// rows, so warps work independently, as in the merge-path kernel: each warp
+// rows -- in the natural order or, for the window-sorted copy, the rows the
+// plan lists at the group's 32 positions -- so warps work independently, as in the merge-path kernel: each warp
 // owns a contiguous run of groups and its own two-stage copy pipeline, and
 // never waits for another warp.  Larger groups take a CTA of G threads per
 // group, which must meet at a barrier before each stage is refilled; CTAs
@@ -42,6 +43,7 @@ struct RgParams {
     long long ngroups;
     const int64_t *gp;
     const int32_t *row_len;
+    const int32_t *perm;  // row at each position (null: the natural order; G = 32 only)
     const int32_t *rg_col;
     const V *rg_val;
     const V *x;
@@ -188,7 +190,7 @@ rgcsr_tma_kernel(const RgParams<V> p) {
                 for (int u = 0; u + w < U; u += 2 * w) acc[u] += acc[u + w];
             V r = p.alpha * acc[0];
             if (p.beta != V(0)) r = fma(p.beta, p.y[row], r);
-            p.y[row] = r;
+            store_stream(p.y + row, r, stream_pol);
         }
     }
 }
@@ -212,6 +214,30 @@ size_t rg_warp_region(int levels) {
     return 128 + kWarpStages * rg_stage_bytes<V>(32, levels);
 }
 
+// Copy chunk c of the group whose slots are [b, e) into a stage.
+template <typename V>
+__device__ __forceinline__ void rg_issue_slots(const RgParams<V> &p, unsigned char *stage, uint64_t *bar,
+                                               long long b, long long e, int c, uint64_t pol) {
+    const int G = 1 << p.g_log2;
+    const long long L = (e - b) >> p.g_log2;
+    const long long lev0 = (long long)c * p.levels;
+    const long long nlev = L - lev0 < p.levels ? L - lev0 : p.levels;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (nlev <= 0) {
+        mbar_expect_tx(bar, 0);
+        return;
+    }
+    const uint32_t n = (uint32_t)(nlev * G);
+    mbar_expect_tx(bar, n * (uint32_t)(sizeof(int) + sizeof(V)));
+    const long long s0 = b + lev0 * G;
+    bulk_copy(stage, p.rg_col + s0, n * (uint32_t)sizeof(int), bar, pol);
+    bulk_copy(stage + (size_t)p.levels * G * sizeof(int), p.rg_val + s0, n * (uint32_t)sizeof(V), bar, pol);
+}
+
+// Everything a group needs besides its slots -- its slot range, and per lane
+// the length, row and old y of the lane's position -- is loaded one group
+// ahead, so that no dependent global load sits between two groups (groups
+// of short rows hold only a few dozen nonzeros).
 template <typename V>
 __global__ void __launch_bounds__(kWarpThreads)
 rgcsr_warp_kernel(const RgParams<V> p) {
@@ -221,42 +247,73 @@ rgcsr_warp_kernel(const RgParams<V> p) {
     const int warp = threadIdx.x >> 5;
     const long long me = (long long)blockIdx.x * (kWarpThreads / 32) + warp;
     if (me >= p.num_warps) return;  // warps never wait for each other
-    const long long g_begin = me * p.ngroups / p.num_warps;
-    const long long g_end = (me + 1) * p.ngroups / p.num_warps;
+    const long long ng = p.ngroups;
+    const long long g_begin = me * ng / p.num_warps;
+    const long long g_end = (me + 1) * ng / p.num_warps;
     const size_t sbytes = rg_stage_bytes<V>(32, p.levels);
     unsigned char *region = dsm + (size_t)warp * (128 + kWarpStages * sbytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(region);
     unsigned char *stages = region + 128;
     const uint64_t stream_pol = l2_policy_evict_first();
     const uint64_t x_pol = l2_policy_evict_last();
+    const bool with_y = p.beta != V(0);
     if (lane == 0) {
         for (int s = 0; s < kWarpStages; ++s) mbar_init(bars + s);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
 
-    // issue cursor (lane 0): the item kWarpStages ahead of the one in use
-    long long ig = g_begin;
+    // issue cursor (lane 0): chunk ic of group ig, slots [ib, ie); the end of
+    // group ig + 1 is already loaded
+    long long ig = g_begin, ib = 0, ie = 0, ie_next = 0;
     int ic = 0;
     if (lane == 0) {
+        ib = p.gp[ig];
+        ie = p.gp[ig + 1];
+        ie_next = ig + 2 <= ng ? p.gp[ig + 2] : ie;
         for (int s = 0; s < kWarpStages && ig < g_end; ++s) {
-            rg_issue(p, stages + s * sbytes, bars + s, ig, ic, stream_pol);
-            const long long L = (p.gp[ig + 1] - p.gp[ig]) >> 5;
-            if (++ic == rg_chunks(L, p.levels)) {
+            rg_issue_slots(p, stages + s * sbytes, bars + s, ib, ie, ic, stream_pol);
+            if (++ic == rg_chunks((ie - ib) >> 5, p.levels)) {
                 ic = 0;
                 ++ig;
+                ib = ie;
+                ie = ie_next;
+                ie_next = ig + 2 <= ng ? p.gp[ig + 2] : ie;
             }
         }
     }
 
+    // compute cursor: group g, slots [gb, ge), the next group's end ge_next
+    long long gb = p.gp[g_begin], ge = p.gp[g_begin + 1];
+    long long ge_next = g_begin + 2 <= ng ? p.gp[g_begin + 2] : ge;
+    int len_n = -1;
+    long long row_n = 0;
+    V yo_n = V(0);
+    {
+        const long long q = g_begin * 32 + lane;
+        if (q < p.m) {
+            len_n = p.row_len[q];
+            row_n = p.perm ? p.perm[q] : q;
+            if (with_y && len_n >= 0) yo_n = p.y[row_n];
+        }
+    }
     long long it = 0;
-    int len_next = g_begin * 32 + lane < p.m ? p.row_len[g_begin * 32 + lane] : -1;
     for (long long g = g_begin; g < g_end; ++g) {
-        const long long L = (p.gp[g + 1] - p.gp[g]) >> 5;
-        const int nch = rg_chunks(L, p.levels);
-        const long long row = g * 32 + lane;
-        const int len = len_next;
-        if (g + 1 < g_end) len_next = row + 32 < p.m ? p.row_len[row + 32] : -1;
+        const int nch = rg_chunks((ge - gb) >> 5, p.levels);
+        const int len = len_n;
+        const long long row = row_n;  // the row at this lane's position
+        const V yo = yo_n;
+        long long ge_nn = ge_next;
+        len_n = -1;
+        if (g + 1 < g_end) {
+            const long long q = (g + 1) * 32 + lane;
+            if (q < p.m) {
+                len_n = p.row_len[q];
+                row_n = p.perm ? p.perm[q] : q;
+                if (with_y && len_n >= 0) yo_n = p.y[row_n];
+            }
+            if (g + 3 <= ng) ge_nn = p.gp[g + 3];
+        }
         V acc[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) acc[u] = V(0);
@@ -290,11 +347,13 @@ rgcsr_warp_kernel(const RgParams<V> p) {
                     acc[u] = fma(sval[(k + u) * 32 + lane], gather_keep(p.x + scol[(k + u) * 32 + lane], x_pol), acc[u]);
             __syncwarp();  // the stage is free
             if (lane == 0 && ig < g_end) {
-                rg_issue(p, stages + s * sbytes, bars + s, ig, ic, stream_pol);
-                const long long Li = (p.gp[ig + 1] - p.gp[ig]) >> 5;
-                if (++ic == rg_chunks(Li, p.levels)) {
+                rg_issue_slots(p, stages + s * sbytes, bars + s, ib, ie, ic, stream_pol);
+                if (++ic == rg_chunks((ie - ib) >> 5, p.levels)) {
                     ic = 0;
                     ++ig;
+                    ib = ie;
+                    ie = ie_next;
+                    ie_next = ig + 2 <= ng ? p.gp[ig + 2] : ie;
                 }
             }
         }
@@ -304,9 +363,12 @@ rgcsr_warp_kernel(const RgParams<V> p) {
 #pragma unroll
                 for (int u = 0; u + w < U; u += 2 * w) acc[u] += acc[u + w];
             V r = p.alpha * acc[0];
-            if (p.beta != V(0)) r = fma(p.beta, p.y[row], r);
-            p.y[row] = r;
+            if (with_y) r = fma(p.beta, yo, r);
+            store_stream(p.y + row, r, stream_pol);
         }
+        gb = ge;
+        ge = ge_next;
+        ge_next = ge_nn;
     }
 }
 
@@ -345,16 +407,18 @@ size_t rg_smem(int G) {
 }
 
 template <typename V>
-cudaError_t launch_rg(int32_t m, int g_log2, const int64_t *group_ptr, const int32_t *row_len, const int32_t *rg_col,
-                      const void *rg_val, const void *x, void *y, double alpha, double beta, int32_t *error,
-                      cudaStream_t stream) {
+cudaError_t launch_rg(int32_t m, int g_log2, const int64_t *group_ptr, const int32_t *row_len, const int32_t *perm,
+                      const int32_t *rg_col, const void *rg_val, const void *x, void *y, double alpha, double beta,
+                      int32_t *error, cudaStream_t stream) {
     const int G = 1 << g_log2;
+    if (perm && G != 32) return cudaErrorInvalidValue;
     RgParams<V> p;
     p.m = m;
     p.g_log2 = g_log2;
     p.ngroups = ((long long)m + G - 1) >> g_log2;
     p.gp = group_ptr;
     p.row_len = row_len;
+    p.perm = perm;
     p.rg_col = rg_col;
     p.rg_val = static_cast<const V *>(rg_val);
     p.x = static_cast<const V *>(x);
@@ -393,12 +457,14 @@ cudaError_t launch_rg(int32_t m, int g_log2, const int64_t *group_ptr, const int
 }  // namespace
 
 cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const int64_t *group_ptr,
-                              const int32_t *row_len, const int32_t *rg_col, const void *rg_val, const void *x,
-                              void *y, double alpha, double beta, int32_t *error, cudaStream_t stream) {
+                              const int32_t *row_len, const int32_t *perm, const int32_t *rg_col,
+                              const void *rg_val, const void *x, void *y, double alpha, double beta,
+                              int32_t *error, cudaStream_t stream) {
     if (m <= 0) return cudaSuccess;
     if (dtype == SPMV_F64)
-        return launch_rg<double>(m, g_log2, group_ptr, row_len, rg_col, rg_val, x, y, alpha, beta, error, stream);
-    return launch_rg<float>(m, g_log2, group_ptr, row_len, rg_col, rg_val, x, y, alpha, beta, error, stream);
+        return launch_rg<double>(m, g_log2, group_ptr, row_len, perm, rg_col, rg_val, x, y, alpha, beta, error,
+                                 stream);
+    return launch_rg<float>(m, g_log2, group_ptr, row_len, perm, rg_col, rg_val, x, y, alpha, beta, error, stream);
 }
 
 }  // namespace lbcsr

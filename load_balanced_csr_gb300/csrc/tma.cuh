@@ -68,6 +68,14 @@ __device__ __forceinline__ double gather_keep(const double *p, uint64_t pol) {
     asm volatile("ld.global.nc.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v) : "l"(p), "l"(pol));
     return v;
 }
+// y is written once per product and not read again in it: store with the
+// stream's (evict-first) policy so that it does not push x out of L2.
+__device__ __forceinline__ void store_stream(float *p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void store_stream(double *p, double v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f64 [%0], %1, %2;" ::"l"(p), "d"(v), "l"(pol) : "memory");
+}
 
 }  // namespace tma
 }  // namespace lbcsr

@@ -169,7 +169,7 @@ def test_rgcsr_update_values_repacks(dtype):
     plan.close()
 
 
-@pytest.mark.parametrize("kernel", ["rgcsr", "long_rows"])
+@pytest.mark.parametrize("kernel", ["rgcsr", "long_rows", "rgcsr_sorted"])
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
 def test_row_kernels_degenerate_shapes(kernel, dtype):
     import torch
@@ -204,3 +204,81 @@ def test_options_are_validated():
                dict(kernel="rgcsr", long_row_min=-1)]:
         with pytest.raises(lb.SpmvError):
             make_plan(A, **kw)
+
+
+WINDOW = 1024
+
+
+def permuted_without(A, perm, drop):
+    """A's rows in the order perm, the rows in `drop` emptied."""
+    lens = np.diff(A.row_ptr).astype(np.int64)
+    dropped = np.zeros(A.m, dtype=bool)
+    dropped[np.asarray(drop, dtype=np.int64)] = True
+    cols, vals, new_lens = [], [], []
+    for r in perm:
+        if dropped[r]:
+            new_lens.append(0)
+            continue
+        b, e = A.row_ptr[r], A.row_ptr[r + 1]
+        cols.append(A.col_idx[b:e])
+        vals.append(A.vals[b:e])
+        new_lens.append(e - b)
+    rp = np.concatenate([[0], np.cumsum(new_lens)]).astype(np.int32)
+    col = np.concatenate(cols) if cols else np.zeros(0, np.int32)
+    val = np.concatenate(vals) if vals else np.zeros(0, A.vals.dtype)
+    return rp, col.astype(np.int32), val.astype(A.vals.dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("L", [0, 512])
+def test_rgcsr_sorted_layout_matches_oracle(dtype, L):
+    """Row order equal to the oracle's window sort; the interleaved copy of
+    the rows in that order (long rows emptied) equal to the oracle's copy."""
+    heavy = {5: 600, 2047: 3000, 3000: 700} if L else {}
+    A = skewed(3333, 5000, 21, dtype, heavy)
+    plan, _ = make_plan(A, kernel="rgcsr_sorted", long_row_min=L or 1 << 30)
+    info = plan.info()
+    assert info["kernel_name"] == "rgcsr_sorted" and info["rgcsr_group"] == 32
+    long_min = L if L else 0
+    perm, eff = oracle.window_sort(A.row_ptr, WINDOW, long_min)
+    np.testing.assert_array_equal(plan.export("rg_perm"), perm)
+    np.testing.assert_array_equal(plan.export("rg_row_len"), eff)
+    ids, _ = oracle.long_rows(A.row_ptr, L, SEG) if L else (np.zeros(0, np.int32), None)
+    rp2, col2, val2 = permuted_without(A, perm, ids)
+    gp, rl, rg_col, rg_val = oracle.rgcsr_pack(rp2, col2, val2, 32)
+    np.testing.assert_array_equal(plan.export("rg_group_ptr"), gp)
+    np.testing.assert_array_equal(plan.export("rg_col"), rg_col)
+    np.testing.assert_array_equal(plan.export("rg_val"), rg_val)
+    assert info["num_long_rows"] == len(ids)
+    plan.close()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (1.5, 0.5), (-2.0, 0.0), (0.0, 1.0)])
+def test_rgcsr_sorted_products(dtype, alpha, beta):
+    cases = [synth.random_csr(20011, 20011, max_len=9, empty_frac=0.25, dist=synth.DIST_NORMAL, seed=1, dtype=dtype),
+             synth.random_csr(1000, 3000, max_len=40, empty_frac=0.1, dist=synth.DIST_NORMAL, seed=2, dtype=dtype),
+             skewed(9000, 300000, 3, dtype, {4: 250000, 8999: 5000, 1024: 600}),
+             synth.random_csr(31, 100, max_len=5, empty_frac=0.3, dist=synth.DIST_NORMAL, seed=4, dtype=dtype)]
+    for k, A in enumerate(cases):
+        x, y0 = vectors(A, k)
+        plan, _ = make_plan(A, kernel="rgcsr_sorted")
+        y = run_plan(plan, A, x, y0, alpha, beta)
+        assert plan.device_status() == 0
+        plan.close()
+        assert_close_to_oracle(A, x, y, alpha, beta, y0, label=f"rgcsr_sorted {dtype} case {k}")
+
+
+def test_rgcsr_sorted_update_values_and_determinism():
+    import torch
+    A = skewed(12000, 200000, 9, "f64", {77: 150000})
+    x, y0 = vectors(A, 9)
+    plan, _ = make_plan(A, kernel="rgcsr_sorted")
+    new_vals = synth.vector(A.nnz, synth.DIST_UNIFORM_PM1, 5, synth.STREAM_Y, "f64")
+    plan.update_values(torch.from_numpy(new_vals).cuda())
+    A2 = synth.CSR(A.m, A.n, A.row_ptr, A.col_idx, new_vals)
+    outs = [run_plan(plan, A2, x, y0, 1.5, 0.5) for _ in range(3)]
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o.view(np.uint64), outs[0].view(np.uint64))
+    assert_close_to_oracle(A2, x, outs[0], 1.5, 0.5, y0, label="rgcsr_sorted after update_values")
+    plan.close()
