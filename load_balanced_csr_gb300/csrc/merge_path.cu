@@ -212,6 +212,13 @@ __device__ __forceinline__ V finish_row(V s, V alpha, V beta, int mode, const V 
     }
 }
 
+template <typename V>
+__device__ __forceinline__ V warp_sum(V v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
 __device__ __forceinline__ long long warp_of_tile(long long t, long long P, long long W) {
     return ((t + 1) * W - 1) / P;  // warp w owns tiles [w*P/W, (w+1)*P/W)
 }
@@ -285,6 +292,13 @@ merge_path_spmv_kernel(const MPParams<V> p) {
 
     const bool with_y = p.mode & 2;
     V carry = V(0);  // sum of the row open at the previous tile's end
+    // fp32: tiles that lie inside one row (no row end) leave their sums in
+    // the lanes, one per lane, and skip the scan; the lanes' shares join
+    // the carry once, when a row end or the end of the run comes.  (fp64
+    // keeps the scan: the extra registers cost more than the skipped adds,
+    // measured on the skewed matrix.)
+    V lane_part = V(0);
+    bool parts_pending = false;
     for (long long t = t_begin; t < t_end; ++t) {
         const int s = (int)((t - t_begin) & 1);
         unsigned char *stage = stages + s * stage_bytes<V, IPL>();
@@ -321,6 +335,21 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             vr[i] = i < run ? sv.val[k0 + i + sh] : V(0);
         }
 
+        if (sizeof(V) == 4 && nrows == 0) {  // the whole tile belongs to the open row
+            V acc = V(0);
+#pragma unroll
+            for (int i = 0; i <= IPL; ++i) {
+                if (sizeof(V) == 8 && i >= Q) break;
+                acc = fma(vr[i], xr[i], acc);
+            }
+            lane_part += acc;
+            parts_pending = true;
+        } else {
+        if (sizeof(V) == 4 && parts_pending) {
+            carry += warp_sum(lane_part);
+            lane_part = V(0);
+            parts_pending = false;
+        }
         // ---- mark each row's last nonzero in the tile (while the gathers fly)
         for (int w = lane; w < nwords + 2; w += 32) sv.bm[w] = 0u;
         __syncwarp();
@@ -401,6 +430,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             const long long first = warp_of_tile(((long long)p.row_ptr[i0] + i0) / T, P, W);
             cut_row<V>(p, lane, 0, head_val, true, me, i0, first, me);
         }
+        }  // nrows > 0
         __syncwarp();  // this stage may now be refilled
 
         // ---- tile t + 2 goes into this stage
@@ -411,6 +441,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         }
     }
 
+    if (sizeof(V) == 4 && parts_pending) carry += warp_sum(lane_part);
     // ---- the row open at the end of the warp's run, if it has nonzeros here
     const int4 last_tile = tile_bounds(p.part, t_end - 1);
     const int ie = last_tile.z, je = last_tile.w;
