@@ -105,6 +105,8 @@ def _bind(cdll):
         "oracle_rgcsr_pack_f32": [i32, vp, vp, vp, i32, vp, vp, vp],
         "oracle_long_rows": [i32, vp, i32, i32, vp, vp, ctypes.POINTER(i64)],
         "oracle_window_sort": [i32, vp, i32, i32, vp, vp],
+        "oracle_spmm_f64": [i32, i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, vp],
+        "oracle_spmm_f32": [i32, i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, vp],
     }
     for name, argtypes in sig.items():
         f = getattr(cdll, name)
@@ -231,3 +233,25 @@ def window_sort(row_ptr, window: int, long_min: int = 0):
     if lib().oracle_window_sort(m, _p(row_ptr), window, long_min, _p(perm), _p(eff)):
         raise ValueError("oracle_window_sort: bad arguments")
     return perm, eff
+
+
+def spmm(row_ptr, col_idx, vals, X, alpha=1.0, beta=0.0, Y_old=None, n=None):
+    """Y = alpha*A*X + beta*Y_old for a row-major X (n-by-k); returns (Y, mag),
+    Y m-by-k of the value type, mag float64."""
+    row_ptr = _i32(row_ptr)
+    col_idx = _i32(col_idx)
+    f64 = np.asarray(vals).dtype == np.float64
+    t = np.float64 if f64 else np.float32
+    vals = np.ascontiguousarray(vals, dtype=t)
+    X = np.ascontiguousarray(X, dtype=t)
+    m = len(row_ptr) - 1
+    k = X.shape[1]
+    n = X.shape[0] if n is None else n
+    yo = np.ascontiguousarray(Y_old, dtype=t) if beta != 0.0 else None
+    Y = np.empty((m, k), dtype=t)
+    mag = np.empty((m, k), dtype=np.float64)
+    fn = lib().oracle_spmm_f64 if f64 else lib().oracle_spmm_f32
+    if fn(m, n, k, _p(row_ptr), _p(col_idx), _p(vals), _p(X), k, float(alpha), float(beta), _p(yo), k,
+          _p(Y), _p(mag)):
+        raise ValueError("oracle_spmm: bad arguments")
+    return Y, mag

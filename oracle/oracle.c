@@ -270,3 +270,38 @@ int oracle_window_sort(int32_t m, const int32_t *row_ptr, int32_t window, int32_
     free(taken);
     return 0;
 }
+
+/* [LBPM] section 4.3, Listing 4: for every row, for every column t of X,
+ * sum vals[nz] * X[indices[nz]][t] over the row's nonzeros. */
+#define ORACLE_SPMM(NAME, T)                                                                               \
+    int NAME(int32_t m, int32_t n, int32_t k, const int32_t *row_ptr, const int32_t *col_idx,            \
+             const T *vals, const T *X, int64_t ldx, double alpha, double beta, const T *Y_old,          \
+             int64_t ldy, T *Y_out, double *mag_out) {                                                    \
+        if (!check_row_ptr_basic(m, row_ptr) || n < 0 || k < 0 || Y_out == NULL || ldx < k) return 1;    \
+        if (beta != 0.0 && (Y_old == NULL || ldy < k)) return 1;                                          \
+        const long double a = (long double)(T)alpha;                                                      \
+        const long double b = (long double)(T)beta;                                                       \
+        for (int32_t i = 0; i < m; ++i) {                                                                 \
+            for (int32_t t = 0; t < k; ++t) {                                                             \
+                long double acc = 0.0L, mag = 0.0L;                                                       \
+                for (int32_t q = row_ptr[i]; q < row_ptr[i + 1]; ++q) {                                   \
+                    long double prod = (long double)vals[q] * (long double)X[(int64_t)col_idx[q] * ldx + t]; \
+                    acc += prod;                                                                          \
+                    mag += prod < 0 ? -prod : prod;                                                       \
+                }                                                                                         \
+                long double y = a * acc, by = 0.0L;                                                       \
+                if (beta != 0.0) {                                                                        \
+                    by = b * (long double)Y_old[(int64_t)i * ldy + t];                                    \
+                    y += by;                                                                              \
+                }                                                                                         \
+                Y_out[(int64_t)i * k + t] = (T)y;                                                         \
+                if (mag_out) {                                                                            \
+                    long double aa = a < 0 ? -a : a;                                                      \
+                    mag_out[(int64_t)i * k + t] = (double)(aa * mag + (by < 0 ? -by : by));               \
+                }                                                                                         \
+            }                                                                                             \
+        }                                                                                                 \
+        return 0;                                                                                         \
+    }
+ORACLE_SPMM(oracle_spmm_f64, double)
+ORACLE_SPMM(oracle_spmm_f32, float)

@@ -123,6 +123,22 @@ int oracle_long_rows(int32_t m, const int32_t *row_ptr, int32_t min_len, int32_t
                      int64_t *seg_begin, int64_t *count);
 
 /*
+ * Y = alpha*A*X + beta*Y_old for k right-hand sides ([LBPM] section 4.3,
+ * Listing 4: the SpMV row loop with an inner loop over the columns of a
+ * dense matrix).  X is n-by-k and Y m-by-k, both row-major with leading
+ * dimensions ldx, ldy >= k: X[c][t] = X[c*ldx + t].  Sums in long double;
+ * mag_out[i*k + t] (may be NULL) = |alpha|*sum_j |a_ij X[j][t]| +
+ * |beta*Y_old[i][t]|.  If beta == 0, Y_old is not read.  Y_out is m-by-k
+ * with leading dimension k.  Returns 0, or 1 on bad arguments.
+ */
+int oracle_spmm_f64(int32_t m, int32_t n, int32_t k, const int32_t *row_ptr, const int32_t *col_idx,
+                    const double *vals, const double *X, int64_t ldx, double alpha, double beta,
+                    const double *Y_old, int64_t ldy, double *Y_out, double *mag_out);
+int oracle_spmm_f32(int32_t m, int32_t n, int32_t k, const int32_t *row_ptr, const int32_t *col_idx,
+                    const float *vals, const float *X, int64_t ldx, double alpha, double beta,
+                    const float *Y_old, int64_t ldy, float *Y_out, double *mag_out);
+
+/*
  * Row order of the window-sorted Row-grouped layout (an extension of
  * [RgCSR] section 3, whose weakness is the padding of a group to its
  * longest row, section 4): inside each window of `window` consecutive rows

@@ -35,6 +35,10 @@ MUTATIONS = [
      [pins.test_window_sort_worked_example]),
     ("window sort ties by last index", "if (best < 0 || len > best_len) {", "if (best < 0 || len >= best_len) {",
      [pins.test_window_sort_worked_example]),
+    ("spmm reads X column-major", "(long double)X[(int64_t)col_idx[q] * ldx + t]", "(long double)X[(int64_t)t * ldx + col_idx[q] % ldx]",
+     [pins.test_spmm_equals_dense_product_exactly]),
+    ("spmm drops the beta term", "                    y += by;                                                                              \\", "                    y += 0;                                                                               \\",
+     [pins.test_spmm_equals_dense_product_exactly]),
 ]
 
 
@@ -49,6 +53,8 @@ def _run_pin(fn):
         cases = [dict(nx=5, ny=9)]
     elif "G" in params:
         cases = [dict(G=4)]
+    elif "k" in params:
+        cases = [dict(k=3)]
     for kw in cases:
         try:
             fn(**kw)

@@ -417,3 +417,49 @@ def test_window_sort_invariants(window):
         assert eff[p] == want
         if p + 1 < A.m and (p + 1) // window == p // window:
             assert eff[p] > eff[p + 1] or (eff[p] == eff[p + 1] and perm[p] < perm[p + 1])
+
+
+# ---------------------------------------------------------------- SpMM
+
+
+@pytest.mark.parametrize("k", [1, 3, 8])
+def test_spmm_equals_dense_product_exactly(k):
+    """Small integers: every product and sum is exact, so Y must equal the
+    dense integer product alpha*A@X + beta*Y_old exactly."""
+    rng = np.random.default_rng(k)
+    m, n = 37, 23
+    A = synth.random_csr(m, n, max_len=9, empty_frac=0.2, dist=synth.DIST_SMALL_INT, seed=k, dtype="f64")
+    dense = np.zeros((m, n), dtype=np.int64)
+    for i in range(m):
+        for q in range(A.row_ptr[i], A.row_ptr[i + 1]):
+            dense[i, A.col_idx[q]] = int(A.vals[q])
+    X = rng.integers(-3, 4, size=(n, k)).astype(np.float64)
+    Y0 = rng.integers(-5, 6, size=(m, k)).astype(np.float64)
+    for alpha, beta in [(1, 0), (2, -3), (0, 1), (-1, 0.5)]:
+        Y, _ = oracle.spmm(A.row_ptr, A.col_idx, A.vals, X, alpha, beta, Y0)
+        want = alpha * (dense @ X.astype(np.int64)) + beta * Y0
+        np.testing.assert_array_equal(Y, want)
+
+
+def test_spmm_identity_right_hand_sides_give_columns():
+    """X = I (n columns): column t of Y is column t of A, exactly."""
+    A = synth.random_csr(40, 12, max_len=6, empty_frac=0.1, dist=synth.DIST_NORMAL, seed=5, dtype="f64")
+    Y, _ = oracle.spmm(A.row_ptr, A.col_idx, A.vals, np.eye(12))
+    want = np.zeros((40, 12))
+    for i in range(40):
+        for q in range(A.row_ptr[i], A.row_ptr[i + 1]):
+            want[i, A.col_idx[q]] = A.vals[q]
+    np.testing.assert_array_equal(Y, want)
+
+
+def test_spmm_columns_are_independent():
+    """Scaling one column of X scales the same column of Y only (powers of
+    two keep it exact)."""
+    A = synth.random_csr(50, 30, max_len=8, empty_frac=0.2, dist=synth.DIST_NORMAL, seed=6, dtype="f64")
+    X = synth.vector(30 * 4, synth.DIST_NORMAL, 6, synth.STREAM_X, "f64").reshape(30, 4)
+    Y, _ = oracle.spmm(A.row_ptr, A.col_idx, A.vals, X)
+    X2 = X.copy()
+    X2[:, 2] *= 4.0
+    Y2, _ = oracle.spmm(A.row_ptr, A.col_idx, A.vals, X2)
+    np.testing.assert_array_equal(Y2[:, [0, 1, 3]], Y[:, [0, 1, 3]])
+    np.testing.assert_array_equal(Y2[:, 2], 4.0 * Y[:, 2])
