@@ -393,6 +393,64 @@ def cpu_baseline_leg(workload_name: str, budget_s: float) -> dict:
             "cpu": cpu_model()}
 
 
+def run_spmm(args, workload_name: str) -> dict | None:
+    """Y = alpha*A*X + beta*Y with k = args.rhs right-hand sides (row-major,
+    seeded X) on the workload's matrix: GFLOP/s = 2*nnz*k/t and the
+    algorithmic bytes nnz*(4+s) + (m+1)*4 + n*k*s + m*k*s*(1 + [beta != 0])."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    W = synth.workload(workload_name)
+    A = W.A
+    k = args.rhs
+    vt = torch.float64 if A.dtype == "f64" else torch.float32
+    s = A.vals.dtype.itemsize
+    rp = torch.from_numpy(A.row_ptr).to(dev)
+    col = torch.from_numpy(A.col_idx).to(dev)
+    val = torch.from_numpy(A.vals).to(dev)
+    X = torch.from_numpy(synth.vector(A.n * k, synth.DIST_NORMAL, 0, synth.STREAM_X, A.dtype)).to(dev).view(A.n, k)
+    Y = torch.zeros((A.m, k), dtype=vt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = lb.Plan(rp, col, val, A.n, kernel=args.kernel, with_spmm=True)
+    for _ in range(args.warmup):
+        plan.execute_multi(X, Y, W.alpha, W.beta, stream)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.15 if sampler else 0)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for a, b in ev:
+        a.record(stream)
+        plan.execute_multi(X, Y, W.alpha, W.beta, stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop(t0, time.time()) if sampler else None
+    per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3
+    plan.close()
+    if rank != 0:
+        return None
+    med = float(np.median(per))
+    bytes_ = A.nnz * (4 + s) + (A.m + 1) * 4 + A.n * k * s + A.m * k * s * (2 if W.beta != 0 else 1)
+    peak, peak_kind = measured_peak()
+    achieved = bytes_ / (float(per.mean()) * 1e-6) / 1e9
+    return {
+        "metric": f"CSR SpMM GFLOP/s (2*nnz*k per product, k={k})", "value": round(2.0 * A.nnz * k / (med * 1e-6) / 1e9, 2),
+        "unit": "GFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "median_us": round(med, 2),
+        "higher_is_better": True, "dtype": A.dtype, "data": "synthetic",
+        "config": {"workload": workload_name, "k": k, "kernel": "spmm (merge-path runs, lanes over columns)",
+                   "launches_per_product": -(-k // 128)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes_per_product": int(bytes_), "traffic": None},
+        "clocks": clocks,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,6 +463,7 @@ def main():
     ap.add_argument("--ipt", type=int, default=0)
     ap.add_argument("--group", type=int, default=0, help="Row-grouped CSR group size (0 = plan's choice)")
     ap.add_argument("--long-min", type=int, default=0, help="long-row threshold (0 = plan's default)")
+    ap.add_argument("--rhs", type=int, default=0, help="k > 0: time SpMM with k right-hand sides instead")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -425,7 +484,7 @@ def main():
         dist.init_process_group("nccl")
     names = synth.WORKLOADS if args.all else [args.workload]
     for name in names:
-        out = run_gpu(args, name)
+        out = run_spmm(args, name) if args.rhs > 0 else run_gpu(args, name)
         if out is not None:
             # the oracle is timed on rank 0 at N = 1 only
             out["cpu_baseline"] = cpu_baseline_leg(name, args.cpu_budget) \

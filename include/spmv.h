@@ -85,6 +85,9 @@ typedef struct {
                                  at least this many nonzeros count as long and
                                  go to the long-row kernel; 0 = default (512).
                                  Allowed: 0 or >= 32 */
+    int32_t with_spmm;        /* nonzero: also prepare spmv_execute_multi (the
+                                 merge-path partition and its scratch, about
+                                 1 KB per warp slot for fp32, 2 KB for fp64) */
 } spmv_options_t;
 
 /*
@@ -181,6 +184,23 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
  */
 spmv_status_t spmv_execute(spmv_plan_t plan, double alpha, const void *x, double beta, void *y,
                            spmv_stream_t stream);
+
+/*
+ * Y = alpha * A * X + beta * Y for k right-hand sides ("A GPU
+ * load-balancing programming model", section 4.3, Listing 4: the row loop
+ * of SpMV with an inner loop over the columns of a dense matrix), on the
+ * plan's merge-path partition.  X is n-by-k and Y m-by-k, device, row-major
+ * with leading dimensions ldx >= k and ldy >= k (element (c, t) of X at
+ * X[c*ldx + t]); value type of the plan.  alpha and beta as for
+ * spmv_execute (beta == 0: Y is write-only).  X and Y must not overlap.
+ * The plan must have been created with options.with_spmm != 0.  Columns
+ * are processed 128 at a time (one launch each); asynchronous, allocates
+ * nothing.  A plan must not run two products at once.
+ * Errors: INVALID_ARG (null plan or pointers, k < 0, ld < k, plan without
+ * with_spmm), CUDA (launch failure).  k == 0 or m == 0 is a no-op.
+ */
+spmv_status_t spmv_execute_multi(spmv_plan_t plan, int32_t k, double alpha, const void *X, int64_t ldx,
+                                 double beta, void *Y, int64_t ldy, spmv_stream_t stream);
 
 /*
  * Point the plan at new values with the same sparsity pattern (vals[nnz],

@@ -34,7 +34,7 @@ class SpmvError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("items_per_thread", ctypes.c_int32),
-                ("rgcsr_group", ctypes.c_int32), ("long_row_min", ctypes.c_int32)]
+                ("rgcsr_group", ctypes.c_int32), ("long_row_min", ctypes.c_int32), ("with_spmm", ctypes.c_int32)]
 
 
 class RowStats(ctypes.Structure):
@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
             "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
             "spmv_plan_device_status": [vp, ctypes.POINTER(i32)],
             "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
+            "spmv_execute_multi": [vp, i32, dbl, vp, ctypes.c_int64, dbl, vp, ctypes.c_int64, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -131,7 +132,7 @@ class Plan:
     ``close()``."""
 
     def __init__(self, row_ptr, col_idx, vals, n: int, *, kernel: str = "auto", items_per_thread: int = 0,
-                 rgcsr_group: int = 0, long_row_min: int = 0, stream=None):
+                 rgcsr_group: int = 0, long_row_min: int = 0, with_spmm: bool = False, stream=None):
         import torch
         for name, t, dt in (("row_ptr", row_ptr, torch.int32), ("col_idx", col_idx, torch.int32)):
             if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
@@ -145,7 +146,7 @@ class Plan:
         self._keep = (row_ptr, col_idx, vals)
         self.m, self.n, self.nnz = m, int(n), nnz
         self.dtype = vals.dtype
-        opts = Options(KERNELS[kernel], items_per_thread, rgcsr_group, long_row_min)
+        opts = Options(KERNELS[kernel], items_per_thread, rgcsr_group, long_row_min, int(bool(with_spmm)))
         handle = ctypes.c_void_p()
         with torch.cuda.device(row_ptr.device):
             check(lib().spmv_plan_create_ex(ctypes.byref(handle), m, self.n, nnz, _ptr(row_ptr), _ptr(col_idx),
@@ -169,6 +170,27 @@ class Plan:
         check(lib().spmv_execute(self._h, float(alpha), _ptr(x), float(beta), _ptr(y), _stream_handle(stream)),
               "spmv_execute")
         return y
+
+    def execute_multi(self, X, Y, alpha: float = 1.0, beta: float = 0.0, stream=None):
+        """Y = alpha*A*X + beta*Y for a row-major X (n-by-k) and Y (m-by-k);
+        rows may be padded (a stride larger than k), columns must be
+        contiguous.  The plan needs with_spmm=True."""
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        if X.dtype != self.dtype or Y.dtype != self.dtype:
+            raise TypeError("X and Y must have the plan's value type")
+        if X.dim() != 2 or Y.dim() != 2 or X.shape[0] != self.n or Y.shape[0] != self.m or X.shape[1] != Y.shape[1]:
+            raise ValueError("X must be n-by-k and Y m-by-k")
+        if X.stride(1) != 1 or Y.stride(1) != 1:
+            raise ValueError("X and Y must be row-major (unit column stride)")
+        if not X.is_cuda or not Y.is_cuda:
+            raise TypeError("X and Y must be CUDA tensors")
+        k = X.shape[1]
+        ldx = X.stride(0) if X.shape[0] > 1 else k
+        ldy = Y.stride(0) if Y.shape[0] > 1 else k
+        check(lib().spmv_execute_multi(self._h, k, float(alpha), _ptr(X), ldx, float(beta), _ptr(Y), ldy,
+                                       _stream_handle(stream)), "spmv_execute_multi")
+        return Y
 
     def update_values(self, vals, stream=None):
         if vals.numel() != self.nnz or vals.dtype != self.dtype or not vals.is_contiguous():

@@ -57,6 +57,15 @@ struct spmv_plan_s {
     int32_t *perm = nullptr;         // [m] row at each position (window-sorted copy only)
     void *rg = nullptr;
     size_t rg_bytes = 0;
+
+    // SpMM (spmv_execute_multi): warps and their scratch
+    bool with_spmm = false;
+    bool has_partition = false;
+    int64_t spmm_warps = 0;
+    void *spmm = nullptr;
+    size_t spmm_bytes = 0;
+    void *spmm_tail = nullptr, *spmm_head = nullptr;
+    int32_t *spmm_arrivals = nullptr;
     int32_t *rg_col = nullptr;       // [rg_slots]
     void *rg_val = nullptr;          // [rg_slots]
 
@@ -146,6 +155,7 @@ void destroy_plan(spmv_plan_s *p) {
     if (!p) return;
     if (p->rg) cudaFree(p->rg);
     if (p->aux) cudaFree(p->aux);
+    if (p->spmm) cudaFree(p->spmm);
     if (p->arena) cudaFree(p->arena);
     delete p;
 }
@@ -430,12 +440,34 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     p->ipt = ipt_forced ? ipt_forced : merge_path_choose_items(dtype, n, p->stats);
     p->tile = (int64_t)merge_path_threads() * p->ipt;
     p->num_tiles = total > 0 ? (total + p->tile - 1) / p->tile : 1;
-    if (p->kernel == SPMV_KERNEL_MERGE_PATH && m > 0) {
+    p->with_spmm = opt.with_spmm != 0;
+    if ((p->kernel == SPMV_KERNEL_MERGE_PATH || p->with_spmm) && m > 0) {
         e = launch_merge_path_partition(m, nnz, row_ptr, p->tile, p->num_tiles, p->part, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) {
             destroy_plan(p);
             return cuda_fail(e, "merge-path partition");
+        }
+        p->has_partition = true;
+    }
+    if (p->with_spmm && m > 0) {
+        p->spmm_warps = spmm_warps(p->num_tiles);
+        const size_t part_bytes = align_up(vs * kSpmmBlocks * 32 * (size_t)p->spmm_warps, 256);
+        p->spmm_bytes = 2 * part_bytes + align_up(sizeof(int32_t) * (size_t)p->spmm_warps, 256);
+        e = cudaMalloc(&p->spmm, p->spmm_bytes);
+        if (e != cudaSuccess) {
+            p->spmm = nullptr;
+            destroy_plan(p);
+            return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpMM scratch: ") + cudaGetErrorString(e));
+        }
+        p->spmm_tail = p->spmm;
+        p->spmm_head = static_cast<char *>(p->spmm) + part_bytes;
+        p->spmm_arrivals = reinterpret_cast<int32_t *>(static_cast<char *>(p->spmm) + 2 * part_bytes);
+        e = cudaMemsetAsync(p->spmm_arrivals, 0, sizeof(int32_t) * (size_t)p->spmm_warps, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) {
+            destroy_plan(p);
+            return cuda_fail(e, "SpMM scratch");
         }
     }
     if (is_rgcsr(p->kernel) || p->kernel == SPMV_KERNEL_LONG_ROWS) {
@@ -501,6 +533,39 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     return SPMV_OK;
 }
 
+spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const void *X, int64_t ldx, double beta,
+                                 void *Y, int64_t ldy, spmv_stream_t stream_handle) {
+    if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
+    if (k < 0) return fail(SPMV_ERR_INVALID_ARG, "k < 0");
+    if (!p->with_spmm) return fail(SPMV_ERR_INVALID_ARG, "plan was created without with_spmm");
+    if (p->m == 0 || k == 0) return SPMV_OK;
+    if (!Y || (!X && p->nnz > 0)) return fail(SPMV_ERR_INVALID_ARG, "X or Y is NULL");
+    if (ldx < k || ldy < k) return fail(SPMV_ERR_INVALID_ARG, "leading dimension smaller than k");
+    SpmmArgs a;
+    a.m = p->m;
+    a.nnz = p->nnz;
+    a.k = k;
+    a.row_ptr = p->row_ptr;
+    a.col_idx = p->col_idx;
+    a.vals = p->vals;
+    a.X = X;
+    a.ldx = ldx;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.part = p->part;
+    a.num_tiles = p->num_tiles;
+    a.tile = p->tile;
+    a.num_warps = p->spmm_warps;
+    a.tail = p->spmm_tail;
+    a.head = p->spmm_head;
+    a.arrivals = p->spmm_arrivals;
+    const cudaError_t e = launch_spmm(p->dtype, a, reinterpret_cast<cudaStream_t>(stream_handle));
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
+    return SPMV_OK;
+}
+
 spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stream_t stream_handle) {
     if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
     if (!vals && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "vals is NULL");
@@ -536,7 +601,7 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->num_tiles = p->num_tiles;
     info->num_long_rows = p->num_long_rows;
     info->launches_per_execute = p->m > 0 ? 1 + (p->num_long_rows > 0 ? 1 : 0) : 0;
-    info->workspace_bytes = (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes);
+    info->workspace_bytes = (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes + p->spmm_bytes);
     info->stats = p->stats;
     info->long_row_min = p->num_long_rows > 0 ? p->long_min : 0;
     info->long_segment_nnz = kLongSegmentNnz;
@@ -559,7 +624,7 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
     size_t size = 0;
     switch (what) {
     case SPMV_EXPORT_PARTITION:
-        if (p->kernel != SPMV_KERNEL_MERGE_PATH) return fail(SPMV_ERR_INVALID_ARG, "plan has no merge-path partition");
+        if (!p->has_partition) return fail(SPMV_ERR_INVALID_ARG, "plan has no merge-path partition");
         src = p->part;
         size = sizeof(int2) * (size_t)(p->num_tiles + 1);
         break;

@@ -145,6 +145,32 @@ struct LongRowsArgs {
 };
 cudaError_t launch_long_rows_spmv(spmv_dtype_t dtype, const LongRowsArgs &a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- SpMM
+// Y = alpha*A*X + beta*Y, X n-by-k and Y m-by-k row-major (ldx, ldy >= k),
+// on the merge-path partition of the plan.  Columns go in slices of
+// kSpmmBlocks * 32 per launch.  Scratch: tail and head partials of
+// [num_warps][kSpmmBlocks * 32] values each, arrivals[num_warps] (zero
+// between products).
+constexpr int kSpmmBlocks = 4;
+constexpr int kSpmmWarpsPerSm = 16;
+int spmm_warps(int64_t num_tiles);
+struct SpmmArgs {
+    int32_t m, nnz, k;
+    const int32_t *row_ptr;
+    const int32_t *col_idx;
+    const void *vals;
+    const void *X;
+    int64_t ldx;
+    void *Y;
+    int64_t ldy;
+    double alpha, beta;
+    const int2 *part;
+    int64_t num_tiles, tile, num_warps;
+    void *tail, *head;
+    int32_t *arrivals;
+};
+cudaError_t launch_spmm(spmv_dtype_t dtype, const SpmmArgs &a, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace lbcsr

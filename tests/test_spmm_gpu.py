@@ -1,0 +1,113 @@
+"""SpMM Y = alpha*A*X + beta*Y (row-major X, k right-hand sides) on the
+merge-path partition, against the CPU oracle element by element: column
+counts around the 32-lane and 128-column slices, padded rows of X and Y,
+rows cut between many warps, empty rows, both value types, several
+alpha/beta; plus its argument checks and determinism."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TAU, to_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def dense_inputs(A, k, seed, ld_pad=0):
+    t = np.float64 if A.dtype == "f64" else np.float32
+    X = synth.vector(A.n * k, synth.DIST_NORMAL, seed, synth.STREAM_X, A.dtype).reshape(A.n, k)
+    Y0 = synth.vector(A.m * k, synth.DIST_NORMAL, seed, synth.STREAM_Y, A.dtype).reshape(A.m, k)
+    return X.astype(t), Y0.astype(t)
+
+
+def on_gpu(M, pad):
+    """M on the GPU as a row-major view with `pad` extra columns per row."""
+    import torch
+    buf = torch.zeros((M.shape[0], M.shape[1] + pad), dtype=torch.float64 if M.dtype == np.float64 else torch.float32,
+                      device="cuda")
+    buf[:, :M.shape[1]] = torch.from_numpy(M).cuda()
+    return buf[:, :M.shape[1]]
+
+
+def check(A, X, Y0, Yg, alpha, beta, label):
+    ref, mag = oracle.spmm(A.row_ptr, A.col_idx, A.vals, X, alpha, beta, Y0)
+    got = Yg.cpu().numpy()
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    bad = ~(err <= TAU[A.dtype] * mag + 1e-30)
+    if bad.any():
+        i, t = np.argwhere(bad)[0]
+        raise AssertionError(f"{label}: {bad.sum()} entries out of tolerance, e.g. ({i}, {t}): got {got[i, t]} "
+                             f"want {ref[i, t]}")
+
+
+def run_spmm(A, k, alpha, beta, kernel="merge_path", pad=0, seed=0):
+    import torch
+    import load_balanced_csr_gb300 as lb
+    X, Y0 = dense_inputs(A, k, seed)
+    rp, col, val = to_gpu(A)
+    with lb.Plan(rp, col, val, A.n, kernel=kernel, with_spmm=True) as plan:
+        Xg = on_gpu(X, pad)
+        Yg = on_gpu(Y0, pad) if beta != 0 else on_gpu(np.full_like(Y0, np.nan), pad)
+        plan.execute_multi(Xg, Yg, alpha, beta)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+    return X, Y0, Yg
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("k", [1, 3, 32, 33, 64, 100, 130])
+def test_spmm_random(dtype, k):
+    A = synth.random_csr(2500, 1800, max_len=14, empty_frac=0.2, dist=synth.DIST_NORMAL, seed=k, dtype=dtype)
+    for alpha, beta in [(1.0, 0.0), (1.5, -0.5)]:
+        X, Y0, Yg = run_spmm(A, k, alpha, beta, pad=3 if k % 2 else 0, seed=k)
+        check(A, X, Y0, Yg, alpha, beta, f"spmm {dtype} k={k} alpha={alpha}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_spmm_rows_cut_between_many_warps(dtype):
+    lens = np.full(3000, 2, dtype=np.int32)
+    lens[10] = 60000       # spans many warps' runs
+    lens[1500:1510] = 5000
+    lens[-1] = 20000       # open at the end of the last run
+    lens[200:260] = 0
+    A = synth.fill_random(lens, 70000, dist=synth.DIST_NORMAL, seed=4, dtype=dtype)
+    for k, kernel in [(8, "merge_path"), (40, "auto")]:
+        X, Y0, Yg = run_spmm(A, k, 0.5, 2.0, kernel=kernel, seed=4)
+        check(A, X, Y0, Yg, 0.5, 2.0, f"spmm cut rows {dtype} k={k}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_spmm_on_every_plan_kernel(dtype):
+    """The SpMM path uses the merge-path partition whatever kernel the plan
+    chose for SpMV."""
+    A = synth.stencil27(12, dist=synth.DIST_UNIFORM_PM1, diag=27.0, seed=2, dtype=dtype)
+    for kernel in ["auto", "rgcsr", "thread_row", "long_rows"]:
+        X, Y0, Yg = run_spmm(A, 16, 1.0, 0.0, kernel=kernel, seed=2)
+        check(A, X, Y0, Yg, 1.0, 0.0, f"spmm stencil plan={kernel}")
+
+
+def test_spmm_deterministic_and_checks():
+    import torch
+    import load_balanced_csr_gb300 as lb
+    lens = np.full(4000, 3, dtype=np.int32)
+    lens[7] = 50000
+    A = synth.fill_random(lens, 60000, dist=synth.DIST_NORMAL, seed=8, dtype="f32")
+    X, _ = dense_inputs(A, 20, 8)
+    rp, col, val = to_gpu(A)
+    with lb.Plan(rp, col, val, A.n, with_spmm=True) as plan:
+        Xg = torch.from_numpy(X).cuda()
+        outs = []
+        for _ in range(3):
+            Yg = torch.zeros((A.m, 20), dtype=torch.float32, device="cuda")
+            plan.execute_multi(Xg, Yg)
+            outs.append(Yg.cpu().numpy())
+        for o in outs[1:]:
+            np.testing.assert_array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+        with pytest.raises(ValueError):
+            plan.execute_multi(Xg, torch.zeros((A.m, 19), dtype=torch.float32, device="cuda"))
+        # k = 0 is a no-op
+        plan.execute_multi(torch.zeros((A.n, 0), dtype=torch.float32, device="cuda"),
+                           torch.zeros((A.m, 0), dtype=torch.float32, device="cuda"))
+    with lb.Plan(rp, col, val, A.n) as plan:  # no SpMM scratch
+        with pytest.raises(lb.SpmvError):
+            plan.execute_multi(Xg, torch.zeros((A.m, 20), dtype=torch.float32, device="cuda"))
