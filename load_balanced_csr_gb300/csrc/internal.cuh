@@ -152,7 +152,7 @@ cudaError_t launch_long_rows_spmv(spmv_dtype_t dtype, const LongRowsArgs &a, cud
 // [num_warps][kSpmmBlocks * 32] values each, arrivals[num_warps] (zero
 // between products).
 constexpr int kSpmmBlocks = 4;
-constexpr int kSpmmWarpsPerSm = 16;
+constexpr int kSpmmWarpsPerSm = 32;
 int spmm_warps(int64_t num_tiles);
 struct SpmmArgs {
     int32_t m, nnz, k;

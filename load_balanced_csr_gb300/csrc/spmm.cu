@@ -6,12 +6,12 @@
 //
 // Each warp takes the same share of the merge path as in the SpMV kernel
 // (the plan's partition: a contiguous run of row ends and nonzeros, cut
-// into equal tiles) and walks its run in merge order; its lanes span 32
-// columns of X and Y (up to kSpmmBlocks * 32 per launch), so every X row it
-// gathers and every Y row it writes is one coalesced access.  Columns and
-// values arrive 32 nonzeros at a time (lane q loads nonzero q, the walk
-// takes them from the lanes by shuffles), row ends 32 rows at a time, and
-// the X rows of the next few nonzeros are loaded before they are needed.
+// into equal tiles) and walks its run row by row.  Its lanes span the
+// columns of X and Y -- 32 at a time (up to kSpmmBlocks * 32 per launch),
+// or, when k is small, k rounded up to a power of two with several
+// nonzeros per warp step -- so every X row it gathers and every Y row it
+// writes is one coalesced access.  Row ends arrive 32 rows at a time, and
+// the loads of 8 warp steps are in flight together.
 //
 // A row cut between warps is finished as in the SpMV kernel: each warp
 // holding part of it stores its k partial sums, counts in on the row's
@@ -27,7 +27,6 @@ namespace {
 using namespace tma;
 
 constexpr int kSpmmThreads = 256;
-constexpr int kSpmmAhead = 4;  // nonzeros whose X rows are loaded ahead
 
 template <typename V>
 struct SpmmParams {
@@ -51,12 +50,14 @@ __device__ __forceinline__ long long spmm_warp_of_unit(long long d, long long T,
     return ((t + 1) * W - 1) / P;  // warp w owns tiles [w*P/W, (w+1)*P/W)
 }
 
-template <typename V, int KB>
+// Lanes of slot 0 write the row (column b * KP + lane for block b).
+template <typename V, int KB, int KP>
 __device__ __forceinline__ void spmm_store_row(const SpmmParams<V> &p, long long row, const V (&acc)[KB], int lane,
                                                uint64_t pol) {
+    if (lane >= KP) return;
 #pragma unroll
     for (int b = 0; b < KB; ++b) {
-        const int c = b * 32 + lane;
+        const int c = b * KP + lane;
         if (c < p.k) {
             V r = p.alpha * acc[b];
             if (p.beta != V(0)) r = fma(p.beta, p.Y[row * p.ldy + c], r);
@@ -68,13 +69,15 @@ __device__ __forceinline__ void spmm_store_row(const SpmmParams<V> &p, long long
 // A row cut between warps first..last: store this warp's partials, count
 // in; the last to arrive adds them in warp order (blocks of 16 warps, then
 // the blocks) and writes the row.
-template <typename V, int KB>
+template <typename V, int KB, int KP>
 __device__ void spmm_cut_row(const SpmmParams<V> &p, int lane, const V (&part)[KB], bool as_head, long long me,
                              long long row, long long first, long long last, uint64_t pol) {
-    constexpr int KW = KB * 32;
+    constexpr int KW = kSpmmBlocks * 32;  // scratch row of a warp
     V *mine = (as_head ? p.head : p.tail) + me * KW;
+    if (lane < KP) {
 #pragma unroll
-    for (int b = 0; b < KB; ++b) mine[b * 32 + lane] = part[b];
+        for (int b = 0; b < KB; ++b) mine[b * KP + lane] = part[b];
+    }
     __threadfence();
     __syncwarp();
     int finisher = 0;
@@ -86,7 +89,7 @@ __device__ void spmm_cut_row(const SpmmParams<V> &p, int lane, const V (&part)[K
     V sum[KB];
 #pragma unroll
     for (int b = 0; b < KB; ++b) {
-        const int c = b * 32 + lane;
+        const int c = b * KP + (lane % KP);
         V total = V(0);
         for (long long w0 = first; w0 < last; w0 += 16) {
             V blk = V(0);
@@ -95,33 +98,34 @@ __device__ void spmm_cut_row(const SpmmParams<V> &p, int lane, const V (&part)[K
         }
         sum[b] = total + __ldcg(p.head + last * KW + c);
     }
-    spmm_store_row<V, KB>(p, row, sum, lane, pol);
+    spmm_store_row<V, KB, KP>(p, row, sum, lane, pol);
     if (lane == 0) p.arrivals[last] = 0;  // ready for the next product
 }
 
-template <typename V, int KB>
+// The walk, row by row.  KP (a power of two, 1..32) is the number of
+// lanes per nonzero: with KB == 1 and k <= KP <= 32, a warp step takes
+// S = 32 / KP nonzeros at once -- lane l serves slot l / KP, column l % KP --
+// and each slot sums every S-th nonzero of the row; the slots are added by
+// xor-shuffles when the row ends.  With KB > 1 (k > 32) KP is 32 and S = 1.
+template <typename V, int KB, int KP>
 __global__ void __launch_bounds__(kSpmmThreads)
 spmm_kernel(const SpmmParams<V> p) {
+    constexpr int S = 32 / KP;  // nonzeros per warp step
+    constexpr int U = 8;        // warp steps whose loads are in flight together
     const int lane = threadIdx.x & 31;
+    const int slot = lane / KP;
+    const int tcol = lane % KP;
     const long long me = (long long)blockIdx.x * (kSpmmThreads / 32) + (threadIdx.x >> 5);
     if (me >= p.W) return;
     const uint64_t stream_pol = l2_policy_evict_first();
     // the warp's run: units [d_s, d_e) of the merge path
-    const int2 s = p.part[me * p.P / p.W];
-    const int2 e = p.part[(me + 1) * p.P / p.W];
-    const long long i_s = s.x, j_s = s.y, i_e = e.x, j_e = e.y;
+    const int2 s0 = p.part[me * p.P / p.W];
+    const int2 e0 = p.part[(me + 1) * p.P / p.W];
+    const long long i_s = s0.x, j_s = s0.y, i_e = e0.x, j_e = e0.y;
 
-    V acc[KB];
-#pragma unroll
-    for (int b = 0; b < KB; ++b) acc[b] = V(0);
     bool head = i_s < p.m && p.row_ptr[i_s] < j_s;  // the first row began in an earlier warp
-
-    long long r = i_s;       // current row
-    long long rb = -(1ll << 40);  // first row whose end the lanes hold (none yet)
-    int re_lane = 0;         // lane q: row_ptr[rb + 1 + q]
-    long long jb = j_s;      // first nonzero the lanes hold
-    int col_lane = 0;
-    V val_lane = V(0);
+    long long rb = -(1ll << 40);                      // first row whose end the lanes hold (none yet)
+    int re_lane = 0;                                  // lane q: row_ptr[rb + 1 + q]
     auto row_end = [&](long long row) -> long long {
         if (row < rb || row >= rb + 32) {  // refill: rows row .. row + 31
             rb = row;
@@ -130,63 +134,57 @@ spmm_kernel(const SpmmParams<V> p) {
         }
         return __shfl_sync(0xffffffffu, re_lane, (int)(row - rb));
     };
-    // finish every row that ends before nonzero j (or, at the run's end,
-    // every row of the run)
-    auto close_rows = [&](long long j) {
-        while (r < i_e) {
-            const long long re = row_end(r);
-            if (re > j) break;
-            if (head) {
-                head = false;
-                const long long first = spmm_warp_of_unit((long long)p.row_ptr[r] + r, p.T, p.P, p.W);
-                spmm_cut_row<V, KB>(p, lane, acc, true, me, r, first, me, stream_pol);
-            } else {
-                spmm_store_row<V, KB>(p, r, acc, lane, stream_pol);
-            }
-#pragma unroll
-            for (int b = 0; b < KB; ++b) acc[b] = V(0);
-            ++r;
-        }
-    };
 
-    for (long long j0 = j_s; j0 < j_e; j0 += 32) {
-        const int nb = (int)(j_e - j0 < 32 ? j_e - j0 : 32);
-        jb = j0;
-        col_lane = lane < nb ? ld_stream(p.col_idx + jb + lane) : 0;
-        val_lane = lane < nb ? ld_stream(p.vals + jb + lane) : V(0);
-        for (int q0 = 0; q0 < nb; q0 += kSpmmAhead) {
-            V xv[kSpmmAhead][KB];
-            V vv[kSpmmAhead];
+    V acc[KB];
+    long long j = j_s;
+    for (long long r = i_s;; ++r) {
+        const long long stop = r < i_e ? row_end(r) : j_e;  // this row's nonzeros in the run: [j, stop)
 #pragma unroll
-            for (int a = 0; a < kSpmmAhead; ++a) {
-                const int q = q0 + a;
-                const int c = __shfl_sync(0xffffffffu, col_lane, q & 31);
-                vv[a] = __shfl_sync(0xffffffffu, val_lane, q & 31);
+        for (int b = 0; b < KB; ++b) acc[b] = V(0);
+        for (; j < stop; j += (long long)U * S) {
+            int cc[U];
+            V vv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const long long q = j + (long long)u * S + slot;
+                cc[u] = q < stop ? ld_stream(p.col_idx + q) : -1;
+                vv[u] = q < stop ? ld_stream(p.vals + q) : V(0);
+            }
+            V xv[U][KB];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int b = 0; b < KB; ++b) {
-                    const int t = b * 32 + lane;
-                    xv[a][b] = q < nb && t < p.k ? ld_gather(p.X + (long long)c * p.ldx + t) : V(0);
+                    const int t = b * KP + tcol;
+                    xv[u][b] = cc[u] >= 0 && t < p.k ? ld_gather(p.X + (long long)cc[u] * p.ldx + t) : V(0);
                 }
-            }
 #pragma unroll
-            for (int a = 0; a < kSpmmAhead; ++a) {
-                const int q = q0 + a;
-                if (q < nb) {
-                    close_rows(jb + q);
+            for (int u = 0; u < U; ++u)
 #pragma unroll
-                    for (int b = 0; b < KB; ++b) acc[b] = fma(vv[a], xv[a][b], acc[b]);
-                }
-            }
+                for (int b = 0; b < KB; ++b) acc[b] = fma(vv[u], xv[u][b], acc[b]);
+        }
+        j = stop;
+        // the slots' sums of this row (a fixed tree)
+#pragma unroll
+        for (int off = KP; off < 32; off <<= 1)
+#pragma unroll
+            for (int b = 0; b < KB; ++b) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+        if (r >= i_e) break;
+        if (head) {
+            head = false;
+            const long long first = spmm_warp_of_unit((long long)p.row_ptr[r] + r, p.T, p.P, p.W);
+            spmm_cut_row<V, KB, KP>(p, lane, acc, true, me, r, first, me, stream_pol);
+        } else {
+            spmm_store_row<V, KB, KP>(p, r, acc, lane, stream_pol);
         }
     }
-    close_rows(j_e);  // rows that end after the run's last nonzero (empty rows too)
     // the row open at the run's end, if it has nonzeros in this run
     if (i_e < p.m) {
         const long long rp_e = p.row_ptr[i_e];
         if (j_e > (rp_e > j_s ? rp_e : j_s)) {
             const long long first = spmm_warp_of_unit(rp_e + i_e, p.T, p.P, p.W);
             const long long last = spmm_warp_of_unit((long long)p.row_ptr[i_e + 1] + i_e, p.T, p.P, p.W);
-            spmm_cut_row<V, KB>(p, lane, acc, false, me, i_e, first, last, stream_pol);
+            spmm_cut_row<V, KB, KP>(p, lane, acc, false, me, i_e, first, last, stream_pol);
         }
     }
 }
@@ -214,7 +212,12 @@ cudaError_t launch_kb(const SpmmArgs &a, int32_t k, const void *X, void *Y, cuda
     p.head = static_cast<V *>(a.head);
     p.arrivals = a.arrivals;
     const unsigned grid = (unsigned)((p.W + kSpmmThreads / 32 - 1) / (kSpmmThreads / 32));
-    spmm_kernel<V, KB><<<grid, kSpmmThreads, 0, stream>>>(p);
+    if (KB > 1 || k > 16) spmm_kernel<V, KB, 32><<<grid, kSpmmThreads, 0, stream>>>(p);
+    else if (k > 8) spmm_kernel<V, 1, 16><<<grid, kSpmmThreads, 0, stream>>>(p);
+    else if (k > 4) spmm_kernel<V, 1, 8><<<grid, kSpmmThreads, 0, stream>>>(p);
+    else if (k > 2) spmm_kernel<V, 1, 4><<<grid, kSpmmThreads, 0, stream>>>(p);
+    else if (k > 1) spmm_kernel<V, 1, 2><<<grid, kSpmmThreads, 0, stream>>>(p);
+    else spmm_kernel<V, 1, 1><<<grid, kSpmmThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

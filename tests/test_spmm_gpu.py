@@ -55,7 +55,7 @@ def run_spmm(A, k, alpha, beta, kernel="merge_path", pad=0, seed=0):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
-@pytest.mark.parametrize("k", [1, 3, 32, 33, 64, 100, 130])
+@pytest.mark.parametrize("k", [1, 2, 3, 8, 16, 17, 32, 33, 64, 100, 130])
 def test_spmm_random(dtype, k):
     A = synth.random_csr(2500, 1800, max_len=14, empty_frac=0.2, dist=synth.DIST_NORMAL, seed=k, dtype=dtype)
     for alpha, beta in [(1.0, 0.0), (1.5, -0.5)]:
