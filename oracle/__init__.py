@@ -107,6 +107,10 @@ def _bind(cdll):
         "oracle_window_sort": [i32, vp, i32, i32, vp, vp],
         "oracle_spmm_f64": [i32, i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, vp],
         "oracle_spmm_f32": [i32, i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, vp],
+        "oracle_transpose_f64": [i32, i32, vp, vp, vp, vp, vp, vp, vp],
+        "oracle_transpose_f32": [i32, i32, vp, vp, vp, vp, vp, vp, vp],
+        "oracle_spmv_transposed_f64": [i32, i32, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
+        "oracle_spmv_transposed_f32": [i32, i32, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
     }
     for name, argtypes in sig.items():
         f = getattr(cdll, name)
@@ -255,3 +259,41 @@ def spmm(row_ptr, col_idx, vals, X, alpha=1.0, beta=0.0, Y_old=None, n=None):
           _p(Y), _p(mag)):
         raise ValueError("oracle_spmm: bad arguments")
     return Y, mag
+
+
+def transpose(row_ptr, col_idx, vals, n: int):
+    """(t_ptr, t_idx, t_vals, t_src): A^T in CSR form, rows of each column in
+    increasing order, t_src the entry's position in A."""
+    row_ptr = _i32(row_ptr)
+    col_idx = _i32(col_idx)
+    f64 = np.asarray(vals).dtype == np.float64
+    t = np.float64 if f64 else np.float32
+    vals = np.ascontiguousarray(vals, dtype=t)
+    m = len(row_ptr) - 1
+    nnz = int(row_ptr[-1])
+    tp = np.empty(n + 1, dtype=np.int32)
+    ti = np.empty(nnz, dtype=np.int32)
+    tv = np.empty(nnz, dtype=t)
+    ts = np.empty(nnz, dtype=np.int32)
+    fn = lib().oracle_transpose_f64 if f64 else lib().oracle_transpose_f32
+    if fn(m, n, _p(row_ptr), _p(col_idx), _p(vals), _p(tp), _p(ti), _p(tv), _p(ts)):
+        raise ValueError("oracle_transpose: bad arguments")
+    return tp, ti, tv, ts
+
+
+def spmv_transposed(row_ptr, col_idx, vals, x, n: int, alpha=1.0, beta=0.0, y_old=None):
+    """y = alpha*A^T*x + beta*y_old (x: m entries, y: n); returns (y, mag)."""
+    row_ptr = _i32(row_ptr)
+    col_idx = _i32(col_idx)
+    f64 = np.asarray(vals).dtype == np.float64
+    t = np.float64 if f64 else np.float32
+    vals = np.ascontiguousarray(vals, dtype=t)
+    x = np.ascontiguousarray(x, dtype=t)
+    m = len(row_ptr) - 1
+    yo = np.ascontiguousarray(y_old, dtype=t) if beta != 0.0 else None
+    y = np.empty(n, dtype=t)
+    mag = np.empty(n, dtype=np.float64)
+    fn = lib().oracle_spmv_transposed_f64 if f64 else lib().oracle_spmv_transposed_f32
+    if fn(m, n, _p(row_ptr), _p(col_idx), _p(vals), _p(x), float(alpha), float(beta), _p(yo), _p(y), _p(mag)):
+        raise ValueError("oracle_spmv_transposed: bad arguments")
+    return y, mag

@@ -305,3 +305,73 @@ int oracle_window_sort(int32_t m, const int32_t *row_ptr, int32_t window, int32_
     }
 ORACLE_SPMM(oracle_spmm_f64, double)
 ORACLE_SPMM(oracle_spmm_f32, float)
+
+/* Counting: column sizes, their prefix sums, then every entry of A in row
+ * order appended to its column -- which lists each column's rows in
+ * increasing order. */
+#define ORACLE_TRANSPOSE(NAME, T)                                                                         \
+    int NAME(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx, const T *vals,        \
+             int32_t *t_ptr, int32_t *t_idx, T *t_vals, int32_t *t_src) {                                 \
+        if (!check_row_ptr_basic(m, row_ptr) || n < 0 || !t_ptr || !t_idx || !t_vals) return 1;         \
+        int32_t nnz = row_ptr[m];                                                                         \
+        for (int32_t j = 0; j <= n; ++j) t_ptr[j] = 0;                                                    \
+        for (int32_t q = 0; q < nnz; ++q) {                                                               \
+            if (col_idx[q] < 0 || col_idx[q] >= n) return 1;                                              \
+            t_ptr[col_idx[q] + 1] += 1;                                                                   \
+        }                                                                                                 \
+        for (int32_t j = 0; j < n; ++j) t_ptr[j + 1] += t_ptr[j];                                         \
+        int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));                     \
+        if (!next) return 1;                                                                              \
+        for (int32_t j = 0; j < n; ++j) next[j] = t_ptr[j];                                               \
+        for (int32_t i = 0; i < m; ++i)                                                                   \
+            for (int32_t q = row_ptr[i]; q < row_ptr[i + 1]; ++q) {                                       \
+                int32_t pos = next[col_idx[q]]++;                                                         \
+                t_idx[pos] = i;                                                                           \
+                t_vals[pos] = vals[q];                                                                    \
+                if (t_src) t_src[pos] = q;                                                                \
+            }                                                                                             \
+        free(next);                                                                                       \
+        return 0;                                                                                         \
+    }
+ORACLE_TRANSPOSE(oracle_transpose_f64, double)
+ORACLE_TRANSPOSE(oracle_transpose_f32, float)
+
+/* y_j = alpha * sum_i a_ij x_i + beta * y_old_j, rows of A in order. */
+#define ORACLE_SPMV_T(NAME, T)                                                                            \
+    int NAME(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx, const T *vals,        \
+             const T *x, double alpha, double beta, const T *y_old, T *y_out, double *mag_out) {          \
+        if (!check_row_ptr_basic(m, row_ptr) || n < 0 || y_out == NULL) return 1;                        \
+        if (beta != 0.0 && y_old == NULL) return 1;                                                       \
+        const long double a = (long double)(T)alpha;                                                      \
+        const long double b = (long double)(T)beta;                                                       \
+        long double *acc = (long double *)calloc((size_t)(n > 0 ? n : 1), sizeof(long double));           \
+        long double *mag = (long double *)calloc((size_t)(n > 0 ? n : 1), sizeof(long double));           \
+        if (!acc || !mag) {                                                                               \
+            free(acc);                                                                                    \
+            free(mag);                                                                                    \
+            return 1;                                                                                     \
+        }                                                                                                 \
+        for (int32_t i = 0; i < m; ++i)                                                                   \
+            for (int32_t q = row_ptr[i]; q < row_ptr[i + 1]; ++q) {                                       \
+                long double prod = (long double)vals[q] * (long double)x[i];                              \
+                acc[col_idx[q]] += prod;                                                                  \
+                mag[col_idx[q]] += prod < 0 ? -prod : prod;                                               \
+            }                                                                                             \
+        for (int32_t j = 0; j < n; ++j) {                                                                 \
+            long double y = a * acc[j], by = 0.0L;                                                        \
+            if (beta != 0.0) {                                                                            \
+                by = b * (long double)y_old[j];                                                           \
+                y += by;                                                                                  \
+            }                                                                                             \
+            y_out[j] = (T)y;                                                                              \
+            if (mag_out) {                                                                                \
+                long double aa = a < 0 ? -a : a;                                                          \
+                mag_out[j] = (double)(aa * mag[j] + (by < 0 ? -by : by));                                 \
+            }                                                                                             \
+        }                                                                                                 \
+        free(acc);                                                                                        \
+        free(mag);                                                                                        \
+        return 0;                                                                                         \
+    }
+ORACLE_SPMV_T(oracle_spmv_transposed_f64, double)
+ORACLE_SPMV_T(oracle_spmv_transposed_f32, float)

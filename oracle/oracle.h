@@ -139,6 +139,32 @@ int oracle_spmm_f32(int32_t m, int32_t n, int32_t k, const int32_t *row_ptr, con
                     const float *Y_old, int64_t ldy, float *Y_out, double *mag_out);
 
 /*
+ * The transpose of A in CSR form (= A in compressed-column form, the
+ * "CSC" the load-balancing paper lists among the formats its CSR
+ * abstraction carries, section 4.1): t_ptr[n+1], t_idx[nnz] (row indices)
+ * and t_vals[nnz], each column's entries in increasing row order, and
+ * t_src[nnz] (may be NULL) the position in A of each entry.  Returns 0, or
+ * 1 on bad arguments.
+ */
+int oracle_transpose_f64(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx, const double *vals,
+                         int32_t *t_ptr, int32_t *t_idx, double *t_vals, int32_t *t_src);
+int oracle_transpose_f32(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx, const float *vals,
+                         int32_t *t_ptr, int32_t *t_idx, float *t_vals, int32_t *t_src);
+
+/*
+ * y = alpha * A^T * x + beta * y_old (x has m entries, y n): y_j = alpha *
+ * sum_i a_ij x_i + beta * y_old_j, summed over A's rows in increasing i,
+ * in long double.  mag_out as for oracle_spmv.  Returns 0, or 1 on bad
+ * arguments.
+ */
+int oracle_spmv_transposed_f64(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx,
+                               const double *vals, const double *x, double alpha, double beta, const double *y_old,
+                               double *y_out, double *mag_out);
+int oracle_spmv_transposed_f32(int32_t m, int32_t n, const int32_t *row_ptr, const int32_t *col_idx,
+                               const float *vals, const float *x, double alpha, double beta, const float *y_old,
+                               float *y_out, double *mag_out);
+
+/*
  * Row order of the window-sorted Row-grouped layout (an extension of
  * [RgCSR] section 3, whose weakness is the padding of a group to its
  * longest row, section 4): inside each window of `window` consecutive rows

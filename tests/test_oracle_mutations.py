@@ -39,6 +39,10 @@ MUTATIONS = [
      [pins.test_spmm_equals_dense_product_exactly]),
     ("spmm drops the beta term", "                    y += by;                                                                              \\", "                    y += 0;                                                                               \\",
      [pins.test_spmm_equals_dense_product_exactly]),
+    ("transpose keeps the row index of the column", "                t_idx[pos] = i;  ", "                t_idx[pos] = col_idx[q];  ",
+     [pins.test_transpose_worked_example]),
+    ("transposed product uses y index for x", "long double prod = (long double)vals[q] * (long double)x[i];", "long double prod = (long double)vals[q] * (long double)x[col_idx[q] % m];",
+     [pins.test_spmv_transposed_equals_dense_product_exactly]),
 ]
 
 

@@ -463,3 +463,43 @@ def test_spmm_columns_are_independent():
     Y2, _ = oracle.spmm(A.row_ptr, A.col_idx, A.vals, X2)
     np.testing.assert_array_equal(Y2[:, [0, 1, 3]], Y[:, [0, 1, 3]])
     np.testing.assert_array_equal(Y2[:, 2], 4.0 * Y[:, 2])
+
+
+# ---------------------------------------------------------------- transpose
+
+
+def test_transpose_worked_example():
+    """A = [[1, 0, 2], [0, 3, 0], [4, 5, 6], [0, 0, 7]] (4 x 3), transposed by
+    hand: columns [1, 4], [3, 5], [2, 6, 7] at rows [0, 2], [1, 2], [0, 2, 3]."""
+    rp = np.array([0, 2, 3, 6, 7], dtype=np.int32)
+    ci = np.array([0, 2, 1, 0, 1, 2, 2], dtype=np.int32)
+    v = np.array([1, 2, 3, 4, 5, 6, 7], dtype=np.float64)
+    tp, ti, tv, ts = oracle.transpose(rp, ci, v, 3)
+    assert tp.tolist() == [0, 2, 4, 7]
+    assert ti.tolist() == [0, 2, 1, 2, 0, 2, 3]
+    assert tv.tolist() == [1, 4, 3, 5, 2, 6, 7]
+    assert ts.tolist() == [0, 3, 2, 4, 1, 5, 6]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_transpose_twice_is_identity(seed):
+    A = synth.random_csr(300, 200, max_len=12, empty_frac=0.2, dist=synth.DIST_NORMAL, seed=seed, dtype="f64")
+    tp, ti, tv, _ = oracle.transpose(A.row_ptr, A.col_idx, A.vals, A.n)
+    rp2, ci2, v2, _ = oracle.transpose(tp, ti, tv, A.m)
+    np.testing.assert_array_equal(rp2, A.row_ptr)
+    np.testing.assert_array_equal(ci2, A.col_idx)  # random_csr sorts each row's columns
+    np.testing.assert_array_equal(v2, A.vals)
+
+
+def test_spmv_transposed_equals_dense_product_exactly():
+    A = synth.random_csr(41, 29, max_len=9, empty_frac=0.2, dist=synth.DIST_SMALL_INT, seed=3, dtype="f64")
+    dense = np.zeros((41, 29), dtype=np.int64)
+    for i in range(41):
+        for q in range(A.row_ptr[i], A.row_ptr[i + 1]):
+            dense[i, A.col_idx[q]] = int(A.vals[q])
+    rng = np.random.default_rng(3)
+    x = rng.integers(-4, 5, size=41).astype(np.float64)
+    y0 = rng.integers(-4, 5, size=29).astype(np.float64)
+    for alpha, beta in [(1, 0), (-2, 3), (0, 1)]:
+        y, _ = oracle.spmv_transposed(A.row_ptr, A.col_idx, A.vals, x, 29, alpha, beta, y0)
+        np.testing.assert_array_equal(y, alpha * (dense.T @ x.astype(np.int64)) + beta * y0)
