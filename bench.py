@@ -198,13 +198,17 @@ def run_gpu(args, workload_name: str) -> dict | None:
     torch.cuda.synchronize(dev)
     t = time.perf_counter()
     plan = lb.Plan(rp, col, val, A.n, kernel=args.kernel, items_per_thread=args.ipt, rgcsr_group=args.group,
-                   long_row_min=args.long_min)
+                   long_row_min=args.long_min, with_transpose=args.transposed)
     torch.cuda.synchronize(dev)
     plan_ms = (time.perf_counter() - t) * 1e3
     info = plan.info()
+    run = plan.execute_transposed if args.transposed else plan  # the workloads are square: x, y fit both ways
+    if args.transposed:
+        info["kernel_name"] = lb.KERNEL_NAMES.get(info["transposed_kernel"], "?") + " (A^T)"
+        info["launches_per_execute"] = info["transposed_launches"]
 
     for _ in range(args.warmup):
-        plan(x, y, W.alpha, W.beta, stream)
+        run(x, y, W.alpha, W.beta, stream)
     torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -220,7 +224,7 @@ def run_gpu(args, workload_name: str) -> dict | None:
     start_all.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
-        plan(x, y, W.alpha, W.beta, stream)
+        run(x, y, W.alpha, W.beta, stream)
         ev[k][1].record(stream)
     end_all.record(stream)
     torch.cuda.synchronize(dev)
@@ -245,7 +249,7 @@ def run_gpu(args, workload_name: str) -> dict | None:
         ke = max(3, min(K, args.e2e_steps))
         for _ in range(2):
             x.copy_(x_h, non_blocking=True)
-            plan(x, y, W.alpha, W.beta, stream)
+            run(x, y, W.alpha, W.beta, stream)
             y_h.copy_(y, non_blocking=True)
         torch.cuda.synchronize(dev)
         s_e, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -254,7 +258,7 @@ def run_gpu(args, workload_name: str) -> dict | None:
             x.copy_(x_h, non_blocking=True)
             if y0_h is not None:
                 y.copy_(y0_h, non_blocking=True)
-            plan(x, y, W.alpha, W.beta, stream)
+            run(x, y, W.alpha, W.beta, stream)
             y_h.copy_(y, non_blocking=True)
         e_e.record(stream)
         torch.cuda.synchronize(dev)
@@ -464,6 +468,7 @@ def main():
     ap.add_argument("--group", type=int, default=0, help="Row-grouped CSR group size (0 = plan's choice)")
     ap.add_argument("--long-min", type=int, default=0, help="long-row threshold (0 = plan's default)")
     ap.add_argument("--rhs", type=int, default=0, help="k > 0: time SpMM with k right-hand sides instead")
+    ap.add_argument("--transposed", action="store_true", help="time the transposed product A^T x instead")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

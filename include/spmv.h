@@ -88,6 +88,9 @@ typedef struct {
     int32_t with_spmm;        /* nonzero: also prepare spmv_execute_multi (the
                                  merge-path partition and its scratch, about
                                  1 KB per warp slot for fp32, 2 KB for fp64) */
+    int32_t with_transpose;   /* nonzero: also prepare spmv_execute_transposed
+                                 (the plan builds A^T in CSR form, 12-16 bytes
+                                 per nonzero, and a plan for it) */
 } spmv_options_t;
 
 /*
@@ -128,6 +131,8 @@ typedef struct {
     int32_t long_segment_nnz;     /* nonzeros per long-row segment (one warp each) */
     int64_t num_long_segments;    /* segments over all long rows */
     int64_t rgcsr_slots;          /* slots of the Row-grouped copy (group_ptr[last]) */
+    int32_t transposed_kernel;    /* spmv_kernel_t of the plan for A^T (-1: none) */
+    int32_t transposed_launches;  /* kernel launches one spmv_execute_transposed issues */
 } spmv_plan_info_t;
 
 /* What spmv_plan_export copies out. */
@@ -140,7 +145,11 @@ typedef enum {
     SPMV_EXPORT_RG_VAL = 4,      /* value type [group_ptr[last]] */
     SPMV_EXPORT_LONG_ROWS = 5,   /* int32[num_long_rows], ascending */
     SPMV_EXPORT_LONG_SEG_BEGIN = 6,/* int64[num_long_rows + 1]: first segment of each long row */
-    SPMV_EXPORT_RG_PERM = 7      /* int32[m]: the row at each position of the window-sorted copy */
+    SPMV_EXPORT_RG_PERM = 7,     /* int32[m]: the row at each position of the window-sorted copy */
+    SPMV_EXPORT_T_PTR = 8,       /* int32[n + 1]: A^T in CSR form, row pointers */
+    SPMV_EXPORT_T_IDX = 9,       /* int32[nnz]: its column indices (rows of A) */
+    SPMV_EXPORT_T_VALS = 10,     /* value type [nnz] */
+    SPMV_EXPORT_T_SRC = 11       /* int32[nnz]: each entry's position in A */
 } spmv_export_t;
 
 /*
@@ -203,10 +212,23 @@ spmv_status_t spmv_execute_multi(spmv_plan_t plan, int32_t k, double alpha, cons
                                  double beta, void *Y, int64_t ldy, spmv_stream_t stream);
 
 /*
+ * y = alpha * A^T * x + beta * y: x has m entries, y has n (device, plan's
+ * value type).  The plan must have been created with
+ * options.with_transpose != 0: it then holds A^T in compressed-row form
+ * (A in compressed-column form, the CSC of "A GPU load-balancing
+ * programming model", section 4.1), each column's entries in increasing
+ * row order, built by a stable radix sort on the GPU, and a plan of its own
+ * for it (statistics, kernel choice, schedule), whose product this runs.
+ * Semantics, synchronisation and errors as for spmv_execute.
+ */
+spmv_status_t spmv_execute_transposed(spmv_plan_t plan, double alpha, const void *x, double beta, void *y,
+                                      spmv_stream_t stream);
+
+/*
  * Point the plan at new values with the same sparsity pattern (vals[nnz],
  * device).  Plans that keep a reordered copy of the values (the
- * Row-grouped CSR kernel) repack it on `stream`; the others only record the
- * pointer.  Same ownership rule as at creation.
+ * Row-grouped CSR kernel, A^T) repack it on `stream`; the others only
+ * record the pointer.  Same ownership rule as at creation.
  */
 spmv_status_t spmv_plan_update_values(spmv_plan_t plan, const void *vals, spmv_stream_t stream);
 

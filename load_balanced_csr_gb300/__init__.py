@@ -21,7 +21,7 @@ __all__ = ["Plan", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
 KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4, "rgcsr_sorted": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 EXPORTS = {"partition": 0, "rg_group_ptr": 1, "rg_row_len": 2, "rg_col": 3, "rg_val": 4, "long_rows": 5,
-           "long_seg_begin": 6, "rg_perm": 7}
+           "long_seg_begin": 6, "rg_perm": 7, "t_ptr": 8, "t_idx": 9, "t_vals": 10, "t_src": 11}
 STATUS = {0: "ok", 1: "invalid argument", 2: "invalid CSR matrix", 3: "allocation failed", 4: "CUDA error",
           5: "unsupported"}
 
@@ -34,7 +34,8 @@ class SpmvError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("items_per_thread", ctypes.c_int32),
-                ("rgcsr_group", ctypes.c_int32), ("long_row_min", ctypes.c_int32), ("with_spmm", ctypes.c_int32)]
+                ("rgcsr_group", ctypes.c_int32), ("long_row_min", ctypes.c_int32), ("with_spmm", ctypes.c_int32),
+                ("with_transpose", ctypes.c_int32)]
 
 
 class RowStats(ctypes.Structure):
@@ -51,7 +52,8 @@ class PlanInfo(ctypes.Structure):
                 ("num_long_rows", ctypes.c_int32), ("launches_per_execute", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("stats", RowStats),
                 ("long_row_min", ctypes.c_int32), ("long_segment_nnz", ctypes.c_int32),
-                ("num_long_segments", ctypes.c_int64), ("rgcsr_slots", ctypes.c_int64)]
+                ("num_long_segments", ctypes.c_int64), ("rgcsr_slots", ctypes.c_int64),
+                ("transposed_kernel", ctypes.c_int32), ("transposed_launches", ctypes.c_int32)]
 
 
 _lib = None
@@ -86,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "spmv_plan_device_status": [vp, ctypes.POINTER(i32)],
             "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
             "spmv_execute_multi": [vp, i32, dbl, vp, ctypes.c_int64, dbl, vp, ctypes.c_int64, vp],
+            "spmv_execute_transposed": [vp, dbl, vp, dbl, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -132,7 +135,8 @@ class Plan:
     ``close()``."""
 
     def __init__(self, row_ptr, col_idx, vals, n: int, *, kernel: str = "auto", items_per_thread: int = 0,
-                 rgcsr_group: int = 0, long_row_min: int = 0, with_spmm: bool = False, stream=None):
+                 rgcsr_group: int = 0, long_row_min: int = 0, with_spmm: bool = False, with_transpose: bool = False,
+                 stream=None):
         import torch
         for name, t, dt in (("row_ptr", row_ptr, torch.int32), ("col_idx", col_idx, torch.int32)):
             if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
@@ -146,7 +150,8 @@ class Plan:
         self._keep = (row_ptr, col_idx, vals)
         self.m, self.n, self.nnz = m, int(n), nnz
         self.dtype = vals.dtype
-        opts = Options(KERNELS[kernel], items_per_thread, rgcsr_group, long_row_min, int(bool(with_spmm)))
+        opts = Options(KERNELS[kernel], items_per_thread, rgcsr_group, long_row_min, int(bool(with_spmm)),
+                       int(bool(with_transpose)))
         handle = ctypes.c_void_p()
         with torch.cuda.device(row_ptr.device):
             check(lib().spmv_plan_create_ex(ctypes.byref(handle), m, self.n, nnz, _ptr(row_ptr), _ptr(col_idx),
@@ -192,6 +197,20 @@ class Plan:
                                        _stream_handle(stream)), "spmv_execute_multi")
         return Y
 
+    def execute_transposed(self, x, y, alpha: float = 1.0, beta: float = 0.0, stream=None):
+        """y = alpha*A^T*x + beta*y (x: m entries, y: n); needs with_transpose=True."""
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        if x.dtype != self.dtype or y.dtype != self.dtype:
+            raise TypeError("x and y must have the plan's value type")
+        if x.numel() != self.m or y.numel() != self.n or not x.is_contiguous() or not y.is_contiguous():
+            raise ValueError("x must have m and y n contiguous entries")
+        if not x.is_cuda or not y.is_cuda:
+            raise TypeError("x and y must be CUDA tensors")
+        check(lib().spmv_execute_transposed(self._h, float(alpha), _ptr(x), float(beta), _ptr(y),
+                                            _stream_handle(stream)), "spmv_execute_transposed")
+        return y
+
     def update_values(self, vals, stream=None):
         if vals.numel() != self.nnz or vals.dtype != self.dtype or not vals.is_contiguous():
             raise ValueError("vals must match the plan's nnz and value type")
@@ -221,7 +240,9 @@ class Plan:
         need = ctypes.c_size_t(0)
         check(lib().spmv_plan_export(self._h, code, None, 0, ctypes.byref(need)), "spmv_plan_export")
         dtype = {"partition": np.int32, "rg_group_ptr": np.int64, "rg_row_len": np.int32, "rg_col": np.int32,
-                 "long_rows": np.int32, "long_seg_begin": np.int64, "rg_perm": np.int32,
+                 "long_rows": np.int32, "long_seg_begin": np.int64, "rg_perm": np.int32, "t_ptr": np.int32,
+                 "t_idx": np.int32, "t_src": np.int32,
+                 "t_vals": np.float64 if str(self.dtype) == "torch.float64" else np.float32,
                  "rg_val": np.float64 if str(self.dtype) == "torch.float64" else np.float32}[what]
         buf = np.empty(need.value // np.dtype(dtype).itemsize, dtype=dtype)
         check(lib().spmv_plan_export(self._h, code, buf.ctypes.data if buf.size else None, need.value, None),

@@ -58,6 +58,13 @@ struct spmv_plan_s {
     void *rg = nullptr;
     size_t rg_bytes = 0;
 
+    // A^T in CSR form (spmv_execute_transposed) and its own plan
+    void *tr = nullptr;
+    size_t tr_bytes = 0;
+    int32_t *t_ptr = nullptr, *t_idx = nullptr, *t_src = nullptr;
+    void *t_vals = nullptr;
+    spmv_plan_s *tplan = nullptr;
+
     // SpMM (spmv_execute_multi): warps and their scratch
     bool with_spmm = false;
     bool has_partition = false;
@@ -153,6 +160,8 @@ int64_t rows_at_least(const spmv_row_stats_t &s, int32_t len) {
 
 void destroy_plan(spmv_plan_s *p) {
     if (!p) return;
+    if (p->tplan) destroy_plan(p->tplan);
+    if (p->tr) cudaFree(p->tr);
     if (p->rg) cudaFree(p->rg);
     if (p->aux) cudaFree(p->aux);
     if (p->spmm) cudaFree(p->spmm);
@@ -282,6 +291,41 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) return cuda_fail(e, "Row-grouped copy");
     }
+    return SPMV_OK;
+}
+
+// A^T in CSR form (one allocation the plan keeps), built with a temporary
+// scratch, and a plan of its own for it.
+spmv_status_t build_transpose(spmv_plan_s *p, cudaStream_t stream) {
+    const size_t vs = value_size(p->dtype);
+    const size_t o_ptr = 0;
+    const size_t o_idx = align_up(o_ptr + sizeof(int32_t) * ((size_t)p->n + 1), 256);
+    const size_t o_src = align_up(o_idx + sizeof(int32_t) * (size_t)p->nnz, 256);
+    const size_t o_val = align_up(o_src + sizeof(int32_t) * (size_t)p->nnz, 256);
+    p->tr_bytes = align_up(o_val + vs * (size_t)p->nnz, 256);
+    cudaError_t e = cudaMalloc(&p->tr, p->tr_bytes);
+    if (e != cudaSuccess) {
+        p->tr = nullptr;
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the transpose: ") + cudaGetErrorString(e));
+    }
+    char *b = static_cast<char *>(p->tr);
+    p->t_ptr = reinterpret_cast<int32_t *>(b + o_ptr);
+    p->t_idx = reinterpret_cast<int32_t *>(b + o_idx);
+    p->t_src = reinterpret_cast<int32_t *>(b + o_src);
+    p->t_vals = b + o_val;
+    void *scratch = nullptr;
+    e = cudaMalloc(&scratch, (size_t)transpose_scratch_bytes(p->n, p->nnz));
+    if (e != cudaSuccess) return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the transpose scratch: ") + cudaGetErrorString(e));
+    e = launch_transpose(p->dtype, p->m, p->n, p->nnz, p->row_ptr, p->col_idx, p->vals, scratch, p->t_ptr, p->t_idx,
+                         p->t_vals, p->t_src, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    cudaFree(scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "transpose");
+    spmv_plan_t t = nullptr;
+    const spmv_status_t st = spmv_plan_create_ex(&t, p->n, p->m, p->nnz, p->t_ptr, p->t_idx, p->t_vals, p->dtype,
+                                                 nullptr, reinterpret_cast<spmv_stream_t>(stream));
+    if (st != SPMV_OK) return st;
+    p->tplan = t;
     return SPMV_OK;
 }
 
@@ -470,6 +514,13 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
             return cuda_fail(e, "SpMM scratch");
         }
     }
+    if (opt.with_transpose) {
+        const spmv_status_t st = build_transpose(p, stream);
+        if (st != SPMV_OK) {
+            destroy_plan(p);
+            return st;
+        }
+    }
     if (is_rgcsr(p->kernel) || p->kernel == SPMV_KERNEL_LONG_ROWS) {
         const spmv_status_t st = build_row_layouts(p, opt, stream);
         if (st != SPMV_OK) {
@@ -566,10 +617,24 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
     return SPMV_OK;
 }
 
+spmv_status_t spmv_execute_transposed(spmv_plan_t p, double alpha, const void *x, double beta, void *y,
+                                      spmv_stream_t stream) {
+    if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
+    if (!p->tplan) return fail(SPMV_ERR_INVALID_ARG, "plan was created without with_transpose");
+    return spmv_execute(p->tplan, alpha, x, beta, y, stream);
+}
+
 spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stream_t stream_handle) {
     if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
     if (!vals && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "vals is NULL");
     p->vals = vals;
+    if (p->tplan) {  // A^T's values in their new order, then its plan's own copy
+        const cudaError_t e = launch_transpose_values(p->dtype, p->nnz, p->t_src, nullptr, vals, nullptr, p->t_vals,
+                                                      reinterpret_cast<cudaStream_t>(stream_handle));
+        if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_update_values");
+        const spmv_status_t st = spmv_plan_update_values(p->tplan, p->t_vals, stream_handle);
+        if (st != SPMV_OK) return st;
+    }
     if (is_rgcsr(p->kernel) && p->rg_slots > 0) {
         // the pattern is unchanged: only the values move into the copy
         const cudaError_t e = launch_rgcsr_pack(p->dtype, p->m, p->row_ptr, p->col_idx, vals, p->g_log2, p->group_ptr,
@@ -601,7 +666,13 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->num_tiles = p->num_tiles;
     info->num_long_rows = p->num_long_rows;
     info->launches_per_execute = p->m > 0 ? 1 + (p->num_long_rows > 0 ? 1 : 0) : 0;
-    info->workspace_bytes = (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes + p->spmm_bytes);
+    info->workspace_bytes = (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes + p->spmm_bytes + p->tr_bytes);
+    info->transposed_kernel = p->tplan ? p->tplan->kernel : -1;
+    if (p->tplan) {
+        spmv_plan_info_t ti;
+        spmv_plan_info(p->tplan, &ti);
+        info->transposed_launches = ti.launches_per_execute;
+    }
     info->stats = p->stats;
     info->long_row_min = p->num_long_rows > 0 ? p->long_min : 0;
     info->long_segment_nnz = kLongSegmentNnz;
@@ -657,6 +728,25 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
         } else {
             src = p->seg_begin;
             size = p->num_long_rows > 0 ? sizeof(int64_t) * (size_t)(p->num_long_rows + 1) : 0;
+        }
+        break;
+    case SPMV_EXPORT_T_PTR:
+    case SPMV_EXPORT_T_IDX:
+    case SPMV_EXPORT_T_VALS:
+    case SPMV_EXPORT_T_SRC:
+        if (!p->tr) return fail(SPMV_ERR_INVALID_ARG, "plan has no transpose");
+        if (what == SPMV_EXPORT_T_PTR) {
+            src = p->t_ptr;
+            size = sizeof(int32_t) * ((size_t)p->n + 1);
+        } else if (what == SPMV_EXPORT_T_IDX) {
+            src = p->t_idx;
+            size = sizeof(int32_t) * (size_t)p->nnz;
+        } else if (what == SPMV_EXPORT_T_SRC) {
+            src = p->t_src;
+            size = sizeof(int32_t) * (size_t)p->nnz;
+        } else {
+            src = p->t_vals;
+            size = value_size(p->dtype) * (size_t)p->nnz;
         }
         break;
     case SPMV_EXPORT_RG_PERM:

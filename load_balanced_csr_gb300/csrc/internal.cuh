@@ -171,6 +171,18 @@ struct SpmmArgs {
 };
 cudaError_t launch_spmm(spmv_dtype_t dtype, const SpmmArgs &a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- transpose
+// A^T in CSR form: t_ptr[n+1], t_idx[nnz] (rows, increasing in each
+// column), t_vals[nnz], t_src[nnz] (position in A).  scratch:
+// transpose_scratch_bytes(n, nnz) bytes, 256-byte aligned.
+int64_t transpose_scratch_bytes(int32_t n, int32_t nnz);
+cudaError_t launch_transpose(spmv_dtype_t dtype, int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
+                             const int32_t *col_idx, const void *vals, void *scratch, int32_t *t_ptr,
+                             int32_t *t_idx, void *t_vals, int32_t *t_src, cudaStream_t stream);
+// t_vals[p] = vals[t_src[p]] (and t_idx[p] = row_of[t_src[p]] when t_idx).
+cudaError_t launch_transpose_values(spmv_dtype_t dtype, int32_t nnz, const int32_t *t_src, const int32_t *row_of,
+                                    const void *vals, int32_t *t_idx, void *t_vals, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace lbcsr
