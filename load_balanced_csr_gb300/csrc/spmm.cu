@@ -6,12 +6,14 @@
 //
 // Each warp takes the same share of the merge path as in the SpMV kernel
 // (the plan's partition: a contiguous run of row ends and nonzeros, cut
-// into equal tiles) and walks its run row by row.  Its lanes span the
-// columns of X and Y -- 32 at a time (up to kSpmmBlocks * 32 per launch),
-// or, when k is small, k rounded up to a power of two with several
-// nonzeros per warp step -- so every X row it gathers and every Y row it
-// writes is one coalesced access.  Row ends arrive 32 rows at a time, and
-// the loads of 8 warp steps are in flight together.
+// into equal tiles).  The rows that lie wholly inside the run are summed
+// by sub-warps of k' lanes (k' = k rounded up to a power of two, at most
+// 32): 32 / k' rows at once, each sub-warp walking its row's nonzeros with
+// its lanes over the columns; with k > 16 a sub-warp is the whole warp,
+// which takes 32 columns at a time (up to kSpmmBlocks * 32 per launch).
+// The rows cut by the run's ends are summed by the whole warp, with several
+// of the row's nonzeros per step when k is small.  Every X row gathered
+// and every Y row written is one coalesced access.
 //
 // A row cut between warps is finished as in the SpMV kernel: each warp
 // holding part of it stores its k partial sums, counts in on the row's
@@ -102,19 +104,111 @@ __device__ void spmm_cut_row(const SpmmParams<V> &p, int lane, const V (&part)[K
     if (lane == 0) p.arrivals[last] = 0;  // ready for the next product
 }
 
-// The walk, row by row.  KP (a power of two, 1..32) is the number of
-// lanes per nonzero: with KB == 1 and k <= KP <= 32, a warp step takes
-// S = 32 / KP nonzeros at once -- lane l serves slot l / KP, column l % KP --
-// and each slot sums every S-th nonzero of the row; the slots are added by
-// xor-shuffles when the row ends.  With KB > 1 (k > 32) KP is 32 and S = 1.
+// Nonzeros [j, stop) of one row summed by the whole warp: S = 32 / KP
+// nonzeros per warp step (lane l serves slot l / KP, column l % KP), the
+// slots added by xor-shuffles at the end; every lane gets the row's sums.
+template <typename V, int KB, int KP>
+__device__ __forceinline__ void spmm_warp_row(const SpmmParams<V> &p, long long j, long long stop, int lane,
+                                              V (&acc)[KB]) {
+    constexpr int S = 32 / KP;
+    constexpr int U = 8;
+    const int slot = lane / KP;
+    const int tcol = lane % KP;
+#pragma unroll
+    for (int b = 0; b < KB; ++b) acc[b] = V(0);
+    for (; j < stop; j += (long long)U * S) {
+        int cc[U];
+        V vv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long q = j + (long long)u * S + slot;
+            cc[u] = q < stop ? ld_stream(p.col_idx + q) : -1;
+            vv[u] = q < stop ? ld_stream(p.vals + q) : V(0);
+        }
+        V xv[U][KB];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int b = 0; b < KB; ++b) {
+                const int t = b * KP + tcol;
+                xv[u][b] = cc[u] >= 0 && t < p.k ? ld_gather(p.X + (long long)cc[u] * p.ldx + t) : V(0);
+            }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int b = 0; b < KB; ++b) acc[b] = fma(vv[u], xv[u][b], acc[b]);
+    }
+#pragma unroll
+    for (int off = KP; off < 32; off <<= 1)
+#pragma unroll
+        for (int b = 0; b < KB; ++b) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+}
+
+// The rows that lie wholly inside a warp's run, [r0, r1), summed by
+// sub-warps of KP lanes (KB == 1): sub-warp s takes rows r0 + s, r0 + s + S,
+// ..., walks each row's nonzeros in order (lanes over columns) and writes
+// its row of Y.  S rows are in flight at once, which matters for short
+// rows.  A row longer than kSpmmSubRowMax would hold up the other
+// sub-warps: the whole warp sums it right after its group.
+constexpr int kSpmmSubRowMax = 64;
+
+template <typename V, int KP>
+__device__ __forceinline__ void spmm_subwarp_rows(const SpmmParams<V> &p, long long r0, long long r1, int lane,
+                                                  uint64_t pol) {
+    constexpr int S = 32 / KP;
+    constexpr int U = 4;  // the tree below adds exactly four sums
+    const int sub = lane / KP;
+    const int tcol = lane % KP;
+    const bool col_ok = tcol < p.k;
+    for (long long rr = r0; rr < r1; rr += S) {
+        const long long r = rr + sub;
+        const bool in = r < r1;
+        long long q = in ? p.row_ptr[r] : 0;
+        const long long e = in ? p.row_ptr[r + 1] : 0;
+        const bool is_long = e - q > kSpmmSubRowMax;
+        const bool has_row = in && !is_long;
+        if (!has_row) q = e;
+        V acc[U];  // nonzero q goes to sum q mod U (added as a tree below)
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = V(0);
+        while (__any_sync(0xffffffffu, q < e)) {
+            int cc[U];
+            V vv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                cc[u] = q + u < e ? ld_stream(p.col_idx + q + u) : -1;
+                vv[u] = q + u < e ? ld_stream(p.vals + q + u) : V(0);
+            }
+            V xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                xv[u] = cc[u] >= 0 && col_ok ? ld_gather(p.X + (long long)cc[u] * p.ldx + tcol) : V(0);
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc[u] = fma(vv[u], xv[u], acc[u]);
+            q += U;
+        }
+        if (has_row && col_ok) {
+            V y = p.alpha * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            if (p.beta != V(0)) y = fma(p.beta, p.Y[r * p.ldy + tcol], y);
+            store_stream(p.Y + r * p.ldy + tcol, y, pol);
+        }
+        // the group's long rows, one by one, by the whole warp
+        unsigned longs = __ballot_sync(0xffffffffu, in && is_long && tcol == 0);
+        while (longs) {
+            const int l = __ffs(longs) - 1;
+            longs &= longs - 1;
+            const long long rl = rr + l / KP;
+            V a[1];
+            spmm_warp_row<V, 1, KP>(p, p.row_ptr[rl], p.row_ptr[rl + 1], lane, a);
+            spmm_store_row<V, 1, KP>(p, rl, a, lane, pol);
+        }
+    }
+}
+
 template <typename V, int KB, int KP>
 __global__ void __launch_bounds__(kSpmmThreads)
 spmm_kernel(const SpmmParams<V> p) {
-    constexpr int S = 32 / KP;  // nonzeros per warp step
-    constexpr int U = 8;        // warp steps whose loads are in flight together
     const int lane = threadIdx.x & 31;
-    const int slot = lane / KP;
-    const int tcol = lane % KP;
     const long long me = (long long)blockIdx.x * (kSpmmThreads / 32) + (threadIdx.x >> 5);
     if (me >= p.W) return;
     const uint64_t stream_pol = l2_policy_evict_first();
@@ -122,66 +216,33 @@ spmm_kernel(const SpmmParams<V> p) {
     const int2 s0 = p.part[me * p.P / p.W];
     const int2 e0 = p.part[(me + 1) * p.P / p.W];
     const long long i_s = s0.x, j_s = s0.y, i_e = e0.x, j_e = e0.y;
-
-    bool head = i_s < p.m && p.row_ptr[i_s] < j_s;  // the first row began in an earlier warp
-    long long rb = -(1ll << 40);                      // first row whose end the lanes hold (none yet)
-    int re_lane = 0;                                  // lane q: row_ptr[rb + 1 + q]
-    auto row_end = [&](long long row) -> long long {
-        if (row < rb || row >= rb + 32) {  // refill: rows row .. row + 31
-            rb = row;
-            const long long q = rb + 1 + lane;
-            re_lane = q <= p.m ? p.row_ptr[q] : p.nnz;
-        }
-        return __shfl_sync(0xffffffffu, re_lane, (int)(row - rb));
-    };
-
     V acc[KB];
-    long long j = j_s;
-    for (long long r = i_s;; ++r) {
-        const long long stop = r < i_e ? row_end(r) : j_e;  // this row's nonzeros in the run: [j, stop)
-#pragma unroll
-        for (int b = 0; b < KB; ++b) acc[b] = V(0);
-        for (; j < stop; j += (long long)U * S) {
-            int cc[U];
-            V vv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const long long q = j + (long long)u * S + slot;
-                cc[u] = q < stop ? ld_stream(p.col_idx + q) : -1;
-                vv[u] = q < stop ? ld_stream(p.vals + q) : V(0);
-            }
-            V xv[U][KB];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int b = 0; b < KB; ++b) {
-                    const int t = b * KP + tcol;
-                    xv[u][b] = cc[u] >= 0 && t < p.k ? ld_gather(p.X + (long long)cc[u] * p.ldx + t) : V(0);
-                }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int b = 0; b < KB; ++b) acc[b] = fma(vv[u], xv[u][b], acc[b]);
+    long long r0 = i_s;
+    // the row open at the run's start, if it began in an earlier warp
+    if (i_s < p.m && p.row_ptr[i_s] < j_s) {
+        if (i_s < i_e) {  // it ends in this run: finish it with the earlier warps' partials
+            spmm_warp_row<V, KB, KP>(p, j_s, p.row_ptr[i_s + 1], lane, acc);
+            const long long first = spmm_warp_of_unit((long long)p.row_ptr[i_s] + i_s, p.T, p.P, p.W);
+            spmm_cut_row<V, KB, KP>(p, lane, acc, true, me, i_s, first, me, stream_pol);
+            r0 = i_s + 1;
         }
-        j = stop;
-        // the slots' sums of this row (a fixed tree)
-#pragma unroll
-        for (int off = KP; off < 32; off <<= 1)
-#pragma unroll
-            for (int b = 0; b < KB; ++b) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
-        if (r >= i_e) break;
-        if (head) {
-            head = false;
-            const long long first = spmm_warp_of_unit((long long)p.row_ptr[r] + r, p.T, p.P, p.W);
-            spmm_cut_row<V, KB, KP>(p, lane, acc, true, me, r, first, me, stream_pol);
-        } else {
+        // else: the whole run lies inside that row -- the tail below
+    }
+    // the rows wholly inside the run
+    if (KB == 1 && KP < 32) {
+        spmm_subwarp_rows<V, KP>(p, r0, i_e, lane, stream_pol);
+    } else {
+        for (long long r = r0; r < i_e; ++r) {
+            spmm_warp_row<V, KB, KP>(p, p.row_ptr[r], p.row_ptr[r + 1], lane, acc);
             spmm_store_row<V, KB, KP>(p, r, acc, lane, stream_pol);
         }
     }
     // the row open at the run's end, if it has nonzeros in this run
     if (i_e < p.m) {
         const long long rp_e = p.row_ptr[i_e];
-        if (j_e > (rp_e > j_s ? rp_e : j_s)) {
+        const long long from = rp_e > j_s ? rp_e : j_s;
+        if (j_e > from) {
+            spmm_warp_row<V, KB, KP>(p, from, j_e, lane, acc);
             const long long first = spmm_warp_of_unit(rp_e + i_e, p.T, p.P, p.W);
             const long long last = spmm_warp_of_unit((long long)p.row_ptr[i_e + 1] + i_e, p.T, p.P, p.W);
             spmm_cut_row<V, KB, KP>(p, lane, acc, false, me, i_e, first, last, stream_pol);
