@@ -65,9 +65,12 @@ typedef enum {
                                    long rows, if any, by the long-row kernel */
     SPMV_KERNEL_LONG_ROWS = 4,  /* long rows by the long-row kernel (one warp per segment of
                                    4096 nonzeros), the other rows one thread per row */
-    SPMV_KERNEL_RGCSR_SORTED = 5 /* Row-grouped CSR (groups of 32) over the rows listed, in
+    SPMV_KERNEL_RGCSR_SORTED = 5,/* Row-grouped CSR (groups of 32) over the rows listed, in
                                    each window of 1024 rows, by decreasing length, which
                                    cuts the padding; long rows by the long-row kernel */
+    SPMV_KERNEL_GROUP_MAPPED = 6 /* group-level schedule ("A GPU load-balancing programming
+                                   model", section 5.2.3): a CTA per 256 rows, their
+                                   nonzeros shared by the CTA's threads */
 } spmv_kernel_t;
 
 /* Options for spmv_plan_create_ex; zero-initialise and set what you need. */

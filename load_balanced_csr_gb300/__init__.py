@@ -18,7 +18,8 @@ from . import _build
 
 __all__ = ["Plan", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
 
-KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4, "rgcsr_sorted": 5}
+KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4, "rgcsr_sorted": 5,
+           "group_mapped": 6}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 EXPORTS = {"partition": 0, "rg_group_ptr": 1, "rg_row_len": 2, "rg_col": 3, "rg_val": 4, "long_rows": 5,
            "long_seg_begin": 6, "rg_perm": 7, "t_ptr": 8, "t_idx": 9, "t_vals": 10, "t_src": 11}

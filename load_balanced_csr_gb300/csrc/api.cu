@@ -110,6 +110,7 @@ spmv_kernel_t env_kernel() {
     if (!std::strcmp(v, "rgcsr")) return SPMV_KERNEL_RGCSR;
     if (!std::strcmp(v, "long_rows")) return SPMV_KERNEL_LONG_ROWS;
     if (!std::strcmp(v, "rgcsr_sorted")) return SPMV_KERNEL_RGCSR_SORTED;
+    if (!std::strcmp(v, "group_mapped")) return SPMV_KERNEL_GROUP_MAPPED;
     return SPMV_KERNEL_AUTO;
 }
 
@@ -389,7 +390,7 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     if (options) opt = *options;
     spmv_kernel_t forced = (spmv_kernel_t)opt.kernel;
     if (forced == SPMV_KERNEL_AUTO) forced = env_kernel();
-    if (forced < SPMV_KERNEL_AUTO || forced > SPMV_KERNEL_RGCSR_SORTED)
+    if (forced < SPMV_KERNEL_AUTO || forced > SPMV_KERNEL_GROUP_MAPPED)
         return fail(SPMV_ERR_INVALID_ARG, "unknown kernel option");
     if (opt.rgcsr_group && opt.rgcsr_group != 32 && opt.rgcsr_group != 64 && opt.rgcsr_group != 128 &&
         opt.rgcsr_group != 256)
@@ -543,6 +544,9 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     switch (p->kernel) {
     case SPMV_KERNEL_THREAD_ROW:
         e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, 0, stream);
+        break;
+    case SPMV_KERNEL_GROUP_MAPPED:
+        e = launch_group_mapped(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, stream);
         break;
     case SPMV_KERNEL_LONG_ROWS:
         // long rows first (they take longest), then the others

@@ -113,6 +113,11 @@ cudaError_t launch_rgcsr_pack(spmv_dtype_t dtype, int32_t m, const int32_t *row_
                               cudaStream_t stream);
 
 // ---------------------------------------------------------------- row kernels
+// Group-mapped schedule: a CTA per 256 rows, atoms staged by chunks.
+cudaError_t launch_group_mapped(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
+                                const void *vals, const void *x, void *y, double alpha, double beta,
+                                cudaStream_t stream);
+
 // Thread per row; rows of length >= skip_min_len (when > 0) are skipped.
 cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr,
                                   const int32_t *col_idx, const void *vals, const void *x, void *y,

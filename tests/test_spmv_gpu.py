@@ -42,7 +42,7 @@ def inputs(m, n, max_len, seed, dtype, empty_frac=0.2, dist=synth.DIST_NORMAL):
 
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
 @pytest.mark.parametrize("alpha,beta", ALPHA_BETA)
-@pytest.mark.parametrize("kernel", ["merge_path", "thread_row"])
+@pytest.mark.parametrize("kernel", ["merge_path", "thread_row", "group_mapped"])
 def test_random_matrices(dtype, alpha, beta, kernel):
     for seed, (m, n, L) in enumerate([(5000, 3000, 20), (20011, 20011, 6), (1, 4000, 4000), (9333, 1, 1)]):
         if kernel == "thread_row" and L > 256:
@@ -94,7 +94,7 @@ def test_degenerate_shapes(dtype):
     plan(torch.zeros(5, dtype=t, device="cuda"), torch.zeros(0, dtype=t, device="cuda"))
     plan.close()
     # nnz = 0 with rows; all empty -> y = beta*y_old
-    for kernel in ("merge_path", "thread_row"):
+    for kernel in ("merge_path", "thread_row", "group_mapped"):
         A = synth.fill_random(np.zeros(3000, np.int32), 10, seed=1, dtype=dtype)
         x = synth.vector(10, synth.DIST_NORMAL, 1, synth.STREAM_X, dtype)
         y0 = synth.vector(3000, synth.DIST_NORMAL, 1, synth.STREAM_Y, dtype)
@@ -108,7 +108,7 @@ def test_degenerate_shapes(dtype):
     # single row, single column, single nonzero
     A = synth.fill_random(np.ones(1, np.int32), 1, seed=2, dtype=dtype)
     x = synth.vector(1, synth.DIST_NORMAL, 2, synth.STREAM_X, dtype)
-    for kernel in ("auto", "merge_path", "thread_row"):
+    for kernel in ("auto", "merge_path", "thread_row", "group_mapped"):
         y, _ = run(A, x, None, 1.0, 0.0, kernel=kernel)
         assert_close_to_oracle(A, x, y, 1.0, 0.0, None, label=f"1x1 {kernel}")
 
@@ -143,7 +143,7 @@ def test_integer_inputs_are_exact():
     """Small-integer values make every sum exact in fp64: the GPU must then
     equal the oracle bit for bit, whatever the summation order."""
     A, x, y0 = inputs(40000, 30000, 40, 12, "f64", dist=synth.DIST_SMALL_INT)
-    for kernel in ("merge_path", "thread_row"):
+    for kernel in ("merge_path", "thread_row", "group_mapped"):
         y, _ = run(A, x, y0, 2.0, -1.0, kernel=kernel)
         ref, _ = oracle.spmv(A.row_ptr, A.col_idx, A.vals, x, 2.0, -1.0, y0)
         np.testing.assert_array_equal(y, ref)
