@@ -174,6 +174,23 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The largest v over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gflops(nnz: int, world: int, ms_per_step: float, k: int = 1) -> float:
+    """Whole-job throughput: every rank runs one product of 2*nnz*k flops per
+    step (replicas), over the slowest rank's time per step."""
+    return 2.0 * nnz * k * world / (ms_per_step * 1e-3) / 1e9
+
+
 def run_gpu(args, workload_name: str) -> dict | None:
     import torch
     import torch.distributed as dist
@@ -233,12 +250,8 @@ def run_gpu(args, workload_name: str) -> dict | None:
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
 
-    total_ms = start_all.elapsed_time(end_all)
+    total_ms = max_over_ranks(start_all.elapsed_time(end_all), world, dev)
     per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3  # us
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
 
     # end to end through the public API: pinned host x in, host y out, every step
     e2e = None
@@ -262,14 +275,10 @@ def run_gpu(args, workload_name: str) -> dict | None:
             y_h.copy_(y, non_blocking=True)
         e_e.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = s_e.elapsed_time(e_e) / ke
-        if world > 1:
-            te = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-            e2e_ms = float(te.item())
+        e2e_ms = max_over_ranks(s_e.elapsed_time(e_e) / ke, world, dev)
         s = A.vals.dtype.itemsize
         h2d = A.n * s + (A.m * s if W.y0 is not None else 0)
-        e2e = {"value": round(2.0 * A.nnz / (e2e_ms * 1e-3) / 1e9 * world, 3), "unit": "GFLOP/s",
+        e2e = {"value": round(job_gflops(A.nnz, world, e2e_ms), 3), "unit": "GFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(A.m * s), "ms_per_step": round(e2e_ms, 4),
                "steps": ke}
     plan.close()
@@ -278,7 +287,7 @@ def run_gpu(args, workload_name: str) -> dict | None:
 
     ms_step = total_ms / K
     bc = compulsory_bytes(A, W.beta)
-    gflops = 2.0 * A.nnz / (ms_step * 1e-3) / 1e9 * world
+    gflops = job_gflops(A.nnz, world, ms_step)
     mean_us = float(per.mean())
     achieved = bc / (mean_us * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
