@@ -176,6 +176,23 @@ struct SpmmArgs {
 };
 cudaError_t launch_spmm(spmv_dtype_t dtype, const SpmmArgs &a, cudaStream_t stream);
 
+// SpMM over a Row-grouped copy with groups of 32 and no long rows (thread
+// per row, X rows gathered with 16-byte loads when aligned).
+struct RgSpmmArgs {
+    int32_t m, k;
+    const int64_t *group_ptr;
+    const int32_t *row_len;
+    const int32_t *perm;  // null: natural order
+    const int32_t *rg_col;
+    const void *rg_val;
+    const void *X;
+    int64_t ldx;
+    void *Y;
+    int64_t ldy;
+    double alpha, beta;
+};
+cudaError_t launch_rg_spmm(spmv_dtype_t dtype, const RgSpmmArgs &a, cudaStream_t stream);
+
 // ---------------------------------------------------------------- transpose
 // A^T in CSR form: t_ptr[n+1], t_idx[nnz] (rows, increasing in each
 // column), t_vals[nnz], t_src[nnz] (position in A).  scratch:

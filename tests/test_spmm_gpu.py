@@ -111,3 +111,17 @@ def test_spmm_deterministic_and_checks():
     with lb.Plan(rp, col, val, A.n) as plan:  # no SpMM scratch
         with pytest.raises(lb.SpmvError):
             plan.execute_multi(Xg, torch.zeros((A.m, 20), dtype=torch.float32, device="cuda"))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("kernel", ["rgcsr", "rgcsr_sorted"])
+def test_spmm_over_the_row_grouped_copy(dtype, kernel):
+    """Plans holding a Row-grouped copy (groups of 32, no long rows) run SpMM
+    one thread per row over it when one slice of columns (32 fp32, 16 fp64)
+    covers k: 16-byte X loads when aligned, scalar loads for a padded X;
+    wider X goes to the merge-path SpMM."""
+    A = synth.random_csr(3000, 2500, max_len=24, empty_frac=0.2, dist=synth.DIST_NORMAL, seed=11, dtype=dtype)
+    for k, pad in [(1, 0), (3, 1), (8, 0), (16, 0), (17, 0), (32, 0), (40, 2), (64, 0)]:
+        for alpha, beta in [(1.0, 0.0), (-0.5, 1.5)]:
+            X, Y0, Yg = run_spmm(A, k, alpha, beta, kernel=kernel, pad=pad, seed=k)
+            check(A, X, Y0, Yg, alpha, beta, f"spmm {kernel} {dtype} k={k} pad={pad}")
