@@ -366,7 +366,7 @@ def run_reference(args, workload_name: str) -> dict | None:
     gflops = 2.0 * nnz_s * args.steps / tot / 1e9
     sample = f"rows [0, {r}) of {A.m} ({nnz_s} of {A.nnz} nonzeros) per step"
     return {
-        "metric": METRIC, "value": round(gflops, 4), "unit": "GFLOP/s", "n_gpus": 0, "steps": args.steps,
+        "metric": METRIC, "value": round(gflops, 4), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": A.dtype, "data": "synthetic", "impl": "reference",
         "config": {"workload": workload_name, "description": W.description, "m": A.m, "n": A.n, "nnz": A.nnz,

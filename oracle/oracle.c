@@ -375,3 +375,52 @@ ORACLE_TRANSPOSE(oracle_transpose_f32, float)
     }
 ORACLE_SPMV_T(oracle_spmv_transposed_f64, double)
 ORACLE_SPMV_T(oracle_spmv_transposed_f32, float)
+
+/* Row by row: scatter every product of row i into a dense long double row
+ * with a mark per column, then gather the marked columns in order. */
+#define ORACLE_SPGEMM(NAME, T)                                                                            \
+    int NAME(int32_t m, int32_t k, int32_t n, const int32_t *a_ptr, const int32_t *a_col, const T *a_val, \
+             const int32_t *b_ptr, const int32_t *b_col, const T *b_val, int64_t *c_row_ptr,              \
+             int32_t *c_col, T *c_val) {                                                                  \
+        if (!check_row_ptr_basic(m, a_ptr) || !check_row_ptr_basic(k, b_ptr) || n < 0 || !c_row_ptr)     \
+            return 1;                                                                                     \
+        long double *acc = (long double *)calloc((size_t)(n > 0 ? n : 1), sizeof(long double));           \
+        char *mark = (char *)calloc((size_t)(n > 0 ? n : 1), 1);                                          \
+        if (!acc || !mark) {                                                                              \
+            free(acc);                                                                                    \
+            free(mark);                                                                                   \
+            return 1;                                                                                     \
+        }                                                                                                 \
+        c_row_ptr[0] = 0;                                                                                 \
+        for (int32_t i = 0; i < m; ++i) {                                                                 \
+            for (int32_t p = a_ptr[i]; p < a_ptr[i + 1]; ++p) {                                           \
+                int32_t q = a_col[p];                                                                     \
+                if (q < 0 || q >= k) {                                                                    \
+                    free(acc);                                                                            \
+                    free(mark);                                                                           \
+                    return 1;                                                                             \
+                }                                                                                         \
+                for (int32_t r = b_ptr[q]; r < b_ptr[q + 1]; ++r) {                                       \
+                    acc[b_col[r]] += (long double)a_val[p] * (long double)b_val[r];                        \
+                    mark[b_col[r]] = 1;                                                                   \
+                }                                                                                         \
+            }                                                                                             \
+            int64_t cnt = 0, out = c_row_ptr[i];                                                          \
+            for (int32_t j = 0; j < n; ++j)                                                               \
+                if (mark[j]) {                                                                            \
+                    if (c_col) {                                                                          \
+                        c_col[out + cnt] = j;                                                             \
+                        c_val[out + cnt] = (T)acc[j];                                                     \
+                    }                                                                                     \
+                    ++cnt;                                                                                \
+                    mark[j] = 0;                                                                          \
+                    acc[j] = 0.0L;                                                                        \
+                }                                                                                         \
+            c_row_ptr[i + 1] = c_row_ptr[i] + cnt;                                                        \
+        }                                                                                                 \
+        free(acc);                                                                                        \
+        free(mark);                                                                                       \
+        return 0;                                                                                         \
+    }
+ORACLE_SPGEMM(oracle_spgemm_f64, double)
+ORACLE_SPGEMM(oracle_spgemm_f32, float)

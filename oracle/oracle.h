@@ -165,6 +165,23 @@ int oracle_spmv_transposed_f32(int32_t m, int32_t n, const int32_t *row_ptr, con
                                float *y_out, double *mag_out);
 
 /*
+ * C = A * B for A m-by-k and B k-by-n in CSR form ([OpSparse], the
+ * Gustavson row-by-row product its sections 4-5 build on: row i of C is
+ * the sum over A's entries a_iq of a_iq times row q of B).  Accumulated in
+ * long double in a dense row; C's entries are the columns any product
+ * reaches (an exact zero sum stays an entry), listed in increasing column
+ * order.  Call with c_col == NULL to get c_row_ptr (m + 1 entries) only;
+ * then again with c_col and c_val of c_row_ptr[m] entries.  Returns 0, or
+ * 1 on bad arguments.
+ */
+int oracle_spgemm_f64(int32_t m, int32_t k, int32_t n, const int32_t *a_ptr, const int32_t *a_col,
+                      const double *a_val, const int32_t *b_ptr, const int32_t *b_col, const double *b_val,
+                      int64_t *c_row_ptr, int32_t *c_col, double *c_val);
+int oracle_spgemm_f32(int32_t m, int32_t k, int32_t n, const int32_t *a_ptr, const int32_t *a_col,
+                      const float *a_val, const int32_t *b_ptr, const int32_t *b_col, const float *b_val,
+                      int64_t *c_row_ptr, int32_t *c_col, float *c_val);
+
+/*
  * Row order of the window-sorted Row-grouped layout (an extension of
  * [RgCSR] section 3, whose weakness is the padding of a group to its
  * longest row, section 4): inside each window of `window` consecutive rows

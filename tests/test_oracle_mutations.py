@@ -43,6 +43,8 @@ MUTATIONS = [
      [pins.test_transpose_worked_example]),
     ("transposed product uses y index for x", "long double prod = (long double)vals[q] * (long double)x[i];", "long double prod = (long double)vals[q] * (long double)x[col_idx[q] % m];",
      [pins.test_spmv_transposed_equals_dense_product_exactly]),
+    ("spgemm drops the last product of a row of B", "for (int32_t r = b_ptr[q]; r < b_ptr[q + 1]; ++r) {", "for (int32_t r = b_ptr[q]; r + 1 < b_ptr[q + 1]; ++r) {",
+     [pins.test_spgemm_equals_dense_product_exactly]),
 ]
 
 

@@ -503,3 +503,51 @@ def test_spmv_transposed_equals_dense_product_exactly():
     for alpha, beta in [(1, 0), (-2, 3), (0, 1)]:
         y, _ = oracle.spmv_transposed(A.row_ptr, A.col_idx, A.vals, x, 29, alpha, beta, y0)
         np.testing.assert_array_equal(y, alpha * (dense.T @ x.astype(np.int64)) + beta * y0)
+
+
+# ---------------------------------------------------------------- SpGEMM
+
+
+def _dense(A, n):
+    D = np.zeros((A.m, n), dtype=np.int64)
+    for i in range(A.m):
+        for q in range(A.row_ptr[i], A.row_ptr[i + 1]):
+            D[i, A.col_idx[q]] = int(A.vals[q])
+    return D
+
+
+def test_spgemm_equals_dense_product_exactly():
+    """Small integers: values exact; the pattern is the set of (i, j) some
+    product reaches (a zero sum stays an entry), columns in order."""
+    A = synth.random_csr(23, 17, max_len=6, empty_frac=0.2, dist=synth.DIST_SMALL_INT, seed=1, dtype="f64")
+    B = synth.random_csr(17, 29, max_len=7, empty_frac=0.2, dist=synth.DIST_SMALL_INT, seed=2, dtype="f64")
+    rp, col, val = oracle.spgemm(A.row_ptr, A.col_idx, A.vals, B.row_ptr, B.col_idx, B.vals, 29)
+    DA, DB = _dense(A, 17), _dense(B, 29)
+    SA, SB = np.zeros((23, 17), np.int64), np.zeros((17, 29), np.int64)  # stored entries, zeros included
+    for i in range(23):
+        SA[i, A.col_idx[A.row_ptr[i]:A.row_ptr[i + 1]]] = 1
+    for i in range(17):
+        SB[i, B.col_idx[B.row_ptr[i]:B.row_ptr[i + 1]]] = 1
+    reach = (SA @ SB) > 0
+    C = DA @ DB
+    for i in range(23):
+        cols = col[rp[i]:rp[i + 1]]
+        assert cols.tolist() == np.flatnonzero(reach[i]).tolist()
+        np.testing.assert_array_equal(val[rp[i]:rp[i + 1]], C[i, cols])
+
+
+def test_spgemm_with_identity_and_permutation():
+    A = synth.random_csr(40, 30, max_len=8, empty_frac=0.1, dist=synth.DIST_NORMAL, seed=4, dtype="f64")
+    eye_p = np.arange(31, dtype=np.int32)
+    rp, col, val = oracle.spgemm(A.row_ptr, A.col_idx, A.vals, eye_p, np.arange(30, dtype=np.int32),
+                                 np.ones(30), 30)
+    np.testing.assert_array_equal(rp, A.row_ptr)
+    np.testing.assert_array_equal(col, A.col_idx)
+    np.testing.assert_array_equal(val, A.vals)
+    perm = np.random.default_rng(4).permutation(30).astype(np.int32)  # B maps column q to perm[q]
+    rp, col, val = oracle.spgemm(A.row_ptr, A.col_idx, A.vals, eye_p, perm, np.ones(30), 30)
+    for i in range(40):
+        cols = A.col_idx[A.row_ptr[i]:A.row_ptr[i + 1]]
+        order = np.argsort(perm[cols])
+        assert col[rp[i]:rp[i + 1]].tolist() == perm[cols][order].tolist()
+        np.testing.assert_array_equal(val[rp[i]:rp[i + 1]], A.vals[A.row_ptr[i]:A.row_ptr[i + 1]][order])
