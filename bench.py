@@ -464,6 +464,76 @@ def run_spmm(args, workload_name: str) -> dict | None:
     }
 
 
+def run_spgemm(args, workload_name: str) -> dict | None:
+    """C = A*A on the workload's matrix (the squared-matrix benchmark of
+    OpSparse): the symbolic phase (handle creation: checks, binning, row
+    sizes) timed on the host around a synchronised call, the numeric phase
+    with CUDA events.  GFLOP/s = 2 * products / numeric time, products = the
+    intermediate products a*b of Gustavson's method."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    A = synth.workload(workload_name).A
+    s = A.vals.dtype.itemsize
+    rp = torch.from_numpy(A.row_ptr).to(dev)
+    col = torch.from_numpy(A.col_idx).to(dev)
+    val = torch.from_numpy(A.vals).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sym = []
+    for _ in range(3):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        h = lb.SpGEMM(rp, col, rp, col, A.n, val.dtype, stream=stream)
+        sym.append((time.perf_counter() - t0) * 1e3)
+        if _ < 2:
+            h.close()
+    out = h.compute(val, val, stream=stream)
+    for _ in range(args.warmup):
+        h.compute(val, val, out=out, stream=stream)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.15 if sampler else 0)
+    K = min(args.steps, 30)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0 = time.time()
+    for a, b in ev:
+        a.record(stream)
+        h.compute(val, val, out=out, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop(t0, time.time()) if sampler else None
+    per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3
+    info = h.info()
+    status = h.device_status()
+    h.close()
+    if rank != 0:
+        return None
+    med = float(np.median(per))
+    products = info["products"]
+    # compulsory bytes of the numeric phase: A and B read once, C written once
+    bytes_ = 2 * (A.nnz * (4 + s) + (A.m + 1) * 4) + info["c_nnz"] * (4 + s) + (A.m + 1) * 4
+    peak, peak_kind = measured_peak()
+    achieved = bytes_ / (float(per.mean()) * 1e-6) / 1e9
+    return {
+        "metric": "SpGEMM C = A*A GFLOP/s (2 * intermediate products / numeric phase)",
+        "value": round(2.0 * products / (med * 1e-6) / 1e9, 2), "unit": "GFLOP/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "median_us": round(med, 1), "higher_is_better": True, "dtype": A.dtype,
+        "data": "synthetic",
+        "config": {"workload": workload_name, "products": products, "c_nnz": info["c_nnz"],
+                   "bin_rows": info["bin_rows"], "dense_slots": info["dense_slots"],
+                   "dense_pieces": info["dense_pieces"], "dense_waves": info["dense_waves"],
+                   "launches_per_compute": info["launches_per_compute"],
+                   "symbolic_ms_median": round(float(np.median(sym)), 2), "device_status": status},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes_per_product": int(bytes_), "traffic": None},
+        "clocks": clocks,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,6 +548,7 @@ def main():
     ap.add_argument("--long-min", type=int, default=0, help="long-row threshold (0 = plan's default)")
     ap.add_argument("--rhs", type=int, default=0, help="k > 0: time SpMM with k right-hand sides instead")
     ap.add_argument("--transposed", action="store_true", help="time the transposed product A^T x instead")
+    ap.add_argument("--spgemm", action="store_true", help="time SpGEMM C = A*A instead")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -498,11 +569,12 @@ def main():
         dist.init_process_group("nccl")
     names = synth.WORKLOADS if args.all else [args.workload]
     for name in names:
-        out = run_spmm(args, name) if args.rhs > 0 else run_gpu(args, name)
+        out = run_spgemm(args, name) if args.spgemm else run_spmm(args, name) if args.rhs > 0 else \
+            run_gpu(args, name)
         if out is not None:
             # the oracle is timed on rank 0 at N = 1 only
             out["cpu_baseline"] = cpu_baseline_leg(name, args.cpu_budget) \
-                if world == 1 and not args.no_cpu_baseline else None
+                if world == 1 and not args.no_cpu_baseline and not args.spgemm else None
             out["source_hash"] = kernel_source_hash()
             print(json.dumps(out), flush=True)
     if world > 1:

@@ -287,6 +287,76 @@ spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz, const int3
  */
 spmv_status_t spmv_plan_device_status(spmv_plan_t plan, int32_t *flags);
 
+/*
+ * Sparse times sparse, C = A * B, after OpSparse ("OpSparse: a highly
+ * optimized framework for sparse general matrix multiplication on GPUs",
+ * sections 3 and 5): Gustavson's row-by-row product (row i of C sums, over
+ * the entries a_ip of row i of A, a_ip times row p of B), in two phases.
+ *
+ * spmv_spgemm_create takes the PATTERNS of A (m-by-k: a_row_ptr[m+1],
+ * a_col_idx[a_nnz]) and B (k-by-n: b_row_ptr[k+1], b_col_idx[b_nnz]), device
+ * int32 CSR arrays that the handle borrows until it is destroyed (their
+ * contents must not change meanwhile).  It checks both as
+ * spmv_plan_create does, counts the products of each row of C, bins the
+ * rows by that count, sizes every row of C (the symbolic phase: sorted
+ * lists for rows of at most 16 products, hash sets in shared memory up to
+ * 4096; above, a dense row of C per row in global memory, the row's
+ * products cut into equal pieces of at most 32768, a CTA each, with up to
+ * 8 GiB of such rows at once),
+ * and writes the number of entries of C to *c_nnz (HOST).  An entry of C
+ * exists where at least one product lands, even if the products sum to
+ * zero.  Synchronous (it waits for `stream` several times).
+ * Limits: m, k, n >= 0; m + a_nnz and k + b_nnz < 2^31; C must have fewer
+ * than 2^31 entries (else INVALID_ARG, with *c_nnz still set).
+ * Errors: INVALID_ARG, INVALID_CSR, ALLOC, CUDA, UNSUPPORTED.  On error
+ * *out is NULL.
+ *
+ * spmv_spgemm_compute is the numeric phase: with the values a_vals[a_nnz]
+ * and b_vals[b_nnz] (device, the handle's value type) it writes C in CSR
+ * form into caller-allocated device arrays c_row_ptr[m+1] (int32),
+ * c_col_idx[c_nnz] (int32, increasing within each row) and c_vals[c_nnz].
+ * It may be called again with new values of the same patterns.
+ * Asynchronous on `stream`; allocates nothing.  Outside the rows of at
+ * most 16 products (summed in the order of the row's products), the
+ * products of an entry are added in an order that may change from call to
+ * call (atomics), so its last bits may too; the pattern is always the same.
+ * Errors: INVALID_ARG (null handle or pointers), CUDA.
+ */
+typedef struct spmv_spgemm_s *spmv_spgemm_t;
+
+typedef struct {
+    int32_t m, k, n;
+    int32_t dtype;               /* spmv_dtype_t */
+    int64_t a_nnz, b_nnz, c_nnz;
+    int64_t products;            /* sum over the rows of C of their products */
+    int64_t bin_rows[8];         /* rows of C by products: <= 16, <= 128, <= 512, <= 1024,
+                                    <= 2048, <= 4096, more (the dense bin); [7] unused */
+    int32_t dense_slots;         /* dense-bin rows of C held at once (one wave) */
+    int32_t launches_per_compute;/* kernel launches one spmv_spgemm_compute issues */
+    int64_t workspace_bytes;     /* device memory the handle owns */
+    int64_t dense_pieces;        /* dense-bin pieces of at most 32768 products, a CTA each */
+    int64_t dense_waves;         /* waves of dense-bin rows (two launches each) */
+} spmv_spgemm_info_t;
+
+spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32_t n, int32_t a_nnz,
+                                 const int32_t *a_row_ptr, const int32_t *a_col_idx, int32_t b_nnz,
+                                 const int32_t *b_row_ptr, const int32_t *b_col_idx, spmv_dtype_t dtype,
+                                 int64_t *c_nnz, spmv_stream_t stream);
+
+spmv_status_t spmv_spgemm_compute(spmv_spgemm_t handle, const void *a_vals, const void *b_vals,
+                                  int32_t *c_row_ptr, int32_t *c_col_idx, void *c_vals, spmv_stream_t stream);
+
+/* Fill *info (HOST). */
+spmv_status_t spmv_spgemm_info(spmv_spgemm_t handle, spmv_spgemm_info_t *info);
+
+/* Kernel-side failure flags (HOST *flags; waits for the device).  Bit 1: a
+ * row of C outgrew the size the symbolic phase found (the patterns changed
+ * after creation); that row is incomplete. */
+spmv_status_t spmv_spgemm_device_status(spmv_spgemm_t handle, int32_t *flags);
+
+/* Free the handle's workspace (waits for the device).  NULL is a no-op. */
+spmv_status_t spmv_spgemm_destroy(spmv_spgemm_t handle);
+
 /* Static text for a status code. */
 const char *spmv_status_string(spmv_status_t status);
 

@@ -16,7 +16,7 @@ import os
 
 from . import _build
 
-__all__ = ["Plan", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
+__all__ = ["Plan", "SpGEMM", "spgemm", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
 
 KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4, "rgcsr_sorted": 5,
            "group_mapped": 6}
@@ -57,6 +57,14 @@ class PlanInfo(ctypes.Structure):
                 ("transposed_kernel", ctypes.c_int32), ("transposed_launches", ctypes.c_int32)]
 
 
+class SpgemmInfo(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("k", ctypes.c_int32), ("n", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("a_nnz", ctypes.c_int64), ("b_nnz", ctypes.c_int64), ("c_nnz", ctypes.c_int64),
+                ("products", ctypes.c_int64), ("bin_rows", ctypes.c_int64 * 8), ("dense_slots", ctypes.c_int32),
+                ("launches_per_compute", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+                ("dense_pieces", ctypes.c_int64), ("dense_waves", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -90,6 +98,12 @@ def lib() -> ctypes.CDLL:
             "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
             "spmv_execute_multi": [vp, i32, dbl, vp, ctypes.c_int64, dbl, vp, ctypes.c_int64, vp],
             "spmv_execute_transposed": [vp, dbl, vp, dbl, vp, vp],
+            "spmv_spgemm_create": [ctypes.POINTER(vp), i32, i32, i32, i32, vp, vp, i32, vp, vp, ctypes.c_int,
+                                   ctypes.POINTER(ctypes.c_int64), vp],
+            "spmv_spgemm_compute": [vp, vp, vp, vp, vp, vp, vp],
+            "spmv_spgemm_info": [vp, ctypes.POINTER(SpgemmInfo)],
+            "spmv_spgemm_device_status": [vp, ctypes.POINTER(i32)],
+            "spmv_spgemm_destroy": [vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -267,3 +281,93 @@ class Plan:
     def __exit__(self, *exc):
         self.close()
         return False
+
+
+class SpGEMM:
+    """C = A*B for CSR matrices on the GPU (A m-by-k, B k-by-n; CUDA int32
+    index tensors).  Creation runs the symbolic phase on the two patterns
+    (borrowed: kept referenced here, their contents must not change) and
+    fixes ``c_nnz``; ``compute`` runs the numeric phase for given values and
+    returns C as (row_ptr, col_idx, vals) CUDA tensors, or fills the ones
+    passed in."""
+
+    def __init__(self, a_row_ptr, a_col_idx, b_row_ptr, b_col_idx, n: int, dtype, *, stream=None):
+        import torch
+        for name, t in (("a_row_ptr", a_row_ptr), ("a_col_idx", a_col_idx), ("b_row_ptr", b_row_ptr),
+                        ("b_col_idx", b_col_idx)):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+        if dtype not in (torch.float32, torch.float64):
+            raise TypeError("dtype must be torch.float32 or torch.float64")
+        self.m, self.k, self.n = a_row_ptr.numel() - 1, b_row_ptr.numel() - 1, int(n)
+        self.a_nnz, self.b_nnz = a_col_idx.numel(), b_col_idx.numel()
+        self.dtype = dtype
+        self.device = a_row_ptr.device
+        self._keep = (a_row_ptr, a_col_idx, b_row_ptr, b_col_idx)
+        handle = ctypes.c_void_p()
+        c_nnz = ctypes.c_int64(0)
+        with torch.cuda.device(self.device):
+            check(lib().spmv_spgemm_create(ctypes.byref(handle), self.m, self.k, self.n, self.a_nnz,
+                                           _ptr(a_row_ptr), _ptr(a_col_idx), self.b_nnz, _ptr(b_row_ptr),
+                                           _ptr(b_col_idx), 1 if dtype == torch.float64 else 0,
+                                           ctypes.byref(c_nnz), _stream_handle(stream)), "spmv_spgemm_create")
+        self._h = handle
+        self.c_nnz = c_nnz.value
+
+    def compute(self, a_vals, b_vals, out=None, stream=None):
+        import torch
+        if self._h is None:
+            raise RuntimeError("SpGEMM handle is closed")
+        if a_vals.numel() != self.a_nnz or b_vals.numel() != self.b_nnz:
+            raise ValueError("a_vals and b_vals must match the patterns' nnz")
+        for t in (a_vals, b_vals):
+            if t.dtype != self.dtype or not t.is_cuda or not t.is_contiguous():
+                raise TypeError("values must be contiguous CUDA tensors of the handle's dtype")
+        if out is None:
+            out = (torch.empty(self.m + 1, dtype=torch.int32, device=self.device),
+                   torch.empty(self.c_nnz, dtype=torch.int32, device=self.device),
+                   torch.empty(self.c_nnz, dtype=self.dtype, device=self.device))
+        rp, col, val = out
+        if rp.numel() != self.m + 1 or col.numel() != self.c_nnz or val.numel() != self.c_nnz:
+            raise ValueError("output arrays must have m + 1, c_nnz and c_nnz entries")
+        if rp.dtype != torch.int32 or col.dtype != torch.int32 or val.dtype != self.dtype:
+            raise TypeError("outputs must be int32, int32 and the handle's dtype")
+        check(lib().spmv_spgemm_compute(self._h, _ptr(a_vals), _ptr(b_vals), rp.data_ptr(), _ptr(col), _ptr(val),
+                                        _stream_handle(stream)), "spmv_spgemm_compute")
+        return rp, col, val
+
+    def info(self) -> dict:
+        inf = SpgemmInfo()
+        check(lib().spmv_spgemm_info(self._h, ctypes.byref(inf)), "spmv_spgemm_info")
+        out = {f: getattr(inf, f) for f, _ in SpgemmInfo._fields_}
+        out["bin_rows"] = list(inf.bin_rows)[:7]
+        return out
+
+    def device_status(self) -> int:
+        flags = ctypes.c_int32(0)
+        check(lib().spmv_spgemm_device_status(self._h, ctypes.byref(flags)), "spmv_spgemm_device_status")
+        return flags.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            check(lib().spmv_spgemm_destroy(self._h), "spmv_spgemm_destroy")
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
+
+
+def spgemm(a_row_ptr, a_col_idx, a_vals, b_row_ptr, b_col_idx, b_vals, n: int, stream=None):
+    """C = A*B in one call: (row_ptr, col_idx, vals) CUDA tensors."""
+    with SpGEMM(a_row_ptr, a_col_idx, b_row_ptr, b_col_idx, n, a_vals.dtype, stream=stream) as h:
+        return h.compute(a_vals, b_vals, stream=stream)

@@ -7,11 +7,13 @@
 // with one cudaMalloc, since allocation is far slower than use), plus a
 // second allocation only for kernels that keep a reordered copy of A.
 // spmv_execute allocates and frees nothing and never waits for the device.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "internal.cuh"
 
@@ -77,6 +79,24 @@ struct spmv_plan_s {
     void *rg_val = nullptr;          // [rg_slots]
 
     spmv_row_stats_t stats{};
+};
+
+// SpGEMM handle: the borrowed patterns, the binning and the symbolic
+// result, and the dense-bin scratch.
+struct spmv_spgemm_s {
+    int32_t m = 0, k = 0, n = 0, a_nnz = 0, b_nnz = 0;
+    spmv_dtype_t dtype = SPMV_F32;
+    int64_t c_nnz = 0, products = 0;
+    void *arena = nullptr;
+    size_t arena_bytes = 0;
+    void *dense = nullptr;     // the slots of a wave of dense rows
+    size_t dense_bytes = 0;
+    void *layout = nullptr;    // dense bin: entry space, pieces, segments
+    void *pieces = nullptr;    // the pieces when they outgrow their place in `layout`
+    size_t layout_bytes = 0;
+    int64_t dense_pieces = 0;
+    std::vector<int64_t> wave_row, wave_piece;  // HOST, [waves + 1]
+    SpgemmArgs args{};
 };
 
 namespace {
@@ -790,6 +810,383 @@ spmv_status_t spmv_plan_export(spmv_plan_t p, spmv_export_t what, void *dst, siz
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess && size) e = cudaMemcpy(dst, src, size, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_export");
+    return SPMV_OK;
+}
+
+// ---------------------------------------------------------------- SpGEMM
+
+static void destroy_spgemm(spmv_spgemm_s *h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    if (h->arena) cudaFree(h->arena);
+    if (h->dense) cudaFree(h->dense);
+    if (h->layout) cudaFree(h->layout);
+    if (h->pieces) cudaFree(h->pieces);
+    delete h;
+}
+
+// The dense bin's layout (see spgemm.cu): entry offsets of the dense rows,
+// products before each entry, pieces and their first entries, waves, and
+// the slots of one wave.  Synchronises the stream.
+static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
+    SpgemmArgs &a = h->args;
+    const int64_t D = a.bin_count[kSpgemmBins - 1];
+    int64_t before = 0;
+    for (int b = 0; b < kSpgemmBins - 1; ++b) before += a.bin_count[b];
+    const int32_t *drows = a.bin_rows + before;
+    const size_t vs = value_size(h->dtype);
+
+    // entries of A of the dense rows: e_off, then their products: pp
+    int64_t *tmp = nullptr;
+    const int64_t scan_d = scan_scratch_elems(D);
+    cudaError_t e = cudaMalloc(&tmp, sizeof(int64_t) * (size_t)(2 * (D + 1) + scan_d));
+    if (e != cudaSuccess) return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM dense layout: ") + cudaGetErrorString(e));
+    int64_t *alen = tmp, *e_off_tmp = tmp + (D + 1), *scan_tmp = tmp + 2 * (D + 1);
+    int64_t entries = 0;
+    e = launch_spgemm_dense_layout(a, drows, D, alen, e_off_tmp, scan_tmp, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&entries, e_off_tmp + D, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        cudaFree(tmp);
+        return cuda_fail(e, "SpGEMM dense layout");
+    }
+    // pieces: each dense row's products cut evenly into ceil(products / piece) parts.
+    // The layout arena is sized for the most pieces the rows can need (known after
+    // rowp), so rowp is computed in a first arena and the pieces in a second.
+    const int64_t scan_e = scan_scratch_elems(std::max<int64_t>(entries, 1));
+    size_t off = 0;
+    const size_t o_eoff = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)(D + 1), 256);
+    const size_t o_pp = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)(entries + 1), 256);
+    const size_t o_rowp = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)(D + 1), 256);
+    const size_t o_blen = off;  // scratch: B lengths, then the pieces
+    off = align_up(off + sizeof(int64_t) * (size_t)std::max<int64_t>(entries, 1), 256);
+    const size_t o_scan = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)scan_e, 256);
+    const int64_t segs = spgemm_segments(h->n), nseg = D * segs;
+    const size_t o_segcnt = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)nseg, 256);
+    const size_t o_segoff = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)(nseg + 1), 256);
+    const size_t o_segscan = off;
+    off = align_up(off + sizeof(int64_t) * (size_t)scan_scratch_elems(nseg), 256);
+    const size_t first_bytes = off;
+    void *first = nullptr;
+    e = cudaMalloc(&first, first_bytes);
+    if (e != cudaSuccess) {
+        cudaFree(tmp);
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM dense layout: ") + cudaGetErrorString(e));
+    }
+    char *fb = static_cast<char *>(first);
+    int64_t *e_off = reinterpret_cast<int64_t *>(fb + o_eoff);
+    int64_t *pp = reinterpret_cast<int64_t *>(fb + o_pp);
+    int64_t *rowp = reinterpret_cast<int64_t *>(fb + o_rowp);
+    std::vector<int64_t> h_rowp((size_t)D + 1);
+    e = cudaMemcpyAsync(e_off, e_off_tmp, sizeof(int64_t) * (size_t)(D + 1), cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess)
+        e = launch_spgemm_dense_products(a, drows, D, e_off, entries, reinterpret_cast<int64_t *>(fb + o_blen), pp,
+                                         rowp, reinterpret_cast<int64_t *>(fb + o_scan), stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h_rowp.data(), rowp, sizeof(int64_t) * (size_t)(D + 1), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    cudaFree(tmp);
+    h->layout = first;
+    h->layout_bytes = first_bytes;
+    if (e != cudaSuccess) return cuda_fail(e, "SpGEMM dense products");
+
+    // pieces (HOST), then their first entries (device)
+    const int64_t piece = spgemm_piece_products();
+    std::vector<int32_t> piece_row;
+    std::vector<int64_t> piece_k0, row_piece((size_t)D + 1);
+    for (int64_t j = 0; j < D; ++j) {
+        row_piece[(size_t)j] = (int64_t)piece_row.size();
+        const int64_t k0 = h_rowp[(size_t)j], len = h_rowp[(size_t)j + 1] - k0;
+        const int64_t np = std::max<int64_t>(1, (len + piece - 1) / piece);
+        for (int64_t c = 0; c < np; ++c) {
+            piece_row.push_back((int32_t)j);
+            piece_k0.push_back(k0 + len * c / np);
+        }
+    }
+    row_piece[(size_t)D] = (int64_t)piece_row.size();
+    piece_k0.push_back(h_rowp[(size_t)D]);
+    const int64_t P = (int64_t)piece_row.size();
+    h->dense_pieces = P;
+    // the pieces live in the blen + scan scratch of the first arena when they fit
+    const size_t need = align_up(sizeof(int64_t) * (size_t)(P + 1), 256) + align_up(sizeof(int64_t) * (size_t)P, 256) +
+                        align_up(sizeof(int32_t) * (size_t)P, 256);
+    if (need > o_segcnt - o_blen) {
+        // a separate allocation for the pieces
+        void *more = nullptr;
+        e = cudaMalloc(&more, need);
+        if (e != cudaSuccess) return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM pieces: ") + cudaGetErrorString(e));
+        h->pieces = more;
+        h->layout_bytes += need;
+    }
+    char *pb = h->pieces ? static_cast<char *>(h->pieces) : fb + o_blen;
+    int64_t *d_k0 = reinterpret_cast<int64_t *>(pb);
+    int64_t *d_pe = reinterpret_cast<int64_t *>(pb + align_up(sizeof(int64_t) * (size_t)(P + 1), 256));
+    int32_t *d_prow = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(d_pe) + align_up(sizeof(int64_t) * (size_t)P, 256));
+    e = cudaMemcpyAsync(d_k0, piece_k0.data(), sizeof(int64_t) * (size_t)(P + 1), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_prow, piece_row.data(), sizeof(int32_t) * (size_t)P, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = launch_spgemm_dense_locate(P, d_k0, pp, entries, d_pe, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "SpGEMM pieces");
+    a.dense_e_off = e_off;
+    a.dense_pp = pp;
+    a.dense_piece_k0 = d_k0;
+    a.dense_piece_e = d_pe;
+    a.dense_piece_row = d_prow;
+    a.dense_segs = segs;
+    a.dense_seg_cnt = reinterpret_cast<int64_t *>(fb + o_segcnt);
+    a.dense_seg_off = reinterpret_cast<int64_t *>(fb + o_segoff);
+    a.dense_seg_scan = reinterpret_cast<int64_t *>(fb + o_segscan);
+    e = cudaMemsetAsync(a.dense_seg_cnt, 0, sizeof(int64_t) * (size_t)nseg, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "SpGEMM segments");
+
+    // slots and waves
+    const int32_t n = h->n;
+    const size_t words = ((size_t)n + 31) / 32, swords = (words + 31) / 32;
+    const size_t per_slot = (size_t)n * vs + (words + swords) * sizeof(unsigned);
+    int64_t S = std::min<int64_t>(D, 1024);
+    S = std::max<int64_t>(1, std::min<int64_t>(S, (int64_t)((size_t(8) << 30) / std::max<size_t>(per_slot, 1))));
+    const size_t vals_bytes = align_up((size_t)n * vs * (size_t)S, 256);
+    const size_t bits_bytes = align_up(words * sizeof(unsigned) * (size_t)S, 256);
+    h->dense_bytes = vals_bytes + bits_bytes + align_up(swords * sizeof(unsigned) * (size_t)S, 256);
+    e = cudaMalloc(&h->dense, h->dense_bytes);
+    if (e != cudaSuccess) {
+        h->dense = nullptr;
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM dense rows: ") + cudaGetErrorString(e));
+    }
+    e = cudaMemsetAsync(h->dense, 0, h->dense_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "SpGEMM dense rows");
+    a.dense_slots = S;
+    a.dense_vals = h->dense;
+    a.dense_bits = reinterpret_cast<unsigned *>(static_cast<char *>(h->dense) + vals_bytes);
+    a.dense_summary = reinterpret_cast<unsigned *>(static_cast<char *>(h->dense) + vals_bytes + bits_bytes);
+    h->wave_row.clear();
+    h->wave_piece.clear();
+    for (int64_t j = 0; j < D; j += S) {
+        h->wave_row.push_back(j);
+        h->wave_piece.push_back(row_piece[(size_t)j]);
+    }
+    h->wave_row.push_back(D);
+    h->wave_piece.push_back(P);
+    a.dense_waves = (int64_t)h->wave_row.size() - 1;
+    a.h_wave_row = h->wave_row.data();
+    a.h_wave_piece = h->wave_piece.data();
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32_t n, int32_t a_nnz,
+                                 const int32_t *a_row_ptr, const int32_t *a_col_idx, int32_t b_nnz,
+                                 const int32_t *b_row_ptr, const int32_t *b_col_idx, spmv_dtype_t dtype,
+                                 int64_t *c_nnz, spmv_stream_t stream_handle) {
+    if (!out) return fail(SPMV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!c_nnz) return fail(SPMV_ERR_INVALID_ARG, "c_nnz is NULL");
+    if (m < 0 || k < 0 || n < 0 || a_nnz < 0 || b_nnz < 0) return fail(SPMV_ERR_INVALID_ARG, "negative size");
+    if ((int64_t)m + a_nnz >= (1LL << 31) || (int64_t)k + b_nnz >= (1LL << 31))
+        return fail(SPMV_ERR_INVALID_ARG, "m + a_nnz and k + b_nnz must be < 2^31");
+    if (dtype != SPMV_F32 && dtype != SPMV_F64) return fail(SPMV_ERR_INVALID_ARG, "unknown dtype");
+    if (!a_row_ptr || !b_row_ptr) return fail(SPMV_ERR_INVALID_ARG, "a_row_ptr or b_row_ptr is NULL");
+    if ((a_nnz > 0 && !a_col_idx) || (b_nnz > 0 && !b_col_idx))
+        return fail(SPMV_ERR_INVALID_ARG, "a_col_idx or b_col_idx is NULL");
+    int dev = 0, major = 0, minor = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return fail(SPMV_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300) only");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+
+    spmv_spgemm_s *h = new (std::nothrow) spmv_spgemm_s();
+    if (!h) return fail(SPMV_ERR_ALLOC, "host allocation failed");
+    h->m = m;
+    h->k = k;
+    h->n = n;
+    h->a_nnz = a_nnz;
+    h->b_nnz = b_nnz;
+    h->dtype = dtype;
+
+    // ---- one arena: checks of A and B, row products, bins, row sizes of C
+    const int ctas_a = stats_num_ctas(m, a_nnz), ctas_b = stats_num_ctas(k, b_nnz);
+    const int64_t chunks = spgemm_chunks(m);
+    const int64_t scan_elems = std::max(scan_scratch_elems(kSpgemmBins * chunks), scan_scratch_elems(std::max<int64_t>(m, 1)));
+    const size_t M = (size_t)std::max<int32_t>(m, 1);
+    size_t off = 0;
+    const size_t off_pa = off;
+    off = align_up(off + sizeof(StatsPartial) * ctas_a, 256);
+    const size_t off_pb = off;
+    off = align_up(off + sizeof(StatsPartial) * ctas_b, 256);
+    const size_t off_stats = off;
+    off = align_up(off + 2 * sizeof(spmv_row_stats_t), 256);
+    const size_t off_products = off;
+    off = align_up(off + sizeof(int64_t) * M, 256);
+    const size_t off_rows = off;
+    off = align_up(off + sizeof(int32_t) * M, 256);
+    const size_t off_nnz = off;
+    off = align_up(off + sizeof(int64_t) * (M + 1), 256);
+    const size_t off_cptr = off;
+    off = align_up(off + sizeof(int64_t) * (M + 1), 256);
+    const size_t off_counts = off;
+    off = align_up(off + sizeof(int64_t) * kSpgemmBins * chunks, 256);
+    const size_t off_offsets = off;
+    off = align_up(off + sizeof(int64_t) * (kSpgemmBins * chunks + 1), 256);
+    const size_t off_scan = off;
+    off = align_up(off + sizeof(int64_t) * scan_elems, 256);
+    const size_t off_err = off;
+    off = align_up(off + sizeof(int32_t), 256);
+    h->arena_bytes = off;
+    e = cudaMalloc(&h->arena, h->arena_bytes);
+    if (e != cudaSuccess) {
+        h->arena = nullptr;
+        destroy_spgemm(h);
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM workspace: ") + cudaGetErrorString(e));
+    }
+    char *base = static_cast<char *>(h->arena);
+    spmv_row_stats_t *d_stats = reinterpret_cast<spmv_row_stats_t *>(base + off_stats);
+    SpgemmArgs &a = h->args;
+    a.m = m;
+    a.n = n;
+    a.a_ptr = a_row_ptr;
+    a.a_col = a_col_idx;
+    a.b_ptr = b_row_ptr;
+    a.b_col = b_col_idx;
+    a.products = reinterpret_cast<int64_t *>(base + off_products);
+    a.bin_rows = reinterpret_cast<int32_t *>(base + off_rows);
+    a.row_nnz = reinterpret_cast<int64_t *>(base + off_nnz);
+    a.c_ptr = reinterpret_cast<int64_t *>(base + off_cptr);
+    a.error = reinterpret_cast<int32_t *>(base + off_err);
+    int64_t *counts = reinterpret_cast<int64_t *>(base + off_counts);
+    int64_t *offsets = reinterpret_cast<int64_t *>(base + off_offsets);
+    int64_t *scan = reinterpret_cast<int64_t *>(base + off_scan);
+
+    // ---- checks of both patterns, read back once
+    spmv_row_stats_t st[2];
+    e = cudaMemsetAsync(base, 0, h->arena_bytes, stream);
+    if (e == cudaSuccess)
+        e = launch_row_stats(m, k, a_nnz, a_row_ptr, a_col_idx, reinterpret_cast<StatsPartial *>(base + off_pa),
+                             ctas_a, d_stats, stream);
+    if (e == cudaSuccess)
+        e = launch_row_stats(k, n, b_nnz, b_row_ptr, b_col_idx, reinterpret_cast<StatsPartial *>(base + off_pb),
+                             ctas_b, d_stats + 1, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(st, d_stats, sizeof st, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        destroy_spgemm(h);
+        return cuda_fail(e, "SpGEMM analysis");
+    }
+    for (int w = 0; w < 2; ++w)
+        if (st[w].flags) {
+            const int f = st[w].flags;
+            destroy_spgemm(h);
+            char msg[160];
+            std::snprintf(msg, sizeof msg, "invalid CSR (%s):%s%s%s%s", w ? "B" : "A", (f & 1) ? " row_ptr[0] != 0;" : "",
+                          (f & 2) ? " row_ptr decreases;" : "", (f & 4) ? " row_ptr[m] != nnz;" : "",
+                          (f & 8) ? " column index outside its range;" : "");
+            return fail(SPMV_ERR_INVALID_CSR, msg);
+        }
+
+    // ---- products per row and bins
+    e = launch_spgemm_analysis(a, counts, offsets, scan, stream);
+    int64_t host_off[kSpgemmBins + 1] = {};
+    if (e == cudaSuccess && m > 0)
+        for (int b = 0; b <= kSpgemmBins && e == cudaSuccess; ++b)
+            e = cudaMemcpyAsync(host_off + b, offsets + b * chunks, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        destroy_spgemm(h);
+        return cuda_fail(e, "SpGEMM binning");
+    }
+    for (int b = 0; b < kSpgemmBins; ++b) a.bin_count[b] = host_off[b + 1] - host_off[b];
+
+    // ---- the dense bin: entry space, pieces of at most spgemm_piece_products()
+    //      products, waves of rows that fit the slots (at most 8 GiB of them)
+    const int64_t dense_rows = a.bin_count[kSpgemmBins - 1];
+    if (dense_rows > 0) {
+        const spmv_status_t st = spgemm_dense_plan(h, stream);
+        if (st != SPMV_OK) {
+            destroy_spgemm(h);
+            return st;
+        }
+    }
+
+    // ---- symbolic phase: the size of every row of C
+    e = launch_spgemm_symbolic(dtype, a, scan, stream);
+    int64_t tot[2] = {0, 0};
+    if (e == cudaSuccess && m > 0) e = cudaMemcpyAsync(tot, a.c_ptr + m, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess && m > 0) {
+        // the total of the products (for the info), summed into row_nnz,
+        // which the numeric phase does not use
+        e = launch_exclusive_scan(a.products, m, a.row_nnz, scan, stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(tot + 1, a.row_nnz + m, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        destroy_spgemm(h);
+        return cuda_fail(e, "SpGEMM symbolic phase");
+    }
+    h->c_nnz = tot[0];
+    h->products = tot[1];
+    *c_nnz = h->c_nnz;
+    if (h->c_nnz >= (1LL << 31)) {
+        destroy_spgemm(h);
+        return fail(SPMV_ERR_INVALID_ARG, "C has 2^31 entries or more (int32 indices)");
+    }
+    *out = h;
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_spgemm_compute(spmv_spgemm_t h, const void *a_vals, const void *b_vals, int32_t *c_row_ptr,
+                                  int32_t *c_col_idx, void *c_vals, spmv_stream_t stream_handle) {
+    if (!h) return fail(SPMV_ERR_INVALID_ARG, "handle is NULL");
+    if (!c_row_ptr) return fail(SPMV_ERR_INVALID_ARG, "c_row_ptr is NULL");
+    if ((h->a_nnz > 0 && !a_vals) || (h->b_nnz > 0 && !b_vals)) return fail(SPMV_ERR_INVALID_ARG, "a_vals or b_vals is NULL");
+    if (h->c_nnz > 0 && (!c_col_idx || !c_vals)) return fail(SPMV_ERR_INVALID_ARG, "c_col_idx or c_vals is NULL");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    const cudaError_t e = launch_spgemm_numeric(h->dtype, h->args, a_vals, b_vals, c_row_ptr, c_col_idx, c_vals, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_spgemm_compute launch");
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_spgemm_info(spmv_spgemm_t h, spmv_spgemm_info_t *info) {
+    if (!h || !info) return fail(SPMV_ERR_INVALID_ARG, "handle or info is NULL");
+    std::memset(info, 0, sizeof *info);
+    info->m = h->m;
+    info->k = h->k;
+    info->n = h->n;
+    info->dtype = h->dtype;
+    info->a_nnz = h->a_nnz;
+    info->b_nnz = h->b_nnz;
+    info->c_nnz = h->c_nnz;
+    info->products = h->products;
+    int launches = h->m > 0 ? 1 : 0;  // the int32 row pointers (m == 0: a memset)
+    for (int b = 0; b < kSpgemmBins; ++b) {
+        info->bin_rows[b] = h->args.bin_count[b];
+        if (b < kSpgemmBins - 1) launches += h->args.bin_count[b] > 0;
+    }
+    launches += 2 * (int)h->args.dense_waves;  // accumulate + finish per wave
+    info->dense_slots = (int32_t)h->args.dense_slots;
+    info->dense_pieces = h->dense_pieces;
+    info->dense_waves = h->args.dense_waves;
+    info->launches_per_compute = launches;
+    info->workspace_bytes = (int64_t)(h->arena_bytes + h->dense_bytes + h->layout_bytes);
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_spgemm_device_status(spmv_spgemm_t h, int32_t *flags) {
+    if (!h || !flags) return fail(SPMV_ERR_INVALID_ARG, "handle or flags is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(flags, h->args.error, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_spgemm_device_status");
+    return SPMV_OK;
+}
+
+spmv_status_t spmv_spgemm_destroy(spmv_spgemm_t h) {
+    destroy_spgemm(h);
     return SPMV_OK;
 }
 
