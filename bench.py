@@ -523,7 +523,8 @@ def run_spgemm(args, workload_name: str) -> dict | None:
         "warmup": args.warmup, "median_us": round(med, 1), "higher_is_better": True, "dtype": A.dtype,
         "data": "synthetic",
         "config": {"workload": workload_name, "products": products, "c_nnz": info["c_nnz"],
-                   "bin_rows": info["bin_rows"], "dense_slots": info["dense_slots"],
+                   "bin_rows": info["bin_rows"], "numeric_bin_rows": info["numeric_bin_rows"],
+                   "dense_slots": info["dense_slots"],
                    "dense_pieces": info["dense_pieces"], "dense_waves": info["dense_waves"],
                    "launches_per_compute": info["launches_per_compute"],
                    "symbolic_ms_median": round(float(np.median(sym)), 2), "device_status": status},

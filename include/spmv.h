@@ -336,6 +336,9 @@ typedef struct {
     int64_t workspace_bytes;     /* device memory the handle owns */
     int64_t dense_pieces;        /* dense-bin pieces of at most 32768 products, a CTA each */
     int64_t dense_waves;         /* waves of dense-bin rows (two launches each) */
+    int64_t numeric_bin_rows[8]; /* the numeric phase's bins: rows of at most 16 products,
+                                    then by entries of C (<= 128, <= 512, <= 1024, <= 2048,
+                                    <= 4096; tables of twice that), the dense bin as above */
 } spmv_spgemm_info_t;
 
 spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32_t n, int32_t a_nnz,

@@ -62,7 +62,8 @@ class SpgemmInfo(ctypes.Structure):
                 ("a_nnz", ctypes.c_int64), ("b_nnz", ctypes.c_int64), ("c_nnz", ctypes.c_int64),
                 ("products", ctypes.c_int64), ("bin_rows", ctypes.c_int64 * 8), ("dense_slots", ctypes.c_int32),
                 ("launches_per_compute", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
-                ("dense_pieces", ctypes.c_int64), ("dense_waves", ctypes.c_int64)]
+                ("dense_pieces", ctypes.c_int64), ("dense_waves", ctypes.c_int64),
+                ("numeric_bin_rows", ctypes.c_int64 * 8)]
 
 
 _lib = None
@@ -341,6 +342,7 @@ class SpGEMM:
         check(lib().spmv_spgemm_info(self._h, ctypes.byref(inf)), "spmv_spgemm_info")
         out = {f: getattr(inf, f) for f, _ in SpgemmInfo._fields_}
         out["bin_rows"] = list(inf.bin_rows)[:7]
+        out["numeric_bin_rows"] = list(inf.numeric_bin_rows)[:7]
         return out
 
     def device_status(self) -> int:

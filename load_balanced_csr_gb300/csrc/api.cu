@@ -15,7 +15,7 @@
 #include <string>
 #include <vector>
 
-#include "internal.cuh"
+#include "spgemm.cuh"
 
 using namespace lbcsr;
 
@@ -948,13 +948,12 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
 
     // slots and waves
     const int32_t n = h->n;
-    const size_t words = ((size_t)n + 31) / 32, swords = (words + 31) / 32;
-    const size_t per_slot = (size_t)n * vs + (words + swords) * sizeof(unsigned);
+    const size_t words = (size_t)spgemm_bit_words(n);
+    const size_t per_slot = (size_t)n * vs + words * sizeof(unsigned);
     int64_t S = std::min<int64_t>(D, 1024);
     S = std::max<int64_t>(1, std::min<int64_t>(S, (int64_t)((size_t(8) << 30) / std::max<size_t>(per_slot, 1))));
     const size_t vals_bytes = align_up((size_t)n * vs * (size_t)S, 256);
-    const size_t bits_bytes = align_up(words * sizeof(unsigned) * (size_t)S, 256);
-    h->dense_bytes = vals_bytes + bits_bytes + align_up(swords * sizeof(unsigned) * (size_t)S, 256);
+    h->dense_bytes = vals_bytes + align_up(words * sizeof(unsigned) * (size_t)S, 256);
     e = cudaMalloc(&h->dense, h->dense_bytes);
     if (e != cudaSuccess) {
         h->dense = nullptr;
@@ -965,7 +964,6 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     a.dense_slots = S;
     a.dense_vals = h->dense;
     a.dense_bits = reinterpret_cast<unsigned *>(static_cast<char *>(h->dense) + vals_bytes);
-    a.dense_summary = reinterpret_cast<unsigned *>(static_cast<char *>(h->dense) + vals_bytes + bits_bytes);
     h->wave_row.clear();
     h->wave_piece.clear();
     for (int64_t j = 0; j < D; j += S) {
@@ -1027,6 +1025,8 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
     off = align_up(off + sizeof(int64_t) * M, 256);
     const size_t off_rows = off;
     off = align_up(off + sizeof(int32_t) * M, 256);
+    const size_t off_num_rows = off;
+    off = align_up(off + sizeof(int32_t) * M, 256);
     const size_t off_nnz = off;
     off = align_up(off + sizeof(int64_t) * (M + 1), 256);
     const size_t off_cptr = off;
@@ -1057,6 +1057,8 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
     a.b_col = b_col_idx;
     a.products = reinterpret_cast<int64_t *>(base + off_products);
     a.bin_rows = reinterpret_cast<int32_t *>(base + off_rows);
+    int32_t *num_rows = reinterpret_cast<int32_t *>(base + off_num_rows);
+    a.num_bin_rows = num_rows;
     a.row_nnz = reinterpret_cast<int64_t *>(base + off_nnz);
     a.c_ptr = reinterpret_cast<int64_t *>(base + off_cptr);
     a.error = reinterpret_cast<int32_t *>(base + off_err);
@@ -1124,11 +1126,19 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
         e = launch_exclusive_scan(a.products, m, a.row_nnz, scan, stream);
         if (e == cudaSuccess) e = cudaMemcpyAsync(tot + 1, a.row_nnz + m, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     }
+    // ---- the numeric phase's bins, by the entries of each row of C (row_nnz as the key)
+    int64_t num_off[kSpgemmBins + 1] = {};
+    if (e == cudaSuccess && m > 0) {
+        e = launch_spgemm_numeric_bins(a, a.row_nnz, counts, offsets, scan, num_rows, stream);
+        for (int b = 0; b <= kSpgemmBins && e == cudaSuccess; ++b)
+            e = cudaMemcpyAsync(num_off + b, offsets + b * chunks, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
         destroy_spgemm(h);
         return cuda_fail(e, "SpGEMM symbolic phase");
     }
+    for (int b = 0; b < kSpgemmBins; ++b) a.num_bin_count[b] = num_off[b + 1] - num_off[b];
     h->c_nnz = tot[0];
     h->products = tot[1];
     *c_nnz = h->c_nnz;
@@ -1166,7 +1176,8 @@ spmv_status_t spmv_spgemm_info(spmv_spgemm_t h, spmv_spgemm_info_t *info) {
     int launches = h->m > 0 ? 1 : 0;  // the int32 row pointers (m == 0: a memset)
     for (int b = 0; b < kSpgemmBins; ++b) {
         info->bin_rows[b] = h->args.bin_count[b];
-        if (b < kSpgemmBins - 1) launches += h->args.bin_count[b] > 0;
+        info->numeric_bin_rows[b] = h->args.num_bin_count[b];
+        if (b < kSpgemmBins - 1) launches += h->args.num_bin_count[b] > 0;
     }
     launches += 2 * (int)h->args.dense_waves;  // accumulate + finish per wave
     info->dense_slots = (int32_t)h->args.dense_slots;

@@ -11,9 +11,11 @@
 // columns in a sorted list in shared memory (no hashing, no sort, products
 // added in order); <= 128 and <= 512 -- a warp per row with a hash table of
 // 256 or 1024 slots; <= 1024, <= 2048, <= 4096 -- 128 or 256 threads per row
-// with 2048, 4096 or 8192 slots; more -- a CTA per row with a dense row of C
-// in global memory, a bit per column and a summary bit per 32 of those.
-// Tables use linear probing and stay at most half full; the thread that
+// with 2048, 4096 or 8192 slots; more -- a dense row of C in global memory
+// (values and a bit per column), each row's products cut into equal pieces
+// of at most 32768, a CTA per piece.
+// Tables use multiplicative hashing and linear probing and stay at most
+// half full; the thread that
 // claims a slot appends it to a list, so that after a row only the claimed
 // slots are read (sorted by column with a bitonic network) and cleared.
 // Values in hash tables are added with atomics, so their summation order
@@ -21,7 +23,7 @@
 // does not.
 #include <climits>
 
-#include "internal.cuh"
+#include "spgemm.cuh"
 
 namespace lbcsr {
 
@@ -266,6 +268,8 @@ sg_hash_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__restrict__ b_v
                int64_t nrows, int64_t *__restrict__ row_nnz, const int64_t *__restrict__ c_ptr,
                int32_t *__restrict__ c_col, V *__restrict__ c_val, int32_t *error) {
     constexpr int HALF = TS / 2;
+    constexpr int kLog2TS = TS == 256 ? 8 : TS == 1024 ? 10 : TS == 2048 ? 11 : TS == 4096 ? 12 : 13;
+    static_assert(1 << kLog2TS == TS, "table sizes are 256, 1024, 2048, 4096 or 8192");
     extern __shared__ __align__(16) unsigned char sg_smem[];
     __shared__ int s_count[GROUPS];
     const int t = threadIdx.x % G;
@@ -290,7 +294,9 @@ sg_hash_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__restrict__ b_v
         const int i = live ? rows[w] : 0;
         if (live) {
             auto insert = [&](int c, V v) {
-                unsigned h = ((unsigned)c * 2654435761u) & (TS - 1);
+                // multiplicative (Fibonacci) hashing: the top bits of the product mix
+                // every bit of the column; low bits would depend on its low bits only
+                unsigned h = ((unsigned)c * 2654435761u) >> (32 - kLog2TS);
                 for (int probe = 0; probe < TS; ++probe) {
                     const int old = atomicCAS(keys + h, -1, c);
                     if (old == -1) {
@@ -348,14 +354,14 @@ sg_hash_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__restrict__ b_v
 // of the entries before e (an exclusive prefix sum of the lengths of the
 // rows of B they pick).  Each dense row's products are cut into pieces of
 // at most kSgPiece, a CTA per piece; the rows of a wave share nothing, each
-// has a slot: a dense row of C in global memory (values, a bit per column,
-// a summary bit per 32 of those bits), into which the pieces add with
-// reductions (no value returned, nothing waited for).  A second kernel then
-// reads each row of the wave back in column order through the summary
-// bits -- the symbolic phase counts it, the numeric phase writes it -- and
-// clears what was used.
+// has a slot: a dense row of C in global memory (values and a bit per
+// column), into which the pieces add with reductions (no value returned,
+// nothing waited for).  A second kernel then reads each row of the wave
+// back in column order -- the symbolic phase counts it, the numeric phase
+// writes it -- and clears what was used.
 constexpr int64_t kSgPiece = 32768;
-constexpr int64_t kSgSegCols = 32768;  // columns per segment when reading rows back (256 threads x 128)
+constexpr int kSgWordsPerThread = 16;                        // words of bits per thread when reading rows back
+constexpr int64_t kSgSegCols = 256 * kSgWordsPerThread * 32;  // columns per segment (131072)
 
 // alen[j] = length of dense row j of A
 __global__ void __launch_bounds__(256)
@@ -409,7 +415,8 @@ struct SgDense {
     const int64_t *e_off, *pp, *piece_k0, *piece_e;
     const int32_t *piece_row;
     int32_t n;
-    unsigned *bits, *summary;
+    int64_t words;         // words of bits per row, a multiple of kSgWordsPerThread
+    unsigned *bits;
     void *vals;
     int64_t segs;          // segments per row
     int64_t *seg_cnt;      // [dense rows * segs]  columns per segment (symbolic)
@@ -432,16 +439,14 @@ sg_dense_accumulate_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__re
     const int64_t c = c_begin + blockIdx.x;
     const int64_t j = d.piece_row[c];
     const int64_t slot = j - j0;
-    const int64_t words = ((int64_t)d.n + 31) / 32, swords = (words + 31) / 32;
+    const int64_t words = d.words;
     unsigned *bits = d.bits + slot * words;
-    unsigned *summary = d.summary + slot * swords;
     V *dense = VALUES ? static_cast<V *>(d.vals) + slot * d.n : nullptr;
     const int64_t k0 = d.piece_k0[c], k1 = d.piece_k0[c + 1];
     const int64_t e_row = d.e_off[j], e_end = d.e_off[j + 1];
     const int32_t p_row = mat.a_ptr[d.drows[j]];
     auto add = [&](int col, V v) {
         atomicOr(bits + (col >> 5), 1u << (col & 31));
-        atomicOr(summary + (col >> 10), 1u << ((col >> 5) & 31));
         if (VALUES) atomicAdd(dense + col, v);
     };
     if (t == 0) s_qn = 0;
@@ -489,38 +494,44 @@ sg_dense_accumulate_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__re
 
 // Reading the rows of a wave back: a CTA per segment of kSgSegCols
 // columns of a row (d.segs segments per row; CTA b takes segment b % segs
-// of the wave's row b / segs), a thread per 128 columns (4 words of bits),
-// so that no thread has more than 128 entries to handle however full the
-// row is.  Symbolic: count the segment's columns into seg_cnt and add them
-// to row_nnz.  Numeric: write the columns and their values in order from
-// the segment's offset (seg_off, an exclusive prefix sum of the symbolic
-// counts over all segments).  Both clear the bits, summary bits and values
-// they read.
+// of the wave's row b / segs), a thread per kSgWordsPerThread consecutive
+// words of bits (read as 16-byte loads), so that no thread has more than
+// 32 * kSgWordsPerThread entries to handle however full the row is.
+// Symbolic: count the segment's columns into seg_cnt and add them to
+// row_nnz.  Numeric: write the columns and their values in order from the
+// segment's offset (seg_off, an exclusive prefix sum of the symbolic counts
+// over all segments).  Both clear the bits and values they read.
 template <typename V, bool VALUES>
 __global__ void __launch_bounds__(256)
 sg_dense_finish_kernel(SgDense d, int64_t j0, int64_t *__restrict__ row_nnz, const int64_t *__restrict__ c_ptr,
                        int32_t *__restrict__ c_col, V *__restrict__ c_val, int32_t *error) {
+    constexpr int WPT = kSgWordsPerThread;
     const int t = threadIdx.x;
     const int64_t slot = blockIdx.x / d.segs, seg = blockIdx.x % d.segs;
     const int64_t j = j0 + slot;
     const int i = d.drows[j];
-    const int64_t words = ((int64_t)d.n + 31) / 32, swords = (words + 31) / 32;
-    unsigned *bits = d.bits + slot * words;
-    unsigned *summary = d.summary + slot * swords;
+    unsigned *bits = d.bits + slot * d.words;
     V *dense = VALUES ? static_cast<V *>(d.vals) + slot * d.n : nullptr;
-    const int64_t sq = seg * (kSgSegCols / 1024) + t / 8;  // my summary word
-    const unsigned sw = sq < swords ? summary[sq] : 0u;
-    const unsigned mine = (sw >> ((t & 7) * 4)) & 0xFu;   // my 4 words of bits
-    const int64_t q0 = sq * 32 + (t & 7) * 4;
-    unsigned w4[4];
+    const int64_t q0 = seg * (kSgSegCols / 32) + (int64_t)t * WPT;  // my first word
+    unsigned w[WPT];
     int cnt = 0;
+    if (q0 + WPT <= d.words) {  // rows of bits are padded to a multiple of WPT words: 16-byte aligned
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        w4[u] = (mine >> u) & 1u ? bits[q0 + u] : 0u;
-        cnt += __popc(w4[u]);
+        for (int u = 0; u < WPT; u += 4) {
+            const uint4 v4 = *reinterpret_cast<const uint4 *>(bits + q0 + u);
+            w[u] = v4.x;
+            w[u + 1] = v4.y;
+            w[u + 2] = v4.z;
+            w[u + 3] = v4.w;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < WPT; ++u) w[u] = q0 + u < d.words ? bits[q0 + u] : 0u;
     }
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) cnt += __popc(w[u]);
     long long tot;
-    const long long before = sg_cta_scan(cnt, &tot);  // synchronises: every summary word is read
+    const long long before = sg_cta_scan(cnt, &tot);
     const int64_t g = j * d.segs + seg;
     if (!VALUES) {
         if (t == 0) {
@@ -532,8 +543,8 @@ sg_dense_finish_kernel(SgDense d, int64_t j0, int64_t *__restrict__ row_nnz, con
         const int64_t end = c_ptr[i + 1];
         int64_t o = base + before;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            for (unsigned b = w4[u]; b; b &= b - 1) {
+        for (int u = 0; u < WPT; ++u)
+            for (unsigned b = w[u]; b; b &= b - 1) {
                 const int64_t col = (q0 + u) * 32 + __ffs(b) - 1;
                 if (o < end) {
                     c_col[o] = (int32_t)col;
@@ -546,9 +557,8 @@ sg_dense_finish_kernel(SgDense d, int64_t j0, int64_t *__restrict__ row_nnz, con
             }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-        if ((mine >> u) & 1u) bits[q0 + u] = 0u;
-    if ((t & 7) == 0 && sw) summary[sq] = 0u;
+    for (int u = 0; u < WPT; ++u)
+        if (w[u]) bits[q0 + u] = 0u;
 }
 
 __global__ void __launch_bounds__(256)
@@ -584,26 +594,30 @@ cudaError_t sg_launch_hash(const SgCsr &mat, const void *a_val, const void *b_va
     return cudaGetLastError();
 }
 
+// One phase over the bins: the symbolic phase bins rows by products, the
+// numeric phase by the entries the symbolic phase found (the dense bin and
+// the list bin hold the same rows in both).
 template <typename V, bool VALUES>
 cudaError_t sg_phase(const SpgemmArgs &a, const void *a_val, const void *b_val, int32_t *c_col, void *c_val,
                      cudaStream_t stream) {
     const SgCsr mat{a.a_ptr, a.a_col, a.b_ptr, a.b_col};
+    const int64_t *count = VALUES ? a.num_bin_count : a.bin_count;
     const int32_t *r[kSgBins];
-    r[0] = a.bin_rows;
-    for (int b = 1; b < kSgBins; ++b) r[b] = r[b - 1] + a.bin_count[b - 1];
+    r[0] = VALUES ? a.num_bin_rows : a.bin_rows;
+    for (int b = 1; b < kSgBins; ++b) r[b] = r[b - 1] + count[b - 1];
     cudaError_t e = cudaSuccess;
-    if (a.bin_count[0] > 0) {
-        long long grid = (a.bin_count[0] + 255) / 256;
+    if (count[0] > 0) {
+        long long grid = (count[0] + 255) / 256;
         const long long cap = (long long)device_sm_count() * 4;
         if (grid > cap) grid = cap;
         sg_list_kernel<V, VALUES><<<(unsigned)grid, 256, 0, stream>>>(
-            mat, static_cast<const V *>(a_val), static_cast<const V *>(b_val), r[0], a.bin_count[0], a.row_nnz,
+            mat, static_cast<const V *>(a_val), static_cast<const V *>(b_val), r[0], count[0], a.row_nnz,
             a.c_ptr, c_col, static_cast<V *>(c_val), a.error);
         e = cudaGetLastError();
     }
 #define SG_HASH(BIN, TS, G, GROUPS)                                                                              \
     if (e == cudaSuccess)                                                                                        \
-        e = sg_launch_hash<V, TS, G, GROUPS, VALUES>(mat, a_val, b_val, r[BIN], a.bin_count[BIN], a.row_nnz,     \
+        e = sg_launch_hash<V, TS, G, GROUPS, VALUES>(mat, a_val, b_val, r[BIN], count[BIN], a.row_nnz,           \
                                                      a.c_ptr, c_col, c_val, a.error, stream);
     SG_HASH(1, 256, 32, 8)
     SG_HASH(2, 1024, 32, 4)
@@ -611,10 +625,10 @@ cudaError_t sg_phase(const SpgemmArgs &a, const void *a_val, const void *b_val, 
     SG_HASH(4, 4096, 256, 1)
     SG_HASH(5, 8192, 256, 1)
 #undef SG_HASH
-    const int64_t dense_rows = a.bin_count[kSgBins - 1];
+    const int64_t dense_rows = count[kSgBins - 1];
     if (e == cudaSuccess && dense_rows > 0) {
         const SgDense d{r[kSgBins - 1], a.dense_e_off, a.dense_pp, a.dense_piece_k0, a.dense_piece_e,
-                        a.dense_piece_row, a.n, a.dense_bits, a.dense_summary, a.dense_vals,
+                        a.dense_piece_row, a.n, spgemm_bit_words(a.n), a.dense_bits, a.dense_vals,
                         a.dense_segs, a.dense_seg_cnt, a.dense_seg_off};
         for (int64_t w = 0; w < a.dense_waves && e == cudaSuccess; ++w) {
             const int64_t j0 = a.h_wave_row[w], j1 = a.h_wave_row[w + 1];
@@ -644,6 +658,11 @@ int64_t spgemm_piece_products() { return kSgPiece; }
 
 int64_t spgemm_segments(int32_t n) { return ((int64_t)n + kSgSegCols - 1) / kSgSegCols; }
 
+int64_t spgemm_bit_words(int32_t n) {
+    const int64_t w = ((int64_t)n + 31) / 32;
+    return (w + kSgWordsPerThread - 1) / kSgWordsPerThread * kSgWordsPerThread;
+}
+
 cudaError_t launch_spgemm_dense_layout(const SpgemmArgs &a, const int32_t *drows, int64_t nrows, int64_t *alen,
                                        int64_t *e_off, int64_t *scan_scratch, cudaStream_t stream) {
     sg_dense_alen_kernel<<<sg_blocks(nrows), 256, 0, stream>>>(nrows, drows, a.a_ptr, alen);
@@ -672,22 +691,51 @@ cudaError_t launch_spgemm_dense_locate(int64_t pieces, const int64_t *piece_k0, 
     return cudaGetLastError();
 }
 
+// Two-pass binning of rows 0 .. m-1 by key (sg_bin): counts per chunk and
+// bin, one exclusive scan over [bin][chunk], then the rows of each bin in
+// increasing order.
+static cudaError_t sg_binning(int32_t m, const int64_t *key, int64_t *chunk_counts, int64_t *chunk_offsets,
+                              int64_t *scan_scratch, int32_t *rows, cudaStream_t stream) {
+    const int64_t chunks = spgemm_chunks(m);
+    sg_bin_count_kernel<<<(unsigned)chunks, 256, 0, stream>>>(m, key, chunks, chunk_counts);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = launch_exclusive_scan(chunk_counts, kSgBins * chunks, chunk_offsets, scan_scratch, stream);
+    if (e == cudaSuccess) {
+        sg_bin_scatter_kernel<<<(unsigned)chunks, 256, 0, stream>>>(m, key, chunks, chunk_offsets, rows);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
 cudaError_t launch_spgemm_analysis(const SpgemmArgs &a, int64_t *chunk_counts, int64_t *chunk_offsets,
                                    int64_t *scan_scratch, cudaStream_t stream) {
     if (a.m <= 0) return cudaSuccess;
     sg_products_kernel<<<sg_blocks((int64_t)a.m * 32), 256, 0, stream>>>(a.m, a.a_ptr, a.a_col, a.b_ptr, a.products);
     cudaError_t e = cudaGetLastError();
-    const int64_t chunks = spgemm_chunks(a.m);
-    if (e == cudaSuccess) {
-        sg_bin_count_kernel<<<(unsigned)chunks, 256, 0, stream>>>(a.m, a.products, chunks, chunk_counts);
-        e = cudaGetLastError();
-    }
-    // bins one after the other: one scan over [bin][chunk]
-    if (e == cudaSuccess) e = launch_exclusive_scan(chunk_counts, kSgBins * chunks, chunk_offsets, scan_scratch, stream);
-    if (e == cudaSuccess) {
-        sg_bin_scatter_kernel<<<(unsigned)chunks, 256, 0, stream>>>(a.m, a.products, chunks, chunk_offsets, a.bin_rows);
-        e = cudaGetLastError();
-    }
+    if (e == cudaSuccess) e = sg_binning(a.m, a.products, chunk_counts, chunk_offsets, scan_scratch, a.bin_rows, stream);
+    return e;
+}
+
+// key of the numeric binning: the products for the list and dense bins,
+// else the row's entries (at least 17, so that such rows stay out of the
+// list bin)
+__global__ void __launch_bounds__(256)
+sg_numeric_key_kernel(int32_t m, const int64_t *__restrict__ products, const int64_t *__restrict__ c_ptr,
+                      int64_t *__restrict__ key) {
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= m) return;
+    const int64_t p = products[i];
+    const int64_t nnz = c_ptr[i + 1] - c_ptr[i];
+    key[i] = (p <= 16 || p > 4096) ? p : (nnz < 17 ? 17 : nnz);
+}
+
+cudaError_t launch_spgemm_numeric_bins(const SpgemmArgs &a, int64_t *key, int64_t *chunk_counts,
+                                       int64_t *chunk_offsets, int64_t *scan_scratch, int32_t *num_bin_rows,
+                                       cudaStream_t stream) {
+    if (a.m <= 0) return cudaSuccess;
+    sg_numeric_key_kernel<<<sg_blocks(a.m), 256, 0, stream>>>(a.m, a.products, a.c_ptr, key);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = sg_binning(a.m, key, chunk_counts, chunk_offsets, scan_scratch, num_bin_rows, stream);
     return e;
 }
 

@@ -134,7 +134,9 @@ def test_spgemm_every_bin(dtype):
     A, B = mixed_pair(dtype, 7)
     info = check_all(A, B, f"spgemm bins {dtype}")
     assert all(c > 0 for c in info["bin_rows"]), info["bin_rows"]
-    assert sum(info["bin_rows"]) == A.m
+    assert sum(info["bin_rows"]) == A.m and sum(info["numeric_bin_rows"]) == A.m
+    assert info["numeric_bin_rows"][0] == info["bin_rows"][0]
+    assert info["numeric_bin_rows"][6] == info["bin_rows"][6]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
@@ -157,6 +159,27 @@ def test_spgemm_square_stencil_identity_permutation(dtype):
         r = perm[i]
         np.testing.assert_array_equal(col[rp[i]:rp[i + 1]], A.col_idx[A.row_ptr[r]:A.row_ptr[r + 1]])
         np.testing.assert_array_equal(val[rp[i]:rp[i + 1]], A.vals[A.row_ptr[r]:A.row_ptr[r + 1]])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_spgemm_many_products_few_columns(dtype):
+    """Rows whose products pile onto few columns: B's rows all live in
+    columns 0..39, so a row of C has at most 40 entries however many
+    products it takes (up to about 3000 here).  The numeric phase sizes its
+    tables by those entries, not by the products."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+    rng = np.random.default_rng(21)
+    k, n = 600, 5000
+    b_lens = rng.integers(1, 40, size=k).astype(np.int32)
+    B0 = synth.fill_random(b_lens, 40, dist=synth.DIST_NORMAL, seed=22, dtype=dtype)
+    B = synth.CSR(k, n, B0.row_ptr, B0.col_idx, B0.vals)
+    a_lens = rng.integers(0, 150, size=800).astype(np.int32)
+    A = synth.fill_random(a_lens, k, dist=synth.DIST_NORMAL, seed=23, dtype=dtype)
+    info = check_all(A, B, f"few columns {dtype}")
+    assert sum(info["numeric_bin_rows"]) == A.m
+    # rows with more than 128 products but at most 40 entries move to the smallest table
+    assert info["numeric_bin_rows"][1] > info["bin_rows"][1]
 
 
 def test_spgemm_degenerate_shapes():
