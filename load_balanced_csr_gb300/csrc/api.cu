@@ -15,6 +15,7 @@
 #include <string>
 #include <vector>
 
+#include "row_spmm.cuh"
 #include "spgemm.cuh"
 
 using namespace lbcsr;
@@ -616,12 +617,10 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
     if (p->m == 0 || k == 0) return SPMV_OK;
     if (!Y || (!X && p->nnz > 0)) return fail(SPMV_ERR_INVALID_ARG, "X or Y is NULL");
     if (ldx < k || ldy < k) return fail(SPMV_ERR_INVALID_ARG, "leading dimension smaller than k");
-    const int32_t rg_kmax = p->dtype == SPMV_F64 ? 16 : 32;  // one slice of columns: the matrix read once
-    if (is_rgcsr(p->kernel) && p->g_log2 == 5 && p->num_long_rows == 0 && (p->rg_slots > 0 || p->nnz == 0) &&
-        k <= rg_kmax) {
-        // the Row-grouped copy serves SpMM too: one thread per row (27-point
-        // stencil 128^3, k = 8: 174 us against 612 us on the merge path;
-        // wider X is sliced and re-reads the matrix, where merge path wins)
+    if (is_rgcsr(p->kernel) && p->g_log2 == 5 && p->num_long_rows == 0 && (p->rg_slots > 0 || p->nnz == 0)) {
+        // the Row-grouped copy serves SpMM too, in slices of 32 (fp32) or 16
+        // (fp64) columns, each slice reading the matrix again (27-point
+        // stencil 128^3: k = 8 in 174 us against 612 us on the merge path)
         RgSpmmArgs r;
         r.m = p->m;
         r.k = k;
@@ -637,6 +636,24 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
         r.alpha = alpha;
         r.beta = beta;
         const cudaError_t e = launch_rg_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
+        if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
+        return SPMV_OK;
+    }
+    if (p->stats.max_len <= kRowSpmmMaxLen && row_spmm_supported(p->dtype, k, X, ldx, Y, ldy)) {
+        // short rows only: a warp per 32 rows straight from CSR, lanes sharing X rows
+        RowSpmmArgs r;
+        r.m = p->m;
+        r.k = k;
+        r.row_ptr = p->row_ptr;
+        r.col_idx = p->col_idx;
+        r.vals = p->vals;
+        r.X = X;
+        r.ldx = ldx;
+        r.Y = Y;
+        r.ldy = ldy;
+        r.alpha = alpha;
+        r.beta = beta;
+        const cudaError_t e = launch_row_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
         return SPMV_OK;
     }

@@ -1,0 +1,138 @@
+// SpMM for matrices whose rows are all short: Y = alpha * A * X + beta * Y
+// straight from CSR, a warp per 32 consecutive rows, in the row loop of
+// "A GPU load-balancing programming model" (section 4.3, Listing 4: the
+// SpMV row loop with an inner loop over the columns of X).  With short
+// rows a warp's rows need about the same number of steps, so the rows
+// balance without a schedule.
+//
+// Level l of the warp is the l-th nonzero of each of its rows.  LPR lanes
+// share one X row slice of KC values (LPR x 16 bytes), so that one load
+// instruction of the warp covers 32 / LPR rows and as many lines; each lane
+// loads its own row's nonzero of a level and the lanes that serve a row take
+// its column and value by shuffles.  A lane keeps KC sums.  Wider X is taken
+// in slices of 32 (fp32) or 16 (fp64) columns, then of the powers of two
+// that remain.
+#include <type_traits>
+
+#include "internal.cuh"
+#include "row_spmm.cuh"
+
+namespace lbcsr {
+
+namespace {
+
+template <typename V, int KC>
+__global__ void __launch_bounds__(256)
+row_spmm_lines_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
+                      const V *__restrict__ val, const V *__restrict__ X, long long ldx, V *__restrict__ Y,
+                      long long ldy, V alpha, V beta) {
+    constexpr int W = 16 / sizeof(V);  // values per 16-byte load
+    constexpr int LPR = KC / W;        // lanes per X row
+    constexpr int RPI = 32 / LPR;      // rows per load instruction
+    constexpr int J = LPR;             // load instructions per level
+    using V4 = typename std::conditional<sizeof(V) == 4, float4, double2>::type;
+    const int64_t p0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * 32;
+    if (p0 >= m) return;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, cc = lane % LPR;
+    const int64_t row_own = p0 + lane;
+    const int start_own = row_own < m ? __ldg(rp + row_own) : 0;
+    const int len_own = row_own < m ? __ldg(rp + row_own + 1) - start_own : 0;
+    const int levels = __reduce_max_sync(0xffffffffu, len_own);
+    int lens[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) lens[j] = __shfl_sync(0xffffffffu, len_own, j * RPI + sub);
+    V acc[J][W];
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int w = 0; w < W; ++w) acc[j][w] = V(0);
+    int c_own = len_own > 0 ? ld_stream(col + start_own) : 0;
+    V v_own = len_own > 0 ? ld_stream(val + start_own) : V(0);
+    for (int l = 0; l < levels; ++l) {
+        int cn = 0;
+        V vn = V(0);
+        if (l + 1 < len_own) {  // the next level's nonzero while this one's X rows are gathered
+            cn = ld_stream(col + start_own + l + 1);
+            vn = ld_stream(val + start_own + l + 1);
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int c = __shfl_sync(0xffffffffu, c_own, j * RPI + sub);
+            const V v = __shfl_sync(0xffffffffu, v_own, j * RPI + sub);
+            if (l < lens[j]) {
+                const V4 q = __ldg(reinterpret_cast<const V4 *>(X + (int64_t)c * ldx + cc * W));
+                const V *f = reinterpret_cast<const V *>(&q);
+#pragma unroll
+                for (int w = 0; w < W; ++w) acc[j][w] = fma(v, f[w], acc[j][w]);
+            }
+        }
+        c_own = cn;
+        v_own = vn;
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int64_t row = p0 + j * RPI + sub;
+        if (row >= m) continue;
+        V *yr = Y + row * ldy + cc * W;
+        V r[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) r[w] = alpha * acc[j][w];
+        if (beta != V(0)) {
+            const V4 o = *reinterpret_cast<const V4 *>(yr);
+            const V *f = reinterpret_cast<const V *>(&o);
+#pragma unroll
+            for (int w = 0; w < W; ++w) r[w] = fma(beta, f[w], r[w]);
+        }
+        V4 out;
+        V *fo = reinterpret_cast<V *>(&out);
+#pragma unroll
+        for (int w = 0; w < W; ++w) fo[w] = r[w];
+        *reinterpret_cast<V4 *>(yr) = out;
+    }
+}
+
+template <typename V, int KC>
+cudaError_t launch_slice(const RowSpmmArgs &a, const V *X, V *Y, cudaStream_t stream) {
+    const int64_t warps = ((int64_t)a.m + 31) / 32;
+    row_spmm_lines_kernel<V, KC><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(
+        a.m, a.row_ptr, a.col_idx, static_cast<const V *>(a.vals), X, a.ldx, Y, a.ldy, (V)a.alpha, (V)a.beta);
+    return cudaGetLastError();
+}
+
+template <typename V>
+cudaError_t launch_typed(const RowSpmmArgs &a, cudaStream_t stream) {
+    constexpr int W = 16 / sizeof(V);
+    constexpr int KMAX = sizeof(V) == 8 ? 16 : 32;
+    int32_t c0 = 0;
+    while (c0 < a.k) {
+        const int32_t rest = a.k - c0;
+        int kc = KMAX;
+        while (kc > rest) kc >>= 1;  // rest is a multiple of W, so kc stays >= W
+        const V *X = static_cast<const V *>(a.X) + c0;
+        V *Y = static_cast<V *>(a.Y) + c0;
+        cudaError_t e;
+        if (kc == KMAX) e = launch_slice<V, KMAX>(a, X, Y, stream);
+        else if (kc >= 4 * W) e = launch_slice<V, 4 * W>(a, X, Y, stream);
+        else if (kc >= 2 * W) e = launch_slice<V, 2 * W>(a, X, Y, stream);
+        else e = launch_slice<V, W>(a, X, Y, stream);
+        if (e != cudaSuccess) return e;
+        c0 += kc;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+bool row_spmm_supported(spmv_dtype_t dtype, int32_t k, const void *X, int64_t ldx, const void *Y, int64_t ldy) {
+    const int64_t s = dtype == SPMV_F64 ? 8 : 4;
+    const int64_t w = 16 / s;
+    return k > 0 && k % w == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(Y) % 16 == 0 &&
+           (ldx * s) % 16 == 0 && (ldy * s) % 16 == 0;
+}
+
+cudaError_t launch_row_spmm(spmv_dtype_t dtype, const RowSpmmArgs &a, cudaStream_t stream) {
+    if (a.m <= 0 || a.k <= 0) return cudaSuccess;
+    return dtype == SPMV_F64 ? launch_typed<double>(a, stream) : launch_typed<float>(a, stream);
+}
+
+}  // namespace lbcsr
