@@ -406,7 +406,7 @@ def cpu_baseline_leg(workload_name: str, budget_s: float) -> dict:
             "cpu": cpu_model()}
 
 
-def spmm_path_of(info: dict, k: int, s: int):
+def spmm_path_of(info: dict, k: int, s: int, row_ptr):
     """(name, launches) of the SpMM path spmv_execute_multi takes for this
     plan with contiguous, 16-byte aligned X and Y of k columns (the choice
     made in the library's spmv_execute_multi, restated for the report)."""
@@ -414,15 +414,19 @@ def spmm_path_of(info: dict, k: int, s: int):
     w = 16 // s
     if info["kernel_name"] in ("rgcsr", "rgcsr_sorted") and info["rgcsr_group"] == 32 and info["num_long_rows"] == 0:
         return "Row-grouped SpMM (thread per row; lanes share X rows from 4 lanes per row)", -(-k // kmax)
-    if info["stats"]["max_len"] <= 64 and k % w == 0:
-        launches, rest = 0, k
+    n_long = int((np.diff(row_ptr) >= 65).sum())
+    if (n_long == 0 or (n_long * 4096 <= info["m"] and k <= 2 * kmax)) and k % w == 0:
+        slices, rest = 0, k
         while rest > 0:
             kc = kmax
             while kc > rest:
                 kc //= 2
             rest -= kc
-            launches += 1
-        return "short-row SpMM from CSR (warp per 32 rows, lanes share X rows)", launches
+            slices += 1
+        if n_long == 0:
+            return "short-row SpMM from CSR (warp per 32 rows, lanes share X rows)", slices
+        return ("CSR SpMM: warp per 32 short rows + warp per 4096-nonzero segment of the rows of 65 or more",
+                2 * slices)
     return "merge-path SpMM (runs of warp tiles, lanes over columns)", -(-k // 128)
 
 
@@ -448,7 +452,7 @@ def run_spmm(args, workload_name: str) -> dict | None:
     Y = torch.zeros((A.m, k), dtype=vt, device=dev)
     stream = torch.cuda.current_stream(dev)
     plan = lb.Plan(rp, col, val, A.n, kernel=args.kernel, with_spmm=True)
-    spmm_path = spmm_path_of(plan.info(), k, s)
+    spmm_path = spmm_path_of(plan.info(), k, s, A.row_ptr)
     for _ in range(args.warmup):
         plan.execute_multi(X, Y, W.alpha, W.beta, stream)
     torch.cuda.synchronize(dev)

@@ -76,6 +76,16 @@ struct spmv_plan_s {
     size_t spmm_bytes = 0;
     void *spmm_tail = nullptr, *spmm_head = nullptr;
     int32_t *spmm_arrivals = nullptr;
+    // SpMM over long rows (rows longer than kRowSpmmMaxLen): their list,
+    // segments, partials and arrival counters, one allocation
+    void *spmm_long = nullptr;
+    size_t spmm_long_bytes = 0;
+    int32_t spmm_num_long = 0;
+    int64_t spmm_num_segs = 0;
+    int32_t *spmm_long_rows = nullptr;
+    int64_t *spmm_seg_begin = nullptr;
+    void *spmm_seg_partial = nullptr;
+    int32_t *spmm_long_arrivals = nullptr;
     int32_t *rg_col = nullptr;       // [rg_slots]
     void *rg_val = nullptr;          // [rg_slots]
 
@@ -187,6 +197,7 @@ void destroy_plan(spmv_plan_s *p) {
     if (p->rg) cudaFree(p->rg);
     if (p->aux) cudaFree(p->aux);
     if (p->spmm) cudaFree(p->spmm);
+    if (p->spmm_long) cudaFree(p->spmm_long);
     if (p->arena) cudaFree(p->arena);
     delete p;
 }
@@ -318,6 +329,66 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
 
 // A^T in CSR form (one allocation the plan keeps), built with a temporary
 // scratch, and a plan of its own for it.
+// The long rows of SpMM: rows of at least kSpmmLongMin nonzeros, listed
+// with the same two passes as the long rows of SpMV, with segment partials
+// of 32 values (one slice of columns).
+spmv_status_t build_spmm_long_rows(spmv_plan_s *p, cudaStream_t stream) {
+    const int32_t m = p->m;
+    const size_t vs = value_size(p->dtype);
+    const int nc = long_rows_num_chunks(m);
+    const int64_t long_ub = rows_at_least(p->stats, kSpmmLongMin);
+    const int64_t segs_ub = (int64_t)p->nnz / kLongSegmentNnz + long_ub;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t o_long = take(sizeof(int32_t) * long_ub);
+    const size_t o_segb = take(sizeof(int64_t) * (long_ub + 1));
+    const size_t o_segp = take(vs * 32 * segs_ub);
+    const size_t o_larr = take(sizeof(int32_t) * long_ub);
+    const size_t o_crow = take(sizeof(int64_t) * nc);
+    const size_t o_cseg = take(sizeof(int64_t) * nc);
+    const size_t o_crow_off = take(sizeof(int64_t) * (nc + 1));
+    const size_t o_cseg_off = take(sizeof(int64_t) * (nc + 1));
+    const size_t o_scr = take(sizeof(int64_t) * scan_scratch_elems(nc));
+    p->spmm_long_bytes = off;
+    cudaError_t e = cudaMalloc(&p->spmm_long, p->spmm_long_bytes);
+    if (e != cudaSuccess) {
+        p->spmm_long = nullptr;
+        return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpMM long-row workspace: ") + cudaGetErrorString(e));
+    }
+    char *base = static_cast<char *>(p->spmm_long);
+    p->spmm_long_rows = reinterpret_cast<int32_t *>(base + o_long);
+    p->spmm_seg_begin = reinterpret_cast<int64_t *>(base + o_segb);
+    p->spmm_seg_partial = base + o_segp;
+    p->spmm_long_arrivals = reinterpret_cast<int32_t *>(base + o_larr);
+    int64_t *chunk_rows = reinterpret_cast<int64_t *>(base + o_crow);
+    int64_t *chunk_segs = reinterpret_cast<int64_t *>(base + o_cseg);
+    int64_t *chunk_row_off = reinterpret_cast<int64_t *>(base + o_crow_off);
+    int64_t *chunk_seg_off = reinterpret_cast<int64_t *>(base + o_cseg_off);
+    int64_t *scratch = reinterpret_cast<int64_t *>(base + o_scr);
+    int64_t sizes[2] = {0, 0};
+    e = cudaMemsetAsync(p->spmm_long_arrivals, 0, sizeof(int32_t) * long_ub, stream);
+    if (e == cudaSuccess) e = launch_long_rows_count(m, p->row_ptr, kSpmmLongMin, chunk_rows, chunk_segs, stream);
+    if (e == cudaSuccess) e = launch_exclusive_scan(chunk_rows, nc, chunk_row_off, scratch, stream);
+    if (e == cudaSuccess) e = launch_exclusive_scan(chunk_segs, nc, chunk_seg_off, scratch, stream);
+    if (e == cudaSuccess)
+        e = launch_long_rows_scatter(m, p->row_ptr, kSpmmLongMin, chunk_row_off, chunk_seg_off, p->spmm_long_rows,
+                                     p->spmm_seg_begin, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&sizes[0], chunk_row_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&sizes[1], chunk_seg_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "SpMM long rows");
+    if (sizes[0] > long_ub || sizes[1] > segs_ub) return fail(SPMV_ERR_CUDA, "SpMM long-row count exceeds its bound");
+    p->spmm_num_long = (int32_t)sizes[0];
+    p->spmm_num_segs = sizes[1];
+    return SPMV_OK;
+}
+
 spmv_status_t build_transpose(spmv_plan_s *p, cudaStream_t stream) {
     const size_t vs = value_size(p->dtype);
     const size_t o_ptr = 0;
@@ -536,6 +607,13 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
             return cuda_fail(e, "SpMM scratch");
         }
     }
+    if (p->with_spmm && m > 0 && p->stats.max_len > kRowSpmmMaxLen) {
+        const spmv_status_t st = build_spmm_long_rows(p, stream);
+        if (st != SPMV_OK) {
+            destroy_plan(p);
+            return st;
+        }
+    }
     if (opt.with_transpose) {
         const spmv_status_t st = build_transpose(p, stream);
         if (st != SPMV_OK) {
@@ -639,8 +717,14 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
         if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
         return SPMV_OK;
     }
-    if (p->stats.max_len <= kRowSpmmMaxLen && row_spmm_supported(p->dtype, k, X, ldx, Y, ldy)) {
-        // short rows only: a warp per 32 rows straight from CSR, lanes sharing X rows
+    // with long rows, at most two slices of columns (each slice reads the
+    // matrix again; skew, fp64, k = 128 in 8 slices: 24.4 ms against 23.3 ms
+    // on the merge path)
+    const bool rare_long = p->spmm_num_long > 0 && (int64_t)p->spmm_num_long * kSpmmRowsPerLongRow <= p->m &&
+                           k <= (p->dtype == SPMV_F64 ? 32 : 64);
+    if ((p->stats.max_len <= kRowSpmmMaxLen || rare_long) && row_spmm_supported(p->dtype, k, X, ldx, Y, ldy)) {
+        // a warp per 32 rows straight from CSR, lanes sharing X rows; rows
+        // longer than kRowSpmmMaxLen, if any, by a warp per 4096-nonzero segment
         RowSpmmArgs r;
         r.m = p->m;
         r.k = k;
@@ -653,6 +737,13 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
         r.ldy = ldy;
         r.alpha = alpha;
         r.beta = beta;
+        r.long_min = kSpmmLongMin;
+        r.num_long = p->spmm_num_long;
+        r.num_segs = p->spmm_num_segs;
+        r.long_rows = p->spmm_long_rows;
+        r.seg_begin = p->spmm_seg_begin;
+        r.seg_partial = p->spmm_seg_partial;
+        r.arrivals = p->spmm_long_arrivals;
         const cudaError_t e = launch_row_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
         return SPMV_OK;
@@ -731,7 +822,8 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->num_tiles = p->num_tiles;
     info->num_long_rows = p->num_long_rows;
     info->launches_per_execute = p->m > 0 ? 1 + (p->num_long_rows > 0 ? 1 : 0) : 0;
-    info->workspace_bytes = (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes + p->spmm_bytes + p->tr_bytes);
+    info->workspace_bytes =
+        (int64_t)(p->arena_bytes + p->aux_bytes + p->rg_bytes + p->spmm_bytes + p->spmm_long_bytes + p->tr_bytes);
     info->transposed_kernel = p->tplan ? p->tplan->kernel : -1;
     if (p->tplan) {
         spmv_plan_info_t ti;

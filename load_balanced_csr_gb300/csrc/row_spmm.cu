@@ -12,6 +12,10 @@
 // its column and value by shuffles.  A lane keeps KC sums.  Wider X is taken
 // in slices of 32 (fp32) or 16 (fp64) columns, then of the powers of two
 // that remain.
+//
+// Rows of at least long_min nonzeros, when the plan lists them, are left to
+// a warp-per-segment kernel (long_spmm_kernel) and skipped here.
+#include <climits>
 #include <type_traits>
 
 #include "internal.cuh"
@@ -25,7 +29,7 @@ template <typename V, int KC>
 __global__ void __launch_bounds__(256)
 row_spmm_lines_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
                       const V *__restrict__ val, const V *__restrict__ X, long long ldx, V *__restrict__ Y,
-                      long long ldy, V alpha, V beta) {
+                      long long ldy, V alpha, V beta, int32_t skip_len) {
     constexpr int W = 16 / sizeof(V);  // values per 16-byte load
     constexpr int LPR = KC / W;        // lanes per X row
     constexpr int RPI = 32 / LPR;      // rows per load instruction
@@ -36,11 +40,13 @@ row_spmm_lines_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *
     const int lane = threadIdx.x & 31, sub = lane / LPR, cc = lane % LPR;
     const int64_t row_own = p0 + lane;
     const int start_own = row_own < m ? __ldg(rp + row_own) : 0;
-    const int len_own = row_own < m ? __ldg(rp + row_own + 1) - start_own : 0;
+    const int len_row = row_own < m ? __ldg(rp + row_own + 1) - start_own : 0;
+    const int len_own = len_row < skip_len ? len_row : 0;  // long rows are the long-row kernel's
     const int levels = __reduce_max_sync(0xffffffffu, len_own);
     int lens[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) lens[j] = __shfl_sync(0xffffffffu, len_own, j * RPI + sub);
+    const unsigned mine_short = __ballot_sync(0xffffffffu, len_row < skip_len);
     V acc[J][W];
 #pragma unroll
     for (int j = 0; j < J; ++j)
@@ -72,7 +78,7 @@ row_spmm_lines_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int64_t row = p0 + j * RPI + sub;
-        if (row >= m) continue;
+        if (row >= m || !((mine_short >> (j * RPI + sub)) & 1u)) continue;
         V *yr = Y + row * ldy + cc * W;
         V r[W];
 #pragma unroll
@@ -91,11 +97,96 @@ row_spmm_lines_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *
     }
 }
 
+// Long rows (len >= skip_len): a warp per segment of kLongSegmentNnz
+// nonzeros, as the long-row SpMV kernel, with the warp's lanes spread over
+// a slice of kc <= 32 columns: KQ lanes (kc rounded up to a power of two)
+// per nonzero, 32 / KQ nonzeros at a time, so that one load instruction
+// reads the X row slices of 32 / KQ nonzeros, each one contiguous run.  The
+// segment's columns and values are loaded 32 at a time, coalesced, and
+// shared by shuffles.  Slots are added by xor shuffles at the end.  A
+// one-segment row is written directly; a longer row's segment partials
+// (kc values each) are added in segment order by the segment that arrives
+// last, which then writes the row of Y.
+template <typename V, int KQ>
+__global__ void __launch_bounds__(256)
+long_spmm_kernel(const int32_t *__restrict__ rp, const int32_t *__restrict__ col, const V *__restrict__ val,
+                 int32_t kc, const V *__restrict__ X, long long ldx, V *__restrict__ Y, long long ldy, V alpha,
+                 V beta, const int32_t *__restrict__ long_rows, const int64_t *__restrict__ seg_begin,
+                 int32_t num_long, int64_t num_segs, V *__restrict__ seg_partial, int32_t *__restrict__ arrivals) {
+    constexpr int S = 32 / KQ;  // nonzeros per step
+    const int lane = threadIdx.x & 31, slot = lane / KQ, cq = lane % KQ;
+    const int64_t sg = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (sg >= num_segs) return;
+    int lo = 0, hi = num_long - 1;  // the long row holding segment sg
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seg_begin[mid] <= sg) lo = mid;
+        else hi = mid - 1;
+    }
+    const int32_t row = long_rows[lo];
+    const int64_t first = seg_begin[lo];
+    const int64_t nsegs = seg_begin[lo + 1] - first;
+    const int32_t rb = rp[row], re = rp[row + 1];
+    const int32_t b = rb + (int32_t)((sg - first) * kLongSegmentNnz);
+    const int32_t e = min(b + kLongSegmentNnz, re);
+    const bool use = cq < kc;
+    const V *xb = X + cq;
+    V acc = V(0);
+    for (int32_t k0 = b; k0 < e; k0 += 32) {
+        const int n = min(32, e - k0);
+        const int c_l = lane < n ? ld_stream(col + k0 + lane) : 0;
+        const V v_l = lane < n ? ld_stream(val + k0 + lane) : V(0);
+#pragma unroll 8
+        for (int i = 0; i < 32; i += S) {
+            const int src = i + slot;
+            const int c = __shfl_sync(0xffffffffu, c_l, src);
+            const V v = __shfl_sync(0xffffffffu, v_l, src);
+            if (src < n && use) acc = fma(v, ld_gather(xb + (int64_t)c * ldx), acc);
+        }
+    }
+#pragma unroll
+    for (int off = KQ; off < 32; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    V *yr = Y + (int64_t)row * ldy + cq;
+    if (nsegs == 1) {
+        if (slot == 0 && use) {
+            V r = alpha * acc;
+            if (beta != V(0)) r = fma(beta, *yr, r);
+            *yr = r;
+        }
+        return;
+    }
+    if (slot == 0 && use) seg_partial[sg * KQ + cq] = acc;
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        last = atomicAdd(arrivals + lo, 1) == (int)(nsegs - 1);
+        if (last) __threadfence();
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    if (slot == 0 && use) {
+        V t = V(0);
+        for (int64_t q = first; q < first + nsegs; ++q) t += __ldcg(seg_partial + q * KQ + cq);
+        V r = alpha * t;
+        if (beta != V(0)) r = fma(beta, *yr, r);
+        *yr = r;
+    }
+    if (lane == 0) arrivals[lo] = 0;  // ready for the next product
+}
+
 template <typename V, int KC>
 cudaError_t launch_slice(const RowSpmmArgs &a, const V *X, V *Y, cudaStream_t stream) {
+    if (a.num_long > 0 && a.num_segs > 0) {
+        long_spmm_kernel<V, KC><<<(unsigned)((a.num_segs + 7) / 8), 256, 0, stream>>>(
+            a.row_ptr, a.col_idx, static_cast<const V *>(a.vals), KC, X, a.ldx, Y, a.ldy, (V)a.alpha, (V)a.beta,
+            a.long_rows, a.seg_begin, a.num_long, a.num_segs, static_cast<V *>(a.seg_partial), a.arrivals);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int64_t warps = ((int64_t)a.m + 31) / 32;
     row_spmm_lines_kernel<V, KC><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(
-        a.m, a.row_ptr, a.col_idx, static_cast<const V *>(a.vals), X, a.ldx, Y, a.ldy, (V)a.alpha, (V)a.beta);
+        a.m, a.row_ptr, a.col_idx, static_cast<const V *>(a.vals), X, a.ldx, Y, a.ldy, (V)a.alpha, (V)a.beta,
+        a.num_long > 0 ? a.long_min : INT32_MAX);
     return cudaGetLastError();
 }
 

@@ -9,6 +9,15 @@ namespace lbcsr {
 // rows longer than this keep SpMM on the merge-path partition
 constexpr int32_t kRowSpmmMaxLen = 64;
 
+// rows of at least this many nonzeros go to the long-row SpMM kernel when
+// the matrix has rows longer than kRowSpmmMaxLen
+constexpr int32_t kSpmmLongMin = kRowSpmmMaxLen + 1;
+// ... and only when they are rare: at most one per kSpmmRowsPerLongRow rows.
+// (Measured on GB300: 65 long rows in 8.4 M, k = 8: 2178 -> 1609 us; 93,535
+// long rows in 4.2 M, k = 32: 3092 -> 7273 us, so such matrices keep the
+// merge-path SpMM.)
+constexpr int64_t kSpmmRowsPerLongRow = 4096;
+
 struct RowSpmmArgs {
     int32_t m, k;
     const int32_t *row_ptr, *col_idx;
@@ -18,6 +27,16 @@ struct RowSpmmArgs {
     void *Y;
     int64_t ldy;
     double alpha, beta;
+    // long rows (num_long == 0: none): rows of length >= long_min, ascending,
+    // their first segments of kLongSegmentNnz nonzeros, per segment a partial
+    // of up to 32 values, per row an arrival counter (zero between products)
+    int32_t long_min;
+    int32_t num_long;
+    int64_t num_segs;
+    const int32_t *long_rows;
+    const int64_t *seg_begin;
+    void *seg_partial;
+    int32_t *arrivals;
 };
 
 // k a multiple of the values per 16 bytes; X, Y 16-byte aligned row by row

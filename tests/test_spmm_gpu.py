@@ -64,14 +64,34 @@ def test_spmm_random(dtype, k):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_spmm_rare_long_rows(dtype):
+    """A few long rows among many short ones (at most one per 4096 rows):
+    with k a multiple of the values per 16 bytes, the short rows go to the
+    CSR warp kernel and rows of at least 65 nonzeros to the warp-per-segment
+    kernel; rows of 64, 65, 4096 and 4097 nonzeros sit on its boundaries,
+    and a row of 60,000 spans 15 segments added by the last to arrive."""
+    rng = np.random.default_rng(12)
+    lens = rng.integers(0, 9, size=70000).astype(np.int32)
+    lens[[5, 700, 33000, 45000, 69999]] = [64, 65, 4096, 4097, 60000]
+    A = synth.fill_random(lens, 80000, dist=synth.DIST_NORMAL, seed=12, dtype=dtype)
+    for k, alpha, beta in [(8, 0.5, 2.0), (16, 1.0, 0.0), (40, -1.5, 0.25), (4, 1.0, 1.0)]:
+        X, Y0, Yg = run_spmm(A, k, alpha, beta, kernel="auto", seed=k)
+        check(A, X, Y0, Yg, alpha, beta, f"spmm rare long rows {dtype} k={k}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
 def test_spmm_rows_cut_between_many_warps(dtype):
+    """Many long rows among few short ones: the merge-path SpMM, rows cut
+    between warps' runs (rows of 64, 65, 4096 and 4097 nonzeros too)."""
     lens = np.full(3000, 2, dtype=np.int32)
     lens[10] = 60000       # spans many warps' runs
     lens[1500:1510] = 5000
     lens[-1] = 20000       # open at the end of the last run
     lens[200:260] = 0
+    lens[300], lens[301], lens[302], lens[303] = 64, 65, 4096, 4097
     A = synth.fill_random(lens, 70000, dist=synth.DIST_NORMAL, seed=4, dtype=dtype)
-    for k, kernel in [(8, "merge_path"), (40, "auto")]:
+    for k, kernel in [(8, "merge_path"), (40, "auto"), (4, "auto"), (64, "auto"), (7, "merge_path"),
+                      (33, "auto")]:
         X, Y0, Yg = run_spmm(A, k, 0.5, 2.0, kernel=kernel, seed=4)
         check(A, X, Y0, Yg, 0.5, 2.0, f"spmm cut rows {dtype} k={k}")
 
