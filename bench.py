@@ -412,8 +412,12 @@ def spmm_path_of(info: dict, k: int, s: int, row_ptr):
     made in the library's spmv_execute_multi, restated for the report)."""
     kmax = 16 if s == 8 else 32
     w = 16 // s
-    if info["kernel_name"] in ("rgcsr", "rgcsr_sorted") and info["rgcsr_group"] == 32 and info["num_long_rows"] == 0:
-        return "Row-grouped SpMM (thread per row; lanes share X rows from 4 lanes per row)", -(-k // kmax)
+    if info["kernel_name"] in ("rgcsr", "rgcsr_sorted") and info["rgcsr_group"] == 32 and \
+            info["num_long_rows"] * 4096 <= info["m"]:
+        if info["num_long_rows"] == 0:
+            return "Row-grouped SpMM (thread per row; lanes share X rows from 4 lanes per row)", -(-k // kmax)
+        return ("Row-grouped SpMM + a warp per 4096-nonzero segment of the long rows",
+                -(-k // kmax) + -(-k // 32))
     n_long = int((np.diff(row_ptr) >= 65).sum())
     if (n_long == 0 or (n_long * 4096 <= info["m"] and k <= 2 * kmax)) and k % w == 0:
         slices, rest = 0, k

@@ -86,6 +86,10 @@ struct spmv_plan_s {
     int64_t *spmm_seg_begin = nullptr;
     void *spmm_seg_partial = nullptr;
     int32_t *spmm_long_arrivals = nullptr;
+    // SpMM over the long rows a Row-grouped plan leaves out: k-wide segment
+    // partials (32 values per segment) and arrival counters
+    void *spmm_rg_long = nullptr;
+    int32_t *spmm_rg_arrivals = nullptr;
     int32_t *rg_col = nullptr;       // [rg_slots]
     void *rg_val = nullptr;          // [rg_slots]
 
@@ -198,6 +202,7 @@ void destroy_plan(spmv_plan_s *p) {
     if (p->aux) cudaFree(p->aux);
     if (p->spmm) cudaFree(p->spmm);
     if (p->spmm_long) cudaFree(p->spmm_long);
+    if (p->spmm_rg_long) cudaFree(p->spmm_rg_long);
     if (p->arena) cudaFree(p->arena);
     delete p;
 }
@@ -628,6 +633,23 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
             return st;
         }
     }
+    if (p->with_spmm && is_rgcsr(p->kernel) && p->num_long_rows > 0) {
+        // SpMM partials for the long rows the Row-grouped copy leaves out
+        const size_t part = align_up(value_size(dtype) * 32 * (size_t)p->num_segs, 256);
+        e = cudaMalloc(&p->spmm_rg_long, part + sizeof(int32_t) * (size_t)p->num_long_rows);
+        if (e != cudaSuccess) {
+            p->spmm_rg_long = nullptr;
+            destroy_plan(p);
+            return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpMM long-row partials: ") + cudaGetErrorString(e));
+        }
+        p->spmm_rg_arrivals = reinterpret_cast<int32_t *>(static_cast<char *>(p->spmm_rg_long) + part);
+        e = cudaMemsetAsync(p->spmm_rg_arrivals, 0, sizeof(int32_t) * (size_t)p->num_long_rows, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) {
+            destroy_plan(p);
+            return cuda_fail(e, "SpMM long-row partials");
+        }
+    }
     *out = p;
     return SPMV_OK;
 }
@@ -695,7 +717,12 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
     if (p->m == 0 || k == 0) return SPMV_OK;
     if (!Y || (!X && p->nnz > 0)) return fail(SPMV_ERR_INVALID_ARG, "X or Y is NULL");
     if (ldx < k || ldy < k) return fail(SPMV_ERR_INVALID_ARG, "leading dimension smaller than k");
-    if (is_rgcsr(p->kernel) && p->g_log2 == 5 && p->num_long_rows == 0 && (p->rg_slots > 0 || p->nnz == 0)) {
+    // Row-grouped plans: long rows, if any, must be rare (as for the CSR path:
+    // a power-law matrix forced onto the window-sorted copy took 5.3 ms at
+    // k = 32 against 3.1 ms on the merge path)
+    const bool rg_long_ok = p->num_long_rows == 0 ||
+                            (p->spmm_rg_long && (int64_t)p->num_long_rows * kSpmmRowsPerLongRow <= p->m);
+    if (is_rgcsr(p->kernel) && p->g_log2 == 5 && rg_long_ok && (p->rg_slots > 0 || p->nnz == 0)) {
         // the Row-grouped copy serves SpMM too, in slices of 32 (fp32) or 16
         // (fp64) columns, each slice reading the matrix again (27-point
         // stencil 128^3: k = 8 in 174 us against 612 us on the merge path)
@@ -713,7 +740,28 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
         r.ldy = ldy;
         r.alpha = alpha;
         r.beta = beta;
-        const cudaError_t e = launch_rg_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
+        cudaError_t e = cudaSuccess;
+        if (p->num_long_rows > 0) {  // the rows the copy leaves out
+            LongSpmmArgs l;
+            l.k = k;
+            l.row_ptr = p->row_ptr;
+            l.col_idx = p->col_idx;
+            l.vals = p->vals;
+            l.X = X;
+            l.ldx = ldx;
+            l.Y = Y;
+            l.ldy = ldy;
+            l.alpha = alpha;
+            l.beta = beta;
+            l.num_long = p->num_long_rows;
+            l.num_segs = p->num_segs;
+            l.long_rows = p->long_rows;
+            l.seg_begin = p->seg_begin;
+            l.seg_partial = p->spmm_rg_long;
+            l.arrivals = p->spmm_rg_arrivals;
+            e = launch_long_spmm(p->dtype, l, reinterpret_cast<cudaStream_t>(stream_handle));
+        }
+        if (e == cudaSuccess) e = launch_rg_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
         return SPMV_OK;
     }

@@ -1,7 +1,8 @@
 // SpMM over the Row-grouped copy: Y = alpha * A * X + beta * Y for plans
 // that hold the interleaved copy of A in groups of 32 rows ("New
 // Row-grouped CSR format for storing the sparse matrices on GPU with
-// implementation in CUDA", section 3) and no long rows.  One thread per
+// implementation in CUDA", section 3); long rows, which the copy leaves
+// out, are the long-row SpMM kernel's.  One thread per
 // row, as in the Row-grouped SpMV kernel: at each level the warp reads its
 // 32 rows' slots as one contiguous line, and every thread gathers its X row
 // -- KC consecutive values, with 16-byte loads when X allows -- and keeps
@@ -150,7 +151,7 @@ rg_spmm_lines_kernel(int32_t m, int64_t ngroups, const int64_t *__restrict__ gp,
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int64_t pos = p0 + j * RPI + sub;
-        if (pos >= m) continue;
+        if (pos >= m || lens[j] < 0) continue;  // (a long row is the long-row kernel's)
         const int64_t row = perm ? perm[pos] : pos;
         V *yr = Y + row * ldy + cc * W;
         V r[W];

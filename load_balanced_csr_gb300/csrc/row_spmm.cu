@@ -214,6 +214,39 @@ cudaError_t launch_typed(const RowSpmmArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_long_spmm(spmv_dtype_t dtype, const LongSpmmArgs &a, cudaStream_t stream) {
+    if (a.num_long <= 0 || a.num_segs <= 0 || a.k <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((a.num_segs + 7) / 8);
+    for (int32_t c0 = 0; c0 < a.k; c0 += 32) {
+        const int32_t kc = a.k - c0 < 32 ? a.k - c0 : 32;
+        const int kq = kc <= 1 ? 1 : kc <= 2 ? 2 : kc <= 4 ? 4 : kc <= 8 ? 8 : kc <= 16 ? 16 : 32;
+#define LONG_SPMM(V, KQ)                                                                                       \
+    long_spmm_kernel<V, KQ><<<blocks, 256, 0, stream>>>(                                                        \
+        a.row_ptr, a.col_idx, static_cast<const V *>(a.vals), kc, static_cast<const V *>(a.X) + c0, a.ldx,      \
+        static_cast<V *>(a.Y) + c0, a.ldy, (V)a.alpha, (V)a.beta, a.long_rows, a.seg_begin, a.num_long,          \
+        a.num_segs, static_cast<V *>(a.seg_partial), a.arrivals)
+#define LONG_SPMM_T(V)                                                                                         \
+    switch (kq) {                                                                                               \
+    case 1: LONG_SPMM(V, 1); break;                                                                             \
+    case 2: LONG_SPMM(V, 2); break;                                                                             \
+    case 4: LONG_SPMM(V, 4); break;                                                                             \
+    case 8: LONG_SPMM(V, 8); break;                                                                             \
+    case 16: LONG_SPMM(V, 16); break;                                                                           \
+    default: LONG_SPMM(V, 32); break;                                                                           \
+    }
+        if (dtype == SPMV_F64) {
+            LONG_SPMM_T(double)
+        } else {
+            LONG_SPMM_T(float)
+        }
+#undef LONG_SPMM_T
+#undef LONG_SPMM
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 bool row_spmm_supported(spmv_dtype_t dtype, int32_t k, const void *X, int64_t ldx, const void *Y, int64_t ldy) {
     const int64_t s = dtype == SPMV_F64 ? 8 : 4;
     const int64_t w = 16 / s;

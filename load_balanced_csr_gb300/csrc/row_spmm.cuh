@@ -39,6 +39,28 @@ struct RowSpmmArgs {
     int32_t *arrivals;
 };
 
+// The long rows alone (any k, any X and Y layout): a warp per segment of
+// kLongSegmentNnz nonzeros of the listed rows, in slices of 32 columns;
+// seg_partial holds 32 values per segment.  Used next to the Row-grouped
+// SpMM, whose copy leaves the long rows out.
+struct LongSpmmArgs {
+    int32_t k;
+    const int32_t *row_ptr, *col_idx;
+    const void *vals;
+    const void *X;
+    int64_t ldx;
+    void *Y;
+    int64_t ldy;
+    double alpha, beta;
+    int32_t num_long;
+    int64_t num_segs;
+    const int32_t *long_rows;
+    const int64_t *seg_begin;
+    void *seg_partial;
+    int32_t *arrivals;
+};
+cudaError_t launch_long_spmm(spmv_dtype_t dtype, const LongSpmmArgs &a, cudaStream_t stream);
+
 // k a multiple of the values per 16 bytes; X, Y 16-byte aligned row by row
 bool row_spmm_supported(spmv_dtype_t dtype, int32_t k, const void *X, int64_t ldx, const void *Y, int64_t ldy);
 cudaError_t launch_row_spmm(spmv_dtype_t dtype, const RowSpmmArgs &a, cudaStream_t stream);

@@ -145,3 +145,20 @@ def test_spmm_over_the_row_grouped_copy(dtype, kernel):
         for alpha, beta in [(1.0, 0.0), (-0.5, 1.5)]:
             X, Y0, Yg = run_spmm(A, k, alpha, beta, kernel=kernel, pad=pad, seed=k)
             check(A, X, Y0, Yg, alpha, beta, f"spmm {kernel} {dtype} k={k} pad={pad}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("kernel", ["rgcsr", "rgcsr_sorted"])
+def test_spmm_row_grouped_with_long_rows(dtype, kernel):
+    """Row-grouped plans whose copy leaves a few long rows out (512 nonzeros
+    or more, at most one per 4096 rows): those rows by the long-row SpMM kernel (a warp per 4096-nonzero
+    segment, slices of 32 columns), the others over the copy.  Rows of 511,
+    512, 4096, 4097 and 30,000 nonzeros; k narrow, wide and odd; X padded."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(0, 40, size=20000).astype(np.int32)  # rare long rows: at most one per 4096
+    lens[[3, 900, 9000, 13100, 19999]] = [511, 512, 4096, 4097, 30000]
+    A = synth.fill_random(lens, 40000, dist=synth.DIST_NORMAL, seed=31, dtype=dtype)
+    for k, pad, alpha, beta in [(1, 0, 1.0, 0.0), (8, 0, 0.5, 2.0), (32, 0, 1.0, 0.0), (33, 1, -1.0, 0.5),
+                                (70, 0, 1.0, 1.0)]:
+        X, Y0, Yg = run_spmm(A, k, alpha, beta, kernel=kernel, pad=pad, seed=k)
+        check(A, X, Y0, Yg, alpha, beta, f"spmm {kernel} long rows {dtype} k={k}")
