@@ -504,7 +504,7 @@ def run_spgemm(args, workload_name: str) -> dict | None:
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    A = synth.workload(workload_name).A
+    A = synth.workload(workload_name, scale=args.scale).A
     s = A.vals.dtype.itemsize
     rp = torch.from_numpy(A.row_ptr).to(dev)
     col = torch.from_numpy(A.col_idx).to(dev)
@@ -550,7 +550,7 @@ def run_spgemm(args, workload_name: str) -> dict | None:
         "value": round(2.0 * products / (med * 1e-6) / 1e9, 2), "unit": "GFLOP/s", "n_gpus": 1, "steps": K,
         "warmup": args.warmup, "median_us": round(med, 1), "higher_is_better": True, "dtype": A.dtype,
         "data": "synthetic",
-        "config": {"workload": workload_name, "products": products, "c_nnz": info["c_nnz"],
+        "config": {"workload": workload_name, "scale": args.scale, "products": products, "c_nnz": info["c_nnz"],
                    "bin_rows": info["bin_rows"], "numeric_bin_rows": info["numeric_bin_rows"],
                    "dense_slots": info["dense_slots"],
                    "dense_pieces": info["dense_pieces"], "dense_waves": info["dense_waves"],
@@ -578,6 +578,8 @@ def main():
     ap.add_argument("--rhs", type=int, default=0, help="k > 0: time SpMM with k right-hand sides instead")
     ap.add_argument("--transposed", action="store_true", help="time the transposed product A^T x instead")
     ap.add_argument("--spgemm", action="store_true", help="time SpGEMM C = A*A instead")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="SpGEMM only: shrink the workload by this factor (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -14,10 +14,12 @@
 // with 2048, 4096 or 8192 slots; more -- a dense row of C in global memory
 // (values and a bit per column), each row's products cut into equal pieces
 // of at most 32768, a CTA per piece.
+// The numeric phase re-bins the rows between those bounds by the entries the
+// symbolic phase found, so that its tables fit the row, not its products.
 // Tables use multiplicative hashing and linear probing and stay at most
-// half full; the thread that
-// claims a slot appends it to a list, so that after a row only the claimed
-// slots are read (sorted by column with a bitonic network) and cleared.
+// half full; the thread that claims a slot appends it to a list, so that
+// after a row only the claimed slots are read (sorted by column by buckets,
+// or a bitonic network) and cleared.
 // Values in hash tables are added with atomics, so their summation order
 // (and the last bits of a sum) may differ from run to run; the pattern of C
 // does not.
@@ -252,14 +254,73 @@ __device__ __forceinline__ void sg_walk_row(const SgCsr &mat, const V *__restric
     }
 }
 
+// Reductions and an exclusive scan over a group of G threads: a warp
+// (G = 32), or the whole CTA (G > 32, one group per CTA; s_a and s_b hold
+// one value per warp).
+template <int G>
+__device__ __forceinline__ void sg_group_minmax(unsigned &lo, unsigned &hi, unsigned *s_a, unsigned *s_b) {
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (G == 32) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        s_a[warp] = lo;
+        s_b[warp] = hi;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < G / 32; ++q) {
+        lo = min(lo, s_a[q]);
+        hi = max(hi, s_b[q]);
+    }
+    __syncthreads();
+}
+
+// exclusive prefix sum of v over the group, and the group's largest v
+template <int G>
+__device__ __forceinline__ int sg_group_scan(int v, int &maxv, int *s_a, int *s_b) {
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x % G) >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    maxv = __reduce_max_sync(0xffffffffu, v);
+    if (G == 32) return incl - v;
+    if (lane == 31) s_a[warp] = incl;
+    if (lane == 0) s_b[warp] = maxv;
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int q = 0; q < G / 32; ++q) {
+        if (q < warp) before += s_a[q];
+        maxv = max(maxv, s_b[q]);
+    }
+    __syncthreads();
+    return before + incl - v;
+}
+
 // Hash-table bins.  Symbolic (VALUES false: count the row's columns) or
 // numeric (VALUES true: accumulate, then write the row sorted by column).
 // A group of G threads per row, GROUPS groups per CTA, each with a table of
 // TS slots (keys, and values when VALUES), a list of the slots claimed (at
-// most TS / 2) and, for the sort, their keys.
-template <int TS, bool VALUES>
+// most TS / 2) and, for the sort, the sorted keys and slots and a bucket
+// histogram of G counters.
+//
+// The sort: the group finds the row's smallest and largest column, counts
+// the claimed keys into G buckets by where they fall in that range, and,
+// after a prefix sum of the counts, scatters them to their buckets; each
+// thread then sorts its own bucket by insertion (a few keys for columns
+// spread over the range).  When a bucket would hold more than
+// kSgBucketMax keys (columns clustered in a narrow part of the range) the
+// group sorts with the bitonic network instead.
+constexpr int kSgBucketMax = 48;
+
+template <int TS, int G, bool VALUES>
 __host__ __device__ constexpr size_t sg_group_smem(size_t vs) {
-    return (size_t)TS * sizeof(int) + (size_t)(TS / 2) * sizeof(int) * (VALUES ? 2 : 1) + (VALUES ? TS * vs : 0);
+    return (size_t)TS * sizeof(int) + (size_t)(TS / 2) * sizeof(int) * (VALUES ? 3 : 1) +
+           (VALUES ? G * sizeof(int) + TS * vs : 0);
 }
 
 template <typename V, int TS, int G, int GROUPS, bool VALUES>
@@ -270,16 +331,22 @@ sg_hash_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__restrict__ b_v
     constexpr int HALF = TS / 2;
     constexpr int kLog2TS = TS == 256 ? 8 : TS == 1024 ? 10 : TS == 2048 ? 11 : TS == 4096 ? 12 : 13;
     static_assert(1 << kLog2TS == TS, "table sizes are 256, 1024, 2048, 4096 or 8192");
+    static_assert(G == 32 || GROUPS == 1, "groups wider than a warp fill the CTA");
     extern __shared__ __align__(16) unsigned char sg_smem[];
     __shared__ int s_count[GROUPS];
+    __shared__ unsigned s_ua[8], s_ub[8];
+    __shared__ int s_ia[8], s_ib[8];
     const int t = threadIdx.x % G;
     const int grp = threadIdx.x / G;
-    // per group: vals [TS] (first, for alignment), keys [TS], slots [HALF], sorted keys [HALF]
-    unsigned char *base = sg_smem + (size_t)grp * sg_group_smem<TS, VALUES>(sizeof(V));
+    // per group: vals [TS] (first, for alignment), keys [TS], slots [HALF],
+    // sorted keys [HALF], sorted slots [HALF], bucket counters [G]
+    unsigned char *base = sg_smem + (size_t)grp * sg_group_smem<TS, G, VALUES>(sizeof(V));
     V *vals = VALUES ? reinterpret_cast<V *>(base) : nullptr;
     int *keys = reinterpret_cast<int *>(base + (VALUES ? TS * sizeof(V) : 0));
     int *slot = keys + TS;
     int *skey = slot + HALF;
+    int *sslot = skey + HALF;
+    int *hist = sslot + HALF;
     int *count = s_count + grp;
     for (int s = t; s < TS; s += G) {
         keys[s] = -1;
@@ -320,18 +387,64 @@ sg_hash_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__restrict__ b_v
         if (!VALUES) {
             if (live && t == 0) row_nnz[i] = claimed;
         } else {
-            int pw = 1;
-            while (pw < cnt) pw <<= 1;
-            for (int j = t; j < pw; j += G) skey[j] = j < cnt ? keys[slot[j]] : INT_MAX;
-            for (int j = cnt + t; j < pw; j += G) slot[j] = 0;
+            // the row's column range, then a histogram over G buckets of it
+            unsigned lo = 0xffffffffu, hi = 0u;
+            for (int j = t; j < cnt; j += G) {
+                const unsigned c = (unsigned)keys[slot[j]];
+                lo = min(lo, c);
+                hi = max(hi, c);
+            }
+            sg_group_minmax<G>(lo, hi, s_ua, s_ub);
+            const unsigned long long span = cnt > 0 ? (unsigned long long)(hi - lo) + 1ull : 1ull;
+            hist[t] = 0;
             sg_sync<G, GROUPS>(grp);
-            sg_sort<G, GROUPS>(skey, slot, pw, t, grp);
+            for (int j = t; j < cnt; j += G) {
+                const unsigned c = (unsigned)keys[slot[j]];
+                atomicAdd(hist + (int)((unsigned long long)(c - lo) * G / span), 1);
+            }
+            sg_sync<G, GROUPS>(grp);
+            const int mine = hist[t];
+            int biggest;
+            const int start = sg_group_scan<G>(mine, biggest, s_ia, s_ib);
+            if (biggest <= kSgBucketMax) {
+                hist[t] = start;  // the bucket's cursor
+                sg_sync<G, GROUPS>(grp);
+                for (int j = t; j < cnt; j += G) {
+                    const int sl = slot[j];
+                    const unsigned c = (unsigned)keys[sl];
+                    const int pos = atomicAdd(hist + (int)((unsigned long long)(c - lo) * G / span), 1);
+                    skey[pos] = (int)c;
+                    sslot[pos] = sl;
+                }
+                sg_sync<G, GROUPS>(grp);
+                for (int a = start + 1; a < start + mine; ++a) {  // insertion sort of my bucket
+                    const int key = skey[a], sl = sslot[a];
+                    int z = a - 1;
+                    while (z >= start && skey[z] > key) {
+                        skey[z + 1] = skey[z];
+                        sslot[z + 1] = sslot[z];
+                        --z;
+                    }
+                    skey[z + 1] = key;
+                    sslot[z + 1] = sl;
+                }
+            } else {  // clustered columns: the bitonic network
+                int pw = 1;
+                while (pw < cnt) pw <<= 1;
+                for (int j = t; j < pw; j += G) {
+                    skey[j] = j < cnt ? keys[slot[j]] : INT_MAX;
+                    sslot[j] = j < cnt ? slot[j] : 0;
+                }
+                sg_sync<G, GROUPS>(grp);
+                sg_sort<G, GROUPS>(skey, sslot, pw, t, grp);
+            }
+            sg_sync<G, GROUPS>(grp);
             if (live) {
                 const long long o = c_ptr[i], room = c_ptr[i + 1] - o;
                 if (t == 0 && claimed != room) atomicOr(error, 2);
                 for (int j = t; j < cnt && j < room; j += G) {
                     c_col[o + j] = skey[j];
-                    c_val[o + j] = vals[slot[j]];
+                    c_val[o + j] = vals[sslot[j]];
                 }
             }
             sg_sync<G, GROUPS>(grp);
@@ -574,7 +687,7 @@ cudaError_t sg_launch_hash(const SgCsr &mat, const void *a_val, const void *b_va
                            int64_t *row_nnz, const int64_t *c_ptr, int32_t *c_col, void *c_val, int32_t *error,
                            cudaStream_t stream) {
     if (nrows <= 0) return cudaSuccess;
-    const size_t smem = GROUPS * sg_group_smem<TS, VALUES>(sizeof(V));
+    const size_t smem = GROUPS * sg_group_smem<TS, G, VALUES>(sizeof(V));
     auto kern = sg_hash_kernel<V, TS, G, GROUPS, VALUES>;
     static bool attr_set = false;  // one value per instantiation
     if (!attr_set) {
