@@ -595,13 +595,15 @@ sg_dense_accumulate_kernel(SgCsr mat, const V *__restrict__ a_val, const V *__re
             const V sav = __shfl_sync(0xffffffffu, av, src);
             for (int r = r0 + lane; r < r1; r += 32) add(mat.b_col[r], VALUES ? sav * b_val[r] : V(0));
         }
-        __syncthreads();
-        const int nq = s_qn;
-        for (int jq = 0; jq < nq; ++jq)
-            for (int r = s_q0[jq] + t; r < s_q1[jq]; r += 256) add(mat.b_col[r], VALUES ? s_qa[jq] * b_val[r] : V(0));
-        __syncthreads();
-        if (t == 0) s_qn = 0;
-        __syncthreads();
+        if (__syncthreads_or(by_cta)) {  // (one barrier when no row of B is that long)
+            const int nq = s_qn;
+            for (int jq = 0; jq < nq; ++jq)
+                for (int r = s_q0[jq] + t; r < s_q1[jq]; r += 256)
+                    add(mat.b_col[r], VALUES ? s_qa[jq] * b_val[r] : V(0));
+            __syncthreads();
+            if (t == 0) s_qn = 0;
+            __syncthreads();
+        }
     }
 }
 
@@ -657,16 +659,33 @@ sg_dense_finish_kernel(SgDense d, int64_t j0, int64_t *__restrict__ row_nnz, con
         int64_t o = base + before;
 #pragma unroll
         for (int u = 0; u < WPT; ++u)
-            for (unsigned b = w[u]; b; b &= b - 1) {
-                const int64_t col = (q0 + u) * 32 + __ffs(b) - 1;
-                if (o < end) {
-                    c_col[o] = (int32_t)col;
-                    c_val[o] = dense[col];
-                } else {
-                    atomicOr(error, 2);
-                }
-                dense[col] = V(0);
-                ++o;
+            for (unsigned b = w[u]; b;) {
+                // up to four set bits at a time: four independent loads in flight
+                int64_t cs[4];
+                V vs[4];
+                int nb = 0;
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    if (b) {
+                        cs[z] = (q0 + u) * 32 + __ffs(b) - 1;
+                        b &= b - 1;
+                        nb = z + 1;
+                    }
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    if (z < nb) vs[z] = dense[cs[z]];
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    if (z < nb) {
+                        if (o < end) {
+                            c_col[o] = (int32_t)cs[z];
+                            c_val[o] = vs[z];
+                        } else {
+                            atomicOr(error, 2);
+                        }
+                        dense[cs[z]] = V(0);
+                        ++o;
+                    }
             }
     }
 #pragma unroll
