@@ -200,14 +200,25 @@ spmv_status_t spmv_execute(spmv_plan_t plan, double alpha, const void *x, double
 /*
  * Y = alpha * A * X + beta * Y for k right-hand sides ("A GPU
  * load-balancing programming model", section 4.3, Listing 4: the row loop
- * of SpMV with an inner loop over the columns of a dense matrix), on the
- * plan's merge-path partition.  X is n-by-k and Y m-by-k, device, row-major
- * with leading dimensions ldx >= k and ldy >= k (element (c, t) of X at
- * X[c*ldx + t]); value type of the plan.  alpha and beta as for
- * spmv_execute (beta == 0: Y is write-only).  X and Y must not overlap.
- * The plan must have been created with options.with_spmm != 0.  Columns
- * are processed 128 at a time (one launch each); asynchronous, allocates
- * nothing.  A plan must not run two products at once.
+ * of SpMV with an inner loop over the columns of a dense matrix).  X is
+ * n-by-k and Y m-by-k, device, row-major with leading dimensions ldx >= k
+ * and ldy >= k (element (c, t) of X at X[c*ldx + t]); value type of the
+ * plan.  alpha and beta as for spmv_execute (beta == 0: Y is write-only).
+ * X and Y must not overlap.  The plan must have been created with
+ * options.with_spmm != 0 (it then holds the merge-path partition, and the
+ * long-row lists the paths below need).
+ *
+ * The call takes the first path that applies: (1) over the plan's
+ * Row-grouped copy (groups of 32; long rows the copy leaves out, if at
+ * most one per 4096 rows, by a warp per 4096-nonzero segment), in slices
+ * of 32 (fp32) or 16 (fp64) columns; (2) for matrices whose rows have at
+ * most 64 nonzeros, or with rows of 65 or more at most one per 4096 rows
+ * and k <= 64 (fp32) / 32 (fp64): a warp per 32 rows straight from CSR,
+ * long rows by a warp per segment -- both need k a multiple of 16 bytes'
+ * worth of values and X, Y 16-byte aligned row by row; (3) otherwise the
+ * merge-path partition, 128 columns per launch.  Every path gives the
+ * same sums up to rounding order; none allocates; asynchronous.  A plan
+ * must not run two products at once.
  * Errors: INVALID_ARG (null plan or pointers, k < 0, ld < k, plan without
  * with_spmm), CUDA (launch failure).  k == 0 or m == 0 is a no-op.
  */
