@@ -708,14 +708,11 @@ cudaError_t sg_launch_hash(const SgCsr &mat, const void *a_val, const void *b_va
     if (nrows <= 0) return cudaSuccess;
     const size_t smem = GROUPS * sg_group_smem<TS, G, VALUES>(sizeof(V));
     auto kern = sg_hash_kernel<V, TS, G, GROUPS, VALUES>;
-    static bool attr_set = false;  // one value per instantiation
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // set on every launch: the setting belongs to the current device
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, G * GROUPS, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, G * GROUPS, smem);
     if (e != cudaSuccess) return e;
     long long grid = (nrows + GROUPS - 1) / GROUPS;
     const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
