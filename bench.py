@@ -27,6 +27,7 @@ import os
 import platform
 import shutil
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -117,8 +118,7 @@ class ClockSampler:
             self.err = "nvidia-smi not found"
             return
         sel = self._select(device_index)
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        self.path = os.path.join(tempfile.gettempdir(), f"spmv_clocks_{os.getpid()}.csv")
         self.fh = open(self.path, "w")
         self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                       "-lms", "50", "-i", sel], stdout=self.fh, stderr=subprocess.DEVNULL)

@@ -3,7 +3,7 @@
  *
  * TEST INFRASTRUCTURE ONLY.  Plain, single-threaded, obviously-correct C that
  * the tests, the smoke check and the benchmark's CPU-baseline leg use to
- * judge the CUDA path.  The product library never includes, links or calls
+ * check the CUDA path.  The product library never includes, links or calls
  * anything here, and nothing here includes or calls the product library.
  *
  * Sources (web pages on load-balanced CSR SpMV):
