@@ -776,8 +776,6 @@ cudaError_t sg_phase(const SpgemmArgs &a, const void *a_val, const void *b_val, 
 
 }  // namespace
 
-int spgemm_bin_of(int64_t products) { return sg_bin(products); }
-
 int64_t spgemm_chunks(int32_t m) {
     const int64_t c = ((int64_t)m + kSgChunk - 1) / kSgChunk;
     return c < 1 ? 1 : c;

@@ -8,7 +8,8 @@ namespace lbcsr {
 // ---------------------------------------------------------------- SpGEMM
 // C = A * B (A m-by-k, B k-by-n, CSR), OpSparse's two phases.  Rows of C
 // are binned by their products (the sum over the row of A of the lengths
-// of the rows of B it picks): bin b of spgemm_bin_of; bin_rows holds the
+// of the rows of B it picks): bins of at most 16, 128, 512, 1024, 2048 and
+// 4096 products, then the rest (the dense bin); bin_rows holds the
 // rows of bin 0, then bin 1, ... each in increasing order.  The last bin is
 // the dense one.
 constexpr int kSpgemmBins = 7;
@@ -37,7 +38,6 @@ struct SpgemmArgs {
     int64_t *dense_seg_scan;  // scan scratch for them
     int32_t *error;        // bit 1: a row of C outgrew its symbolic size
 };
-int spgemm_bin_of(int64_t products);
 int64_t spgemm_chunks(int32_t m);  // classification chunks; counts/offsets hold kSpgemmBins * chunks (+1)
 int64_t spgemm_piece_products();  // products per piece of the dense bin
 int64_t spgemm_segments(int32_t n);  // column segments per dense row when it is read back
