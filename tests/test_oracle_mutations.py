@@ -45,6 +45,10 @@ MUTATIONS = [
      [pins.test_spmv_transposed_equals_dense_product_exactly]),
     ("spgemm drops the last product of a row of B", "for (int32_t r = b_ptr[q]; r < b_ptr[q + 1]; ++r) {", "for (int32_t r = b_ptr[q]; r + 1 < b_ptr[q + 1]; ++r) {",
      [pins.test_spgemm_equals_dense_product_exactly]),
+    ("spgemm keeps only entries whose sum is nonzero", "                if (mark[j]) {  ", "                if (mark[j] && acc[j] != 0.0L) {",
+     [pins.test_spgemm_equals_dense_product_exactly]),
+    ("spgemm carries a row's sums into the next row", "                    acc[j] = 0.0L;  ", "                    acc[j] += 0.0L; ",
+     [pins.test_spgemm_equals_dense_product_exactly, pins.test_spgemm_with_identity_and_permutation]),
 ]
 
 
