@@ -39,6 +39,10 @@ MUTATIONS = [
      [pins.test_spmm_equals_dense_product_exactly]),
     ("spmm drops the beta term", "                    y += by;                                                                              \\", "                    y += 0;                                                                               \\",
      [pins.test_spmm_equals_dense_product_exactly]),
+    ("transpose lists a column's rows in decreasing order",
+     "        for (int32_t i = 0; i < m; ++i)                                                                   \\\n            for (int32_t q = row_ptr[i];",
+     "        for (int32_t i = m - 1; i >= 0; --i)                                                              \\\n            for (int32_t q = row_ptr[i];",
+     [pins.test_transpose_worked_example]),
     ("transpose keeps the row index of the column", "                t_idx[pos] = i;  ", "                t_idx[pos] = col_idx[q];  ",
      [pins.test_transpose_worked_example]),
     ("transposed product uses y index for x", "long double prod = (long double)vals[q] * (long double)x[i];", "long double prod = (long double)vals[q] * (long double)x[col_idx[q] % m];",
