@@ -45,13 +45,16 @@ SPEC_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def compulsory_bytes(A, beta: float) -> int:
-    """nnz*(4+s) + (m+1)*4 + n*s + m*s (+ m*s when beta != 0): every index and
-    value once, x once, y written once and read once only when beta != 0 (the
-    bytes-per-nonzero model of the Row-grouped CSR page, section 3, extended
-    by row_ptr, x and y)."""
+def compulsory_bytes(A, beta: float | None = None) -> int:
+    """B_c = nnz*(4+s) + (m+1)*4 + n*s + 2*m*s: every column index and value
+    once, row_ptr once, x once, y read and written once (the bytes-per-nonzero
+    model of the Row-grouped CSR page, section 3, extended by row_ptr, x and
+    y).  This is the roofline's byte count.  With beta given, the count the
+    product actually needs: y is only written when beta == 0 (BLAS
+    convention), so m*s fewer bytes."""
     s = A.vals.dtype.itemsize
-    return A.nnz * (4 + s) + (A.m + 1) * 4 + A.n * s + (2 if beta != 0 else 1) * A.m * s
+    y_bytes = 2 * A.m * s if beta is None or beta != 0 else A.m * s
+    return A.nnz * (4 + s) + (A.m + 1) * 4 + A.n * s + y_bytes
 
 
 def measured_peak():
@@ -99,6 +102,25 @@ def recorded_traffic(workload: str, kernel: str):
     if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None, None
     return e.get("dram_bytes_per_launch"), e.get("note")
+
+
+def roofline(bc: int, bc_beta: int, mean_us: float, workload: str, kernel: str) -> dict:
+    """The product's roofline entry: B_c (y read and written) over the mean
+    CUDA-event time of one product, against the measured copy bandwidth and
+    the 8 TB/s spec; frac_beta_aware uses the bytes the product needs (no y
+    read when beta == 0)."""
+    peak, peak_kind = measured_peak()
+    achieved = bc / (mean_us * 1e-6) / 1e9
+    achieved_b = bc_beta / (mean_us * 1e-6) / 1e9
+    traffic, traffic_note = recorded_traffic(workload, kernel)
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
+            "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
+            "frac_beta_aware": round(achieved_b / peak, 4), "traffic": traffic, "kernel": kernel,
+            "algorithmic_bytes_per_launch": int(bc), "beta_aware_bytes_per_launch": int(bc_beta)}
+    if traffic_note:
+        roof["traffic_note"] = traffic_note
+    return roof
 
 
 # ------------------------------------------------------------------ clocks
@@ -286,18 +308,11 @@ def run_gpu(args, workload_name: str) -> dict | None:
         return None
 
     ms_step = total_ms / K
-    bc = compulsory_bytes(A, W.beta)
+    bc = compulsory_bytes(A)
+    bc_beta = compulsory_bytes(A, W.beta)
     gflops = job_gflops(A.nnz, world, ms_step)
     mean_us = float(per.mean())
-    achieved = bc / (mean_us * 1e-6) / 1e9
-    peak, peak_kind = measured_peak()
-    traffic, traffic_note = recorded_traffic(workload_name, info["kernel_name"])
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
-            "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4), "traffic": traffic,
-            "kernel": info["kernel_name"], "algorithmic_bytes_per_launch": int(bc)}
-    if traffic_note:
-        roof["traffic_note"] = traffic_note
+    roof = roofline(bc, bc_beta, mean_us, workload_name, info["kernel_name"])
     out = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -307,7 +322,7 @@ def run_gpu(args, workload_name: str) -> dict | None:
                    "items_per_tile": info["items_per_tile"], "num_tiles": info["num_tiles"],
                    "l2": "inputs larger than L2, no flush (x stays L2-resident across steps)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-        "gbs_effective": round(achieved, 1),
+        "gbs_effective": roof["achieved"],
         "median_us": round(float(np.median(per)), 3), "p10_us": round(float(np.percentile(per, 10)), 3),
         "p90_us": round(float(np.percentile(per, 90)), 3), "compulsory_bytes": int(bc),
         "plan_ms": round(plan_ms, 3), "roofline": roof,
@@ -343,6 +358,117 @@ def oracle_sample(W, budget_s: float):
     rate = max(nnz_r, 1) / max(t, 1e-6)
     r = rows_for(rate * budget_s)
     return r, int(A.row_ptr[r])
+
+
+def copy_bandwidth(dev) -> float:
+    """Device copy bandwidth measured in this run: b.copy_(a) over 1 GiB of
+    bf16 (read + write bytes), best of 10, CUDA events -- the method of the
+    measured peak, repeated on this machine."""
+    import torch
+    a = torch.empty(1 << 29, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = float("inf")
+    for _ in range(12):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * (1 << 30) / (best * 1e-3) / 1e9
+
+
+def per_config_entry(name: str, dev, warmup: int, min_runs: int, min_seconds: float, cpu_budget: float,
+                     copy_gbs: float | None) -> dict:
+    """One workload with the plan's own kernel choice: median time per product
+    over at least min_runs runs (and at least min_seconds of them, so that the
+    clock sampler sees the timed region), one CUDA event pair per run, inputs
+    larger than L2 and no flush between runs; GFLOP/s = 2*nnz/t, GB/s =
+    B_c/t and the roofline fractions with t the median; the oracle on a
+    bounded sample of rows on one host core."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+    W = synth.workload(name)
+    A = W.A
+    vt = torch.float64 if A.dtype == "f64" else torch.float32
+    rp = torch.from_numpy(A.row_ptr).to(dev)
+    col = torch.from_numpy(A.col_idx).to(dev)
+    val = torch.from_numpy(A.vals).to(dev)
+    x = torch.from_numpy(W.x).to(dev)
+    y = torch.from_numpy(W.y0).to(dev) if W.y0 is not None else torch.zeros(A.m, dtype=vt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    plan = lb.Plan(rp, col, val, A.n)
+    torch.cuda.synchronize(dev)
+    plan_ms = (time.perf_counter() - t) * 1e3
+    info = plan.info()
+    for _ in range(max(warmup, 10)):
+        plan(x, y, W.alpha, W.beta, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(5):
+        plan(x, y, W.alpha, W.beta, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_us = e0.elapsed_time(e1) * 1e3 / 5
+    runs = int(min(5000, max(min_runs, min_seconds / max(est_us * 1e-6, 1e-7))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+    sampler = ClockSampler(dev.index or 0)
+    time.sleep(0.15)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for a, b in ev:
+        a.record(stream)
+        plan(x, y, W.alpha, W.beta, stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop(t0, time.time())
+    status = plan.device_status()
+    plan.close()
+    per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3
+    med = float(np.median(per))
+    bc, bc_beta = compulsory_bytes(A), compulsory_bytes(A, W.beta)
+    peak, peak_kind = measured_peak()
+    gbs = bc / (med * 1e-6) / 1e9
+    entry = {
+        "workload": name, "description": W.description, "kernel": info["kernel_name"], "dtype": A.dtype,
+        "m": A.m, "n": A.n, "nnz": A.nnz, "alpha": W.alpha, "beta": W.beta, "runs": runs, "warmup": max(warmup, 10),
+        "median_us": round(med, 3), "mean_us": round(float(per.mean()), 3),
+        "p10_us": round(float(np.percentile(per, 10)), 3), "p90_us": round(float(np.percentile(per, 90)), 3),
+        "gflops": round(2.0 * A.nnz / (med * 1e-6) / 1e9, 2), "gbs_effective": round(gbs, 1),
+        "roofline": {"bound": "hbm", "time": "median", "bytes": int(bc), "beta_aware_bytes": int(bc_beta),
+                     "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "peak_source": f"{peak_kind} copy bandwidth",
+                     "frac": round(gbs / peak, 4),
+                     "frac_beta_aware": round(bc_beta / (med * 1e-6) / 1e9 / peak, 4),
+                     "frac_of_spec_8tbs": round(gbs / SPEC_HBM_GBS, 4),
+                     "frac_of_copy_this_run": round(gbs / copy_gbs, 4) if copy_gbs else None,
+                     "meets_70pct": bool(gbs / peak >= 0.70)},
+        "plan_ms": round(plan_ms, 3), "launches_per_execute": info["launches_per_execute"],
+        "items_per_tile": info["items_per_tile"], "num_tiles": info["num_tiles"],
+        "device_status": status, "clocks": clocks,
+        "l2": "inputs larger than L2 (laplace2d_64 excepted), no flush between runs",
+    }
+    del rp, col, val, x, y
+    torch.cuda.empty_cache()
+    entry["cpu_baseline"] = cpu_baseline_leg(name, cpu_budget) if cpu_budget > 0 else None
+    return entry
+
+
+def run_per_config(args) -> dict:
+    """Every workload on one GPU (spec: each config's median time per
+    product, GFLOP/s, GB/s and roofline fractions, with the oracle beside
+    it)."""
+    import torch
+    _, _, local = dist_env()
+    dev = torch.device("cuda", local)
+    copy_gbs = copy_bandwidth(dev)
+    entries = [per_config_entry(name, dev, args.warmup, 100, 0.3, args.per_config_cpu_budget, copy_gbs)
+               for name in synth.WORKLOADS]
+    return {"copy_gbs_this_run": round(copy_gbs, 1), "configs": entries}
 
 
 def run_reference(args, workload_name: str) -> dict | None:
@@ -563,6 +689,62 @@ def run_spgemm(args, workload_name: str) -> dict | None:
     }
 
 
+def run_gather(args, workload_name: str) -> dict | None:
+    """Ceilings of the x gather on the workload's column pattern, by load
+    path (spmv_gather_ceiling): the columns and the gathered values only, no
+    matrix values, no floating-point work.  Each path is timed with CUDA
+    events over args.steps launches after args.warmup; `gathers_per_sm_clk`
+    divides the gathers by the SM count and the sampled SM clock."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    W = synth.workload(workload_name)
+    A = W.A
+    col = torch.from_numpy(A.col_idx).to(dev)
+    x = torch.from_numpy(W.x).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    xb = W.x.view(np.uint64 if A.dtype == "f64" else np.uint32)
+    want = int(np.sum(xb[A.col_idx].astype(np.uint64), dtype=np.uint64))
+    want_stream = int(np.sum(A.col_idx.astype(np.uint64), dtype=np.uint64))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {}
+    sampler = ClockSampler(local)
+    time.sleep(0.15)
+    t0 = time.time()
+    for path in lb.GATHER_PATHS:
+        cs = torch.zeros(1, dtype=torch.int64, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        lb.gather_ceiling(path, col, x, cs, err, stream)
+        torch.cuda.synchronize(dev)
+        ok = (int(cs.item()) & (2**64 - 1)) == (want_stream if path == "stream" else want) and int(err.item()) == 0
+        for _ in range(args.warmup):
+            lb.gather_ceiling(path, col, x, cs, err, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        for a, b in ev:
+            a.record(stream)
+            lb.gather_ceiling(path, col, x, cs, err, stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3
+        res[path] = {"median_us": round(float(np.median(per)), 2), "checksum_ok": bool(ok)}
+    clocks = sampler.stop(t0, time.time())
+    mhz = clocks.get("sm_mhz") or 2070.0
+    for path, r in res.items():
+        if path != "stream":
+            r["gathers_per_sm_clk"] = round(A.nnz / (r["median_us"] * 1e-6) / (sms * mhz * 1e6), 3)
+    return {"metric": "x-gather ceiling by load path (columns + gathers only)", "unit": "us",
+            "higher_is_better": False, "dtype": A.dtype, "data": "synthetic",
+            "config": {"workload": workload_name, "nnz": A.nnz, "n": A.n, "steps": args.steps,
+                       "warmup": args.warmup, "sms": sms},
+            "paths": res, "clocks": clocks}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -578,11 +760,17 @@ def main():
     ap.add_argument("--rhs", type=int, default=0, help="k > 0: time SpMM with k right-hand sides instead")
     ap.add_argument("--transposed", action="store_true", help="time the transposed product A^T x instead")
     ap.add_argument("--spgemm", action="store_true", help="time SpGEMM C = A*A instead")
+    ap.add_argument("--gather-only", action="store_true",
+                    help="time the x gather alone on the workload's columns, by load path")
     ap.add_argument("--scale", type=int, default=1,
                     help="SpGEMM only: shrink the workload by this factor (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload block (default run, N = 1 only)")
+    ap.add_argument("--per-config-cpu-budget", type=float, default=3.0,
+                    help="seconds of oracle time per workload in the per-config block")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -600,6 +788,11 @@ def main():
         dist.init_process_group("nccl")
     names = synth.WORKLOADS if args.all else [args.workload]
     for name in names:
+        if args.gather_only:
+            out = run_gather(args, name)
+            if out is not None:
+                print(json.dumps(out), flush=True)
+            continue
         out = run_spgemm(args, name) if args.spgemm else run_spmm(args, name) if args.rhs > 0 else \
             run_gpu(args, name)
         if out is not None:
@@ -607,6 +800,9 @@ def main():
             out["cpu_baseline"] = cpu_baseline_leg(name, args.cpu_budget) \
                 if world == 1 and not args.no_cpu_baseline and not args.spgemm else None
             out["source_hash"] = kernel_source_hash()
+            if world == 1 and not args.no_per_config and not args.all and args.rhs == 0 and not args.spgemm \
+                    and not args.transposed and args.kernel == "auto":
+                out["per_config"] = run_per_config(args)
             print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

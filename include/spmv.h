@@ -299,6 +299,46 @@ spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz, const int3
 spmv_status_t spmv_plan_device_status(spmv_plan_t plan, int32_t *flags);
 
 /*
+ * Diagnostic: the ceiling of the x gather for a column pattern, by load
+ * path.  The Row-grouped CSR page (sections 3 and 4) names the gather of x
+ * as what limits SpMV once the matrix stream is coalesced (x through the
+ * texture cache gave 1.3-1.8x); this call measures how fast each of the
+ * GPU's load paths can gather x[col_idx[k]] for k = 0 .. nnz-1, with no
+ * matrix values and no floating-point work, so that a kernel's time can be
+ * set against the best one.
+ *
+ * path (spmv_gather_path_t): STREAM reads col_idx only; L1 gathers through
+ * the read-only path (ld.global.nc); L2 through L2 only (ld.global.cg);
+ * BULK16 by one 16-byte Tensor Memory Accelerator copy per gather into
+ * shared memory; TMA4 by tile::gather4 tensor copies (x viewed as rows of
+ * 32 bytes, four rows per instruction); L1_TMA4 half by L1, half by TMA4;
+ * L1_TMA4_QUARTER three quarters by L1, one by TMA4; TMA4_16 as TMA4 over
+ * rows of 16 bytes.
+ * col_idx[nnz] (device, int32, each in [0, n)), x[n] (device, dtype; 16-byte
+ * aligned for the copy paths, BULK16 to TMA4_16, which also need
+ * n * sizeof(value) >= 32).  *checksum (device uint64, zeroed by the caller) receives the sum,
+ * modulo 2^64, of the bit patterns of the gathered values (the same for
+ * every path except STREAM, which sums the columns instead).  *error
+ * (device int32, zeroed by the caller): bit 0 is set if a copy did not
+ * complete within about a second.  Asynchronous on `stream`; allocates
+ * nothing.  Errors: INVALID_ARG; UNSUPPORTED when x is misaligned for the
+ * path or the tensor-map encoder is unavailable; CUDA on launch failure.
+ */
+typedef enum {
+    SPMV_GATHER_STREAM = 0,
+    SPMV_GATHER_L1 = 1,
+    SPMV_GATHER_L2 = 2,
+    SPMV_GATHER_BULK16 = 3,
+    SPMV_GATHER_TMA4 = 4,
+    SPMV_GATHER_L1_TMA4 = 5,
+    SPMV_GATHER_L1_TMA4_QUARTER = 6,
+    SPMV_GATHER_TMA4_16 = 7
+} spmv_gather_path_t;
+
+spmv_status_t spmv_gather_ceiling(int32_t path, int32_t nnz, const int32_t *col_idx, int32_t n, const void *x,
+                                  spmv_dtype_t dtype, uint64_t *checksum, int32_t *error, spmv_stream_t stream);
+
+/*
  * Sparse times sparse, C = A * B, after OpSparse ("OpSparse: a highly
  * optimized framework for sparse general matrix multiplication on GPUs",
  * sections 3 and 5): Gustavson's row-by-row product (row i of C sums, over

@@ -16,7 +16,8 @@ import os
 
 from . import _build
 
-__all__ = ["Plan", "SpGEMM", "spgemm", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions"]
+__all__ = ["Plan", "SpGEMM", "spgemm", "SpmvError", "lib", "KERNELS", "EXPORTS", "header_functions",
+           "gather_ceiling", "GATHER_PATHS"]
 
 KERNELS = {"auto": 0, "merge_path": 1, "thread_row": 2, "rgcsr": 3, "long_rows": 4, "rgcsr_sorted": 5,
            "group_mapped": 6}
@@ -105,6 +106,7 @@ def lib() -> ctypes.CDLL:
             "spmv_spgemm_info": [vp, ctypes.POINTER(SpgemmInfo)],
             "spmv_spgemm_device_status": [vp, ctypes.POINTER(i32)],
             "spmv_spgemm_destroy": [vp],
+            "spmv_gather_ceiling": [i32, i32, vp, i32, vp, ctypes.c_int, vp, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -373,3 +375,23 @@ def spgemm(a_row_ptr, a_col_idx, a_vals, b_row_ptr, b_col_idx, b_vals, n: int, s
     """C = A*B in one call: (row_ptr, col_idx, vals) CUDA tensors."""
     with SpGEMM(a_row_ptr, a_col_idx, b_row_ptr, b_col_idx, n, a_vals.dtype, stream=stream) as h:
         return h.compute(a_vals, b_vals, stream=stream)
+
+
+GATHER_PATHS = {"stream": 0, "l1": 1, "l2": 2, "bulk16": 3, "tma4": 4, "l1_tma4": 5, "l1_tma4_quarter": 6,
+                "tma4_16": 7}
+
+
+def gather_ceiling(path: str, col_idx, x, checksum, error, stream=None) -> None:
+    """Diagnostic: gather x[col_idx[k]] for every k by one load path and add
+    the values' bit patterns into ``checksum`` (a zeroed CUDA int64 tensor of
+    one element; ``error`` likewise, int32).  Asynchronous on ``stream``."""
+    import torch
+    if col_idx.dtype != torch.int32 or not col_idx.is_cuda or not col_idx.is_contiguous():
+        raise TypeError("col_idx must be a contiguous CUDA int32 tensor")
+    if not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous CUDA tensor")
+    if checksum.dtype != torch.int64 or error.dtype != torch.int32:
+        raise TypeError("checksum must be int64 and error int32")
+    check(lib().spmv_gather_ceiling(GATHER_PATHS[path], col_idx.numel(), _ptr(col_idx), x.numel(), _ptr(x),
+                                    _dtype_code(x), checksum.data_ptr(), error.data_ptr(), _stream_handle(stream)),
+          f"spmv_gather_ceiling({path})")

@@ -11,13 +11,24 @@ import synth
 
 def test_compulsory_bytes_by_hand():
     # 3 x 5, rows of 2, 0 and 3 nonzeros, fp32: indices and values 5 * (4 + 4),
-    # row_ptr 4 * 4, x 5 * 4, y written 3 * 4 (and read 3 * 4 more when beta != 0)
+    # row_ptr 4 * 4, x 5 * 4, y read and written 2 * 3 * 4 (the roofline's
+    # count); the beta-aware count drops the y read when beta == 0
     A = synth.CSR(3, 5, np.array([0, 2, 2, 5], np.int32), np.array([0, 4, 1, 2, 3], np.int32),
                   np.ones(5, np.float32))
+    assert bench.compulsory_bytes(A) == 40 + 16 + 20 + 24
     assert bench.compulsory_bytes(A, 0.0) == 40 + 16 + 20 + 12
     assert bench.compulsory_bytes(A, 0.5) == 40 + 16 + 20 + 24
     B = synth.CSR(3, 5, A.row_ptr, A.col_idx, np.ones(5, np.float64))
+    assert bench.compulsory_bytes(B) == 5 * 12 + 16 + 40 + 48
     assert bench.compulsory_bytes(B, 0.0) == 5 * 12 + 16 + 40 + 24
+
+
+def test_roofline_fractions():
+    # 1e9 bytes in 1e6 us (1 s) is 1 GB/s; the beta-aware count is half of it
+    r = bench.roofline(10**9, 5 * 10**8, 10**6, "none", "none")
+    assert r["achieved"] == 1.0 and r["unit"] == "GB/s"
+    assert abs(r["frac"] - 1.0 / r["peak"]) < 1e-4
+    assert abs(r["frac_beta_aware"] - 0.5 / r["peak"]) < 1e-4
 
 
 def _info(kernel, m, num_long=0, max_len=8, group=32):
