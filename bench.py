@@ -706,10 +706,12 @@ def run_gather(args, workload_name: str) -> dict | None:
     W = synth.workload(workload_name)
     A = W.A
     col = torch.from_numpy(A.col_idx).to(dev)
+    vals = torch.from_numpy(A.vals).to(dev)
     x = torch.from_numpy(W.x).to(dev)
     stream = torch.cuda.current_stream(dev)
-    xb = W.x.view(np.uint64 if A.dtype == "f64" else np.uint32)
-    want = int(np.sum(xb[A.col_idx].astype(np.uint64), dtype=np.uint64))
+    ut = np.uint64 if A.dtype == "f64" else np.uint32
+    want = int(np.sum(W.x.view(ut)[A.col_idx].astype(np.uint64), dtype=np.uint64))
+    want_vals = (want + int(np.sum(A.vals.view(ut).astype(np.uint64), dtype=np.uint64))) & (2**64 - 1)
     want_stream = int(np.sum(A.col_idx.astype(np.uint64), dtype=np.uint64))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
@@ -719,16 +721,17 @@ def run_gather(args, workload_name: str) -> dict | None:
     for path in lb.GATHER_PATHS:
         cs = torch.zeros(1, dtype=torch.int64, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
-        lb.gather_ceiling(path, col, x, cs, err, stream)
+        lb.gather_ceiling(path, col, x, cs, err, stream, vals=vals)
         torch.cuda.synchronize(dev)
-        ok = (int(cs.item()) & (2**64 - 1)) == (want_stream if path == "stream" else want) and int(err.item()) == 0
+        expect = want_stream if path == "stream" else want_vals if path in lb.GATHER_WITH_VALUES else want
+        ok = (int(cs.item()) & (2**64 - 1)) == expect and int(err.item()) == 0
         for _ in range(args.warmup):
-            lb.gather_ceiling(path, col, x, cs, err, stream)
+            lb.gather_ceiling(path, col, x, cs, err, stream, vals=vals)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         torch.cuda.synchronize(dev)
         for a, b in ev:
             a.record(stream)
-            lb.gather_ceiling(path, col, x, cs, err, stream)
+            lb.gather_ceiling(path, col, x, cs, err, stream, vals=vals)
             b.record(stream)
         torch.cuda.synchronize(dev)
         per = np.array([a.elapsed_time(b) for a, b in ev]) * 1e3

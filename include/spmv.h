@@ -136,6 +136,9 @@ typedef struct {
     int64_t rgcsr_slots;          /* slots of the Row-grouped copy (group_ptr[last]) */
     int32_t transposed_kernel;    /* spmv_kernel_t of the plan for A^T (-1: none) */
     int32_t transposed_launches;  /* kernel launches one spmv_execute_transposed issues */
+    int64_t merge_path_warps;     /* merge-path kernel: warps W, each owning a contiguous run of
+                                     about num_tiles / W tiles (for 16-byte aligned arrays; 0 when
+                                     the plan runs another kernel) */
 } spmv_plan_info_t;
 
 /* What spmv_plan_export copies out. */
@@ -272,23 +275,36 @@ spmv_status_t spmv_plan_export(spmv_plan_t plan, spmv_export_t what, void *dst, 
  * streams.
  *
  * Arguments as spmv_plan_create plus spmv_execute (device arrays, the
- * caller's stream).  It runs the merge-path kernel with its scratch in one
- * fixed-size array (about 7.3 MB) inside the library's device image, which
- * every GPU that loads the library holds until the process exits.  Limit:
- * ceil((m + nnz) / 1024) <= 262,144 tiles, i.e. m + nnz <= 268,435,456;
- * larger sizes return SPMV_ERR_INVALID_ARG.  The matrix is NOT checked (use spmv_plan_create
- * once to validate it); invalid indices give undefined results.
- * All calls share the scratch array and each call clears what must start
- * at zero, so calls that overlap on the GPU (two streams, two host threads)
- * race.  The first call on a device looks up the array's device address;
- * make that first call before any stream capture.  Asynchronous otherwise.
- * Returns SPMV_OK, SPMV_ERR_INVALID_ARG or SPMV_ERR_CUDA (no message is set
- * for spmv_last_error).
+ * caller's stream).  It runs the merge-path kernel (tiles of 384 rows plus
+ * nonzeros) with its scratch in one fixed-size array (about 6 MB) inside the
+ * library's device image, which every GPU that loads the library holds
+ * until the process exits.  Limit: m + nnz <= 2^28 = 268,435,456; larger
+ * sizes return SPMV_ERR_INVALID_ARG.  The matrix is NOT checked (use
+ * spmv_plan_create once to validate it); invalid indices give undefined
+ * results.  All calls share the scratch array and each call clears what must
+ * start at zero, so calls that overlap on the GPU (two streams, two host
+ * threads) race.  Every call looks up the array's device address (a host
+ * table lookup once the library's module is loaded on the device); the first
+ * call on a device loads that module, so make it before any stream capture.
+ * Asynchronous otherwise.  A tile copy that does not complete within about a
+ * second stops that part of the product and sets a flag that
+ * spmv_noalloc_device_status reports.  Returns SPMV_OK, SPMV_ERR_INVALID_ARG
+ * or SPMV_ERR_CUDA (no message is set for spmv_last_error).
  */
 spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz, const int32_t *row_ptr,
                                    const int32_t *col_idx, const void *vals, spmv_dtype_t dtype,
                                    double alpha, const void *x, double beta, void *y,
                                    spmv_stream_t stream);
+
+/*
+ * Kernel-side failure flags of the last spmv_execute_noalloc on the current
+ * device (HOST *flags; waits for the whole device, so not during a stream
+ * capture; allocates nothing).  0 = no failure; bit 0: a tile copy did not
+ * complete within about a second, and that product's y is incomplete.  The
+ * pages have no counterpart.  Returns SPMV_OK, SPMV_ERR_INVALID_ARG or
+ * SPMV_ERR_CUDA.
+ */
+spmv_status_t spmv_noalloc_device_status(int32_t *flags);
 
 /*
  * Kernel-side failure flags of a plan (HOST *flags; waits for the device).
@@ -313,7 +329,18 @@ spmv_status_t spmv_plan_device_status(spmv_plan_t plan, int32_t *flags);
  * shared memory; TMA4 by tile::gather4 tensor copies (x viewed as rows of
  * 32 bytes, four rows per instruction); L1_TMA4 half by L1, half by TMA4;
  * L1_TMA4_QUARTER three quarters by L1, one by TMA4; TMA4_16 as TMA4 over
- * rows of 16 bytes.
+ * rows of 16 bytes.  Three paths also stream the values vals[nnz] (device,
+ * dtype) beside the L1 gathers, to measure what bringing in the matrix
+ * costs the gathers: STREAM_LDG by coalesced loads, STREAM_BULK by one bulk
+ * copy per 256 nonzeros and array into shared memory, STREAM_CPASYNC by
+ * 16-byte cp.async (both need col_idx and vals 16-byte aligned),
+ * STREAM_LDG_OCC as STREAM_LDG with the staged paths' shared memory reserved
+ * (as many warps per SM), STREAM_LDG_STS by coalesced loads that the lanes
+ * store to shared memory and read back, STREAM_LDG_FEW as STREAM_LDG with no
+ * shared memory but only as many CTAs per SM as the staged paths fit,
+ * STREAM_LDG_RES_1 .. _6 as STREAM_LDG with 4 CTAs per SM and 32, 64, ...,
+ * 192 KB of shared memory reserved per SM (the L1 left to the gathers);
+ * their checksum adds the values' bit patterns too.
  * col_idx[nnz] (device, int32, each in [0, n)), x[n] (device, dtype; 16-byte
  * aligned for the copy paths, BULK16 to TMA4_16, which also need
  * n * sizeof(value) >= 32).  *checksum (device uint64, zeroed by the caller) receives the sum,
@@ -332,11 +359,20 @@ typedef enum {
     SPMV_GATHER_TMA4 = 4,
     SPMV_GATHER_L1_TMA4 = 5,
     SPMV_GATHER_L1_TMA4_QUARTER = 6,
-    SPMV_GATHER_TMA4_16 = 7
+    SPMV_GATHER_TMA4_16 = 7,
+    SPMV_GATHER_STREAM_LDG = 8,
+    SPMV_GATHER_STREAM_BULK = 9,
+    SPMV_GATHER_STREAM_CPASYNC = 10,
+    SPMV_GATHER_STREAM_LDG_OCC = 11,
+    SPMV_GATHER_STREAM_LDG_STS = 12,
+    SPMV_GATHER_STREAM_LDG_FEW = 13,
+    SPMV_GATHER_STREAM_LDG_RES_1 = 14, /* .. _RES_6 = 19 */
+    SPMV_GATHER_STREAM_LDG_RES_6 = 19
 } spmv_gather_path_t;
 
 spmv_status_t spmv_gather_ceiling(int32_t path, int32_t nnz, const int32_t *col_idx, int32_t n, const void *x,
-                                  spmv_dtype_t dtype, uint64_t *checksum, int32_t *error, spmv_stream_t stream);
+                                  const void *vals, spmv_dtype_t dtype, uint64_t *checksum, int32_t *error,
+                                  spmv_stream_t stream);
 
 /*
  * Sparse times sparse, C = A * B, after OpSparse ("OpSparse: a highly

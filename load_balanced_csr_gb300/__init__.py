@@ -55,7 +55,8 @@ class PlanInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64), ("stats", RowStats),
                 ("long_row_min", ctypes.c_int32), ("long_segment_nnz", ctypes.c_int32),
                 ("num_long_segments", ctypes.c_int64), ("rgcsr_slots", ctypes.c_int64),
-                ("transposed_kernel", ctypes.c_int32), ("transposed_launches", ctypes.c_int32)]
+                ("transposed_kernel", ctypes.c_int32), ("transposed_launches", ctypes.c_int32),
+                ("merge_path_warps", ctypes.c_int64)]
 
 
 class SpgemmInfo(ctypes.Structure):
@@ -98,6 +99,7 @@ def lib() -> ctypes.CDLL:
             "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
             "spmv_plan_device_status": [vp, ctypes.POINTER(i32)],
             "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
+            "spmv_noalloc_device_status": [ctypes.POINTER(i32)],
             "spmv_execute_multi": [vp, i32, dbl, vp, ctypes.c_int64, dbl, vp, ctypes.c_int64, vp],
             "spmv_execute_transposed": [vp, dbl, vp, dbl, vp, vp],
             "spmv_spgemm_create": [ctypes.POINTER(vp), i32, i32, i32, i32, vp, vp, i32, vp, vp, ctypes.c_int,
@@ -106,7 +108,7 @@ def lib() -> ctypes.CDLL:
             "spmv_spgemm_info": [vp, ctypes.POINTER(SpgemmInfo)],
             "spmv_spgemm_device_status": [vp, ctypes.POINTER(i32)],
             "spmv_spgemm_destroy": [vp],
-            "spmv_gather_ceiling": [i32, i32, vp, i32, vp, ctypes.c_int, vp, vp, vp],
+            "spmv_gather_ceiling": [i32, i32, vp, i32, vp, vp, ctypes.c_int, vp, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -378,13 +380,17 @@ def spgemm(a_row_ptr, a_col_idx, a_vals, b_row_ptr, b_col_idx, b_vals, n: int, s
 
 
 GATHER_PATHS = {"stream": 0, "l1": 1, "l2": 2, "bulk16": 3, "tma4": 4, "l1_tma4": 5, "l1_tma4_quarter": 6,
-                "tma4_16": 7}
+                "tma4_16": 7, "stream_ldg": 8, "stream_bulk": 9, "stream_cpasync": 10, "stream_ldg_occ": 11,
+                "stream_ldg_sts": 12, "stream_ldg_few": 13, **{f"stream_ldg_res{32 * k}k": 13 + k for k in range(1, 7)}}
+GATHER_WITH_VALUES = tuple(k for k in GATHER_PATHS if k.startswith("stream_"))
 
 
-def gather_ceiling(path: str, col_idx, x, checksum, error, stream=None) -> None:
+def gather_ceiling(path: str, col_idx, x, checksum, error, stream=None, vals=None) -> None:
     """Diagnostic: gather x[col_idx[k]] for every k by one load path and add
     the values' bit patterns into ``checksum`` (a zeroed CUDA int64 tensor of
-    one element; ``error`` likewise, int32).  Asynchronous on ``stream``."""
+    one element; ``error`` likewise, int32).  The paths in
+    GATHER_WITH_VALUES also stream ``vals`` (nnz entries of x's type) and add
+    their bit patterns.  Asynchronous on ``stream``."""
     import torch
     if col_idx.dtype != torch.int32 or not col_idx.is_cuda or not col_idx.is_contiguous():
         raise TypeError("col_idx must be a contiguous CUDA int32 tensor")
@@ -392,6 +398,10 @@ def gather_ceiling(path: str, col_idx, x, checksum, error, stream=None) -> None:
         raise TypeError("x must be a contiguous CUDA tensor")
     if checksum.dtype != torch.int64 or error.dtype != torch.int32:
         raise TypeError("checksum must be int64 and error int32")
+    if path in GATHER_WITH_VALUES and (vals is None or vals.dtype != x.dtype or vals.numel() != col_idx.numel()
+                                       or not vals.is_cuda or not vals.is_contiguous()):
+        raise TypeError("this path needs vals: a contiguous CUDA tensor of x's type with one entry per column")
     check(lib().spmv_gather_ceiling(GATHER_PATHS[path], col_idx.numel(), _ptr(col_idx), x.numel(), _ptr(x),
-                                    _dtype_code(x), checksum.data_ptr(), error.data_ptr(), _stream_handle(stream)),
+                                    _ptr(vals) if vals is not None else None, _dtype_code(x), checksum.data_ptr(),
+                                    error.data_ptr(), _stream_handle(stream)),
           f"spmv_gather_ceiling({path})")

@@ -36,19 +36,38 @@ def _inputs() -> list[str]:
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def stale() -> bool:
+STAMP = os.path.join(OBJDIR, "flags.txt")
+
+
+def _flags_used() -> str | None:
+    try:
+        with open(STAMP) as f:
+            return f.read()
+    except OSError:
+        return None
+
+
+def stale(extra: list[str] | None = None) -> bool:
+    """The library is missing, older than a source, or built with other
+    extra nvcc flags."""
     if not os.path.exists(LIB):
+        return True
+    if (_flags_used() or "") != " ".join(extra or []):
         return True
     t = os.path.getmtime(LIB)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and not stale():
+    """Compile every source for sm_103a and link libspmv.so.  Extra nvcc
+    flags come from `extra` and the SPMV_NVCC_EXTRA environment variable
+    (compile-time tuning parameters, e.g. -DLBCSR_MP_STAGES=1)."""
+    extra = (extra or []) + os.environ.get("SPMV_NVCC_EXTRA", "").split()
+    if not force and not stale(extra):
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + ARCH + ["-I", INCLUDE, "-I", CSRC] + (extra or [])
+    flags = NVCC_FLAGS + ARCH + ["-I", INCLUDE, "-I", CSRC] + extra
 
     def compile_one(src: str) -> str:
         obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
@@ -70,6 +89,8 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
         os.replace(tmp, LIB)
+        with open(STAMP, "w") as f:
+            f.write(" ".join(extra))
     finally:
         if os.path.exists(tmp):
             os.unlink(tmp)

@@ -127,6 +127,60 @@ spmv_status_t cuda_fail(cudaError_t e, const char *what) {
     return fail(SPMV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+
+// ---------------------------------------------------------------- fault injection
+// Host-side failures injected into plan and SpGEMM-handle creation, so that
+// tests can walk every clean-up path without faulting a GPU.  With
+// SPMV_FAULT=alloc:N the N-th device allocation of a creation call fails as
+// if the device were out of memory; with SPMV_FAULT=launch:N its N-th launch
+// step reports a launch failure without launching anything.  The variable
+// is read at the start of each creation call and counts on the calling
+// thread; unset (the normal case) it costs one getenv per creation.
+struct FaultPlan {
+    int kind = 0;  // 1: allocation, 2: launch step
+    long long at = 0;
+    long long allocs = 0, launches = 0;
+};
+thread_local FaultPlan g_fault;
+
+void fault_arm() {
+    g_fault = FaultPlan{};
+    const char *v = getenv("SPMV_FAULT");
+    if (!v) return;
+    if (!strncmp(v, "alloc:", 6)) g_fault.kind = 1, g_fault.at = atoll(v + 6);
+    else if (!strncmp(v, "launch:", 7)) g_fault.kind = 2, g_fault.at = atoll(v + 7);
+}
+
+template <typename T>
+cudaError_t dev_malloc(T **ptr, size_t bytes) {
+    if (g_fault.kind == 1 && ++g_fault.allocs == g_fault.at) {
+        *ptr = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(reinterpret_cast<void **>(ptr), bytes);
+}
+
+bool launch_fault() { return g_fault.kind == 2 && ++g_fault.launches == g_fault.at; }
+
+// Arms the injection for one creation call and disarms it on return (a
+// plan's creation of the plan for its transpose counts as part of it).
+thread_local int g_fault_depth = 0;
+struct FaultScope {
+    FaultScope() {
+        if (g_fault_depth++ == 0) fault_arm();
+    }
+    ~FaultScope() {
+        if (--g_fault_depth == 0) g_fault = FaultPlan{};
+    }
+};
+
+}  // namespace
+
+// A launch step of a creation call (the injected failure skips the launch).
+#define LAUNCH(call) (launch_fault() ? cudaErrorLaunchFailure : (call))
+
+namespace {
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 size_t value_size(spmv_dtype_t d) { return d == SPMV_F64 ? 8 : 4; }
@@ -209,6 +263,13 @@ void destroy_plan(spmv_plan_s *p) {
 
 constexpr int32_t kDefaultLongRowMin = 512;
 
+// A creation call that fails after launching work waits for that work
+// before it frees the memory the work writes.
+void abandon_plan(spmv_plan_s *p, cudaStream_t stream) {
+    cudaStreamSynchronize(stream);
+    destroy_plan(p);
+}
+
 // The long-row list and, for the Row-grouped kernel, its layout and copy of
 // A.  Two passes over row_ptr per structure, sized on the host from the
 // statistics where they bound it, read back where they do not.
@@ -254,7 +315,7 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
     const size_t o_gp = take(rgcsr ? sizeof(int64_t) * (p->ngroups + 1) : 0);
     const size_t o_scr = take(sizeof(int64_t) * scan_scratch_elems(scan_n));
     p->aux_bytes = off;
-    cudaError_t e = cudaMalloc(&p->aux, p->aux_bytes);
+    cudaError_t e = dev_malloc(&p->aux, p->aux_bytes);
     if (e != cudaSuccess) {
         p->aux = nullptr;
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the row-kernel workspace: ") + cudaGetErrorString(e));
@@ -280,12 +341,12 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
     int64_t sizes[3] = {0, 0, 0};
     if (long_ub > 0) e = cudaMemsetAsync(p->long_arrivals, 0, sizeof(int32_t) * long_ub, stream);
     if (e == cudaSuccess && has_long) {
-        e = launch_long_rows_count(m, p->row_ptr, p->long_min, chunk_rows, chunk_segs, stream);
-        if (e == cudaSuccess) e = launch_exclusive_scan(chunk_rows, nc, chunk_row_off, scratch, stream);
-        if (e == cudaSuccess) e = launch_exclusive_scan(chunk_segs, nc, chunk_seg_off, scratch, stream);
+        e = LAUNCH(launch_long_rows_count(m, p->row_ptr, p->long_min, chunk_rows, chunk_segs, stream));
+        if (e == cudaSuccess) e = LAUNCH(launch_exclusive_scan(chunk_rows, nc, chunk_row_off, scratch, stream));
+        if (e == cudaSuccess) e = LAUNCH(launch_exclusive_scan(chunk_segs, nc, chunk_seg_off, scratch, stream));
         if (e == cudaSuccess)
-            e = launch_long_rows_scatter(m, p->row_ptr, p->long_min, chunk_row_off, chunk_seg_off, p->long_rows,
-                                         p->seg_begin, stream);
+            e = LAUNCH(launch_long_rows_scatter(m, p->row_ptr, p->long_min, chunk_row_off, chunk_seg_off, p->long_rows,
+                                         p->seg_begin, stream));
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(&sizes[0], chunk_row_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
         if (e == cudaSuccess)
@@ -293,11 +354,11 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
     }
     if (e == cudaSuccess && rgcsr && m > 0) {
         if (sorted)
-            e = launch_window_sort(m, p->row_ptr, has_long ? p->long_min : 0, p->perm, p->row_len, gsize, stream);
+            e = LAUNCH(launch_window_sort(m, p->row_ptr, has_long ? p->long_min : 0, p->perm, p->row_len, gsize, stream));
         else
-            e = launch_rgcsr_lengths(m, p->row_ptr, p->g_log2, has_long ? p->long_min : 0, p->row_len, gsize,
-                                     stream);
-        if (e == cudaSuccess) e = launch_exclusive_scan(gsize, p->ngroups, p->group_ptr, scratch, stream);
+            e = LAUNCH(launch_rgcsr_lengths(m, p->row_ptr, p->g_log2, has_long ? p->long_min : 0, p->row_len, gsize,
+                                     stream));
+        if (e == cudaSuccess) e = LAUNCH(launch_exclusive_scan(gsize, p->ngroups, p->group_ptr, scratch, stream));
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(&sizes[2], p->group_ptr + p->ngroups, sizeof(int64_t), cudaMemcpyDeviceToHost,
                                 stream);
@@ -315,7 +376,7 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
     if (rgcsr && p->rg_slots > 0) {
         const size_t col_bytes = align_up(sizeof(int32_t) * (size_t)p->rg_slots, 256);
         p->rg_bytes = col_bytes + vs * (size_t)p->rg_slots;
-        e = cudaMalloc(&p->rg, p->rg_bytes);
+        e = dev_malloc(&p->rg, p->rg_bytes);
         if (e != cudaSuccess) {
             p->rg = nullptr;
             return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the Row-grouped copy: ") + cudaGetErrorString(e));
@@ -324,8 +385,8 @@ spmv_status_t build_row_layouts(spmv_plan_s *p, const spmv_options_t &opt, cudaS
         p->rg_val = static_cast<char *>(p->rg) + col_bytes;
         e = cudaMemsetAsync(p->rg, 0, p->rg_bytes, stream);  // pads: column 0, value 0
         if (e == cudaSuccess)
-            e = launch_rgcsr_pack(p->dtype, m, p->row_ptr, p->col_idx, p->vals, p->g_log2, p->group_ptr, p->row_len,
-                                  p->perm, p->rg_col, p->rg_val, true, stream);
+            e = LAUNCH(launch_rgcsr_pack(p->dtype, m, p->row_ptr, p->col_idx, p->vals, p->g_log2, p->group_ptr, p->row_len,
+                                  p->perm, p->rg_col, p->rg_val, true, stream));
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) return cuda_fail(e, "Row-grouped copy");
     }
@@ -359,7 +420,7 @@ spmv_status_t build_spmm_long_rows(spmv_plan_s *p, cudaStream_t stream) {
     const size_t o_cseg_off = take(sizeof(int64_t) * (nc + 1));
     const size_t o_scr = take(sizeof(int64_t) * scan_scratch_elems(nc));
     p->spmm_long_bytes = off;
-    cudaError_t e = cudaMalloc(&p->spmm_long, p->spmm_long_bytes);
+    cudaError_t e = dev_malloc(&p->spmm_long, p->spmm_long_bytes);
     if (e != cudaSuccess) {
         p->spmm_long = nullptr;
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpMM long-row workspace: ") + cudaGetErrorString(e));
@@ -376,12 +437,12 @@ spmv_status_t build_spmm_long_rows(spmv_plan_s *p, cudaStream_t stream) {
     int64_t *scratch = reinterpret_cast<int64_t *>(base + o_scr);
     int64_t sizes[2] = {0, 0};
     e = cudaMemsetAsync(p->spmm_long_arrivals, 0, sizeof(int32_t) * long_ub, stream);
-    if (e == cudaSuccess) e = launch_long_rows_count(m, p->row_ptr, kSpmmLongMin, chunk_rows, chunk_segs, stream);
-    if (e == cudaSuccess) e = launch_exclusive_scan(chunk_rows, nc, chunk_row_off, scratch, stream);
-    if (e == cudaSuccess) e = launch_exclusive_scan(chunk_segs, nc, chunk_seg_off, scratch, stream);
+    if (e == cudaSuccess) e = LAUNCH(launch_long_rows_count(m, p->row_ptr, kSpmmLongMin, chunk_rows, chunk_segs, stream));
+    if (e == cudaSuccess) e = LAUNCH(launch_exclusive_scan(chunk_rows, nc, chunk_row_off, scratch, stream));
+    if (e == cudaSuccess) e = LAUNCH(launch_exclusive_scan(chunk_segs, nc, chunk_seg_off, scratch, stream));
     if (e == cudaSuccess)
-        e = launch_long_rows_scatter(m, p->row_ptr, kSpmmLongMin, chunk_row_off, chunk_seg_off, p->spmm_long_rows,
-                                     p->spmm_seg_begin, stream);
+        e = LAUNCH(launch_long_rows_scatter(m, p->row_ptr, kSpmmLongMin, chunk_row_off, chunk_seg_off, p->spmm_long_rows,
+                                     p->spmm_seg_begin, stream));
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(&sizes[0], chunk_row_off + nc, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess)
@@ -401,7 +462,7 @@ spmv_status_t build_transpose(spmv_plan_s *p, cudaStream_t stream) {
     const size_t o_src = align_up(o_idx + sizeof(int32_t) * (size_t)p->nnz, 256);
     const size_t o_val = align_up(o_src + sizeof(int32_t) * (size_t)p->nnz, 256);
     p->tr_bytes = align_up(o_val + vs * (size_t)p->nnz, 256);
-    cudaError_t e = cudaMalloc(&p->tr, p->tr_bytes);
+    cudaError_t e = dev_malloc(&p->tr, p->tr_bytes);
     if (e != cudaSuccess) {
         p->tr = nullptr;
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the transpose: ") + cudaGetErrorString(e));
@@ -412,10 +473,10 @@ spmv_status_t build_transpose(spmv_plan_s *p, cudaStream_t stream) {
     p->t_src = reinterpret_cast<int32_t *>(b + o_src);
     p->t_vals = b + o_val;
     void *scratch = nullptr;
-    e = cudaMalloc(&scratch, (size_t)transpose_scratch_bytes(p->n, p->nnz));
+    e = dev_malloc(&scratch, (size_t)transpose_scratch_bytes(p->n, p->nnz));
     if (e != cudaSuccess) return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the transpose scratch: ") + cudaGetErrorString(e));
-    e = launch_transpose(p->dtype, p->m, p->n, p->nnz, p->row_ptr, p->col_idx, p->vals, scratch, p->t_ptr, p->t_idx,
-                         p->t_vals, p->t_src, stream);
+    e = LAUNCH(launch_transpose(p->dtype, p->m, p->n, p->nnz, p->row_ptr, p->col_idx, p->vals, scratch, p->t_ptr, p->t_idx,
+                         p->t_vals, p->t_src, stream));
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     cudaFree(scratch);
     if (e != cudaSuccess) return cuda_fail(e, "transpose");
@@ -475,6 +536,7 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
                                   spmv_dtype_t dtype, const spmv_options_t *options,
                                   spmv_stream_t stream_handle) {
     g_last_error.clear();
+    FaultScope fault_scope;
     if (!out) return fail(SPMV_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (m < 0 || n < 0 || nnz < 0) return fail(SPMV_ERR_INVALID_ARG, "negative size");
@@ -543,10 +605,10 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     const size_t off_err = off;
     off = align_up(off + sizeof(int32_t), 256);
     p->arena_bytes = off;
-    e = cudaMalloc(&p->arena, p->arena_bytes);
+    e = dev_malloc(&p->arena, p->arena_bytes);
     if (e != cudaSuccess) {
         p->arena = nullptr;
-        destroy_plan(p);
+        abandon_plan(p, stream);
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the plan workspace: ") + cudaGetErrorString(e));
     }
     char *base = static_cast<char *>(p->arena);
@@ -560,16 +622,16 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
 
     // ---- analysis: statistics + validity, read back once
     e = cudaMemsetAsync(p->arrivals, 0, off_err + sizeof(int32_t) - off_arr, stream);
-    if (e == cudaSuccess) e = launch_row_stats(m, n, nnz, row_ptr, col_idx, partials, stats_ctas, d_stats, stream);
+    if (e == cudaSuccess) e = LAUNCH(launch_row_stats(m, n, nnz, row_ptr, col_idx, partials, stats_ctas, d_stats, stream));
     if (e == cudaSuccess) e = cudaMemcpyAsync(&p->stats, d_stats, sizeof(spmv_row_stats_t), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
-        destroy_plan(p);
+        abandon_plan(p, stream);
         return cuda_fail(e, "plan analysis");
     }
     if (p->stats.flags) {
         const int f = p->stats.flags;
-        destroy_plan(p);
+        abandon_plan(p, stream);
         char msg[160];
         std::snprintf(msg, sizeof msg, "invalid CSR:%s%s%s%s", (f & 1) ? " row_ptr[0] != 0;" : "",
                       (f & 2) ? " row_ptr decreases;" : "", (f & 4) ? " row_ptr[m] != nnz;" : "",
@@ -584,10 +646,10 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     p->num_tiles = total > 0 ? (total + p->tile - 1) / p->tile : 1;
     p->with_spmm = opt.with_spmm != 0;
     if ((p->kernel == SPMV_KERNEL_MERGE_PATH || p->with_spmm) && m > 0) {
-        e = launch_merge_path_partition(m, nnz, row_ptr, p->tile, p->num_tiles, p->part, stream);
+        e = LAUNCH(launch_merge_path_partition(m, nnz, row_ptr, p->tile, p->num_tiles, p->part, stream));
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) {
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return cuda_fail(e, "merge-path partition");
         }
         p->has_partition = true;
@@ -596,10 +658,10 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
         p->spmm_warps = spmm_warps(p->num_tiles);
         const size_t part_bytes = align_up(vs * kSpmmBlocks * 32 * (size_t)p->spmm_warps, 256);
         p->spmm_bytes = 2 * part_bytes + align_up(sizeof(int32_t) * (size_t)p->spmm_warps, 256);
-        e = cudaMalloc(&p->spmm, p->spmm_bytes);
+        e = dev_malloc(&p->spmm, p->spmm_bytes);
         if (e != cudaSuccess) {
             p->spmm = nullptr;
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpMM scratch: ") + cudaGetErrorString(e));
         }
         p->spmm_tail = p->spmm;
@@ -608,45 +670,45 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
         e = cudaMemsetAsync(p->spmm_arrivals, 0, sizeof(int32_t) * (size_t)p->spmm_warps, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) {
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return cuda_fail(e, "SpMM scratch");
         }
     }
     if (p->with_spmm && m > 0 && p->stats.max_len > kRowSpmmMaxLen) {
         const spmv_status_t st = build_spmm_long_rows(p, stream);
         if (st != SPMV_OK) {
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return st;
         }
     }
     if (opt.with_transpose) {
         const spmv_status_t st = build_transpose(p, stream);
         if (st != SPMV_OK) {
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return st;
         }
     }
     if (is_rgcsr(p->kernel) || p->kernel == SPMV_KERNEL_LONG_ROWS) {
         const spmv_status_t st = build_row_layouts(p, opt, stream);
         if (st != SPMV_OK) {
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return st;
         }
     }
     if (p->with_spmm && is_rgcsr(p->kernel) && p->num_long_rows > 0) {
         // SpMM partials for the long rows the Row-grouped copy leaves out
         const size_t part = align_up(value_size(dtype) * 32 * (size_t)p->num_segs, 256);
-        e = cudaMalloc(&p->spmm_rg_long, part + sizeof(int32_t) * (size_t)p->num_long_rows);
+        e = dev_malloc(&p->spmm_rg_long, part + sizeof(int32_t) * (size_t)p->num_long_rows);
         if (e != cudaSuccess) {
             p->spmm_rg_long = nullptr;
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpMM long-row partials: ") + cudaGetErrorString(e));
         }
         p->spmm_rg_arrivals = reinterpret_cast<int32_t *>(static_cast<char *>(p->spmm_rg_long) + part);
         e = cudaMemsetAsync(p->spmm_rg_arrivals, 0, sizeof(int32_t) * (size_t)p->num_long_rows, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) {
-            destroy_plan(p);
+            abandon_plan(p, stream);
             return cuda_fail(e, "SpMM long-row partials");
         }
     }
@@ -664,24 +726,24 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     cudaError_t e = cudaSuccess;
     switch (p->kernel) {
     case SPMV_KERNEL_THREAD_ROW:
-        e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, 0, stream);
+        e = LAUNCH(launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, 0, stream));
         break;
     case SPMV_KERNEL_GROUP_MAPPED:
-        e = launch_group_mapped(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, stream);
+        e = LAUNCH(launch_group_mapped(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, stream));
         break;
     case SPMV_KERNEL_LONG_ROWS:
         // long rows first (they take longest), then the others
-        if (p->num_long_rows > 0) e = launch_long_part(p, x, y, alpha, beta, stream);
+        if (p->num_long_rows > 0) e = LAUNCH(launch_long_part(p, x, y, alpha, beta, stream));
         if (e == cudaSuccess)
-            e = launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta,
-                                      p->num_long_rows > 0 ? p->long_min : 0, stream);
+            e = LAUNCH(launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta,
+                                      p->num_long_rows > 0 ? p->long_min : 0, stream));
         break;
     case SPMV_KERNEL_RGCSR:
     case SPMV_KERNEL_RGCSR_SORTED:
-        if (p->num_long_rows > 0) e = launch_long_part(p, x, y, alpha, beta, stream);
+        if (p->num_long_rows > 0) e = LAUNCH(launch_long_part(p, x, y, alpha, beta, stream));
         if (e == cudaSuccess)
-            e = launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->perm, p->rg_col, p->rg_val,
-                                  x, y, alpha, beta, p->device_error, stream);
+            e = LAUNCH(launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->perm, p->rg_col, p->rg_val,
+                                  x, y, alpha, beta, p->device_error, stream));
         break;
     case SPMV_KERNEL_MERGE_PATH:
     default: {
@@ -701,7 +763,7 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
         a.head_partial = p->head_partial;
         a.arrivals = p->arrivals;
         a.error = p->device_error;
-        e = launch_merge_path_spmv(p->dtype, p->ipt, a, stream);
+        e = LAUNCH(launch_merge_path_spmv(p->dtype, p->ipt, a, stream));
         break;
     }
     }
@@ -759,9 +821,9 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
             l.seg_begin = p->seg_begin;
             l.seg_partial = p->spmm_rg_long;
             l.arrivals = p->spmm_rg_arrivals;
-            e = launch_long_spmm(p->dtype, l, reinterpret_cast<cudaStream_t>(stream_handle));
+            e = LAUNCH(launch_long_spmm(p->dtype, l, reinterpret_cast<cudaStream_t>(stream_handle)));
         }
-        if (e == cudaSuccess) e = launch_rg_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
+        if (e == cudaSuccess) e = LAUNCH(launch_rg_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle)));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
         return SPMV_OK;
     }
@@ -792,7 +854,7 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
         r.seg_begin = p->spmm_seg_begin;
         r.seg_partial = p->spmm_seg_partial;
         r.arrivals = p->spmm_long_arrivals;
-        const cudaError_t e = launch_row_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle));
+        const cudaError_t e = LAUNCH(launch_row_spmm(p->dtype, r, reinterpret_cast<cudaStream_t>(stream_handle)));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
         return SPMV_OK;
     }
@@ -816,7 +878,7 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
     a.tail = p->spmm_tail;
     a.head = p->spmm_head;
     a.arrivals = p->spmm_arrivals;
-    const cudaError_t e = launch_spmm(p->dtype, a, reinterpret_cast<cudaStream_t>(stream_handle));
+    const cudaError_t e = LAUNCH(launch_spmm(p->dtype, a, reinterpret_cast<cudaStream_t>(stream_handle)));
     if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_multi launch");
     return SPMV_OK;
 }
@@ -833,17 +895,17 @@ spmv_status_t spmv_plan_update_values(spmv_plan_t p, const void *vals, spmv_stre
     if (!vals && p->nnz > 0) return fail(SPMV_ERR_INVALID_ARG, "vals is NULL");
     p->vals = vals;
     if (p->tplan) {  // A^T's values in their new order, then its plan's own copy
-        const cudaError_t e = launch_transpose_values(p->dtype, p->nnz, p->t_src, nullptr, vals, nullptr, p->t_vals,
-                                                      reinterpret_cast<cudaStream_t>(stream_handle));
+        const cudaError_t e = LAUNCH(launch_transpose_values(p->dtype, p->nnz, p->t_src, nullptr, vals, nullptr, p->t_vals,
+                                                      reinterpret_cast<cudaStream_t>(stream_handle)));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_update_values");
         const spmv_status_t st = spmv_plan_update_values(p->tplan, p->t_vals, stream_handle);
         if (st != SPMV_OK) return st;
     }
     if (is_rgcsr(p->kernel) && p->rg_slots > 0) {
         // the pattern is unchanged: only the values move into the copy
-        const cudaError_t e = launch_rgcsr_pack(p->dtype, p->m, p->row_ptr, p->col_idx, vals, p->g_log2, p->group_ptr,
+        const cudaError_t e = LAUNCH(launch_rgcsr_pack(p->dtype, p->m, p->row_ptr, p->col_idx, vals, p->g_log2, p->group_ptr,
                                                 p->row_len, p->perm, p->rg_col, p->rg_val, false,
-                                                reinterpret_cast<cudaStream_t>(stream_handle));
+                                                reinterpret_cast<cudaStream_t>(stream_handle)));
         if (e != cudaSuccess) return cuda_fail(e, "spmv_plan_update_values");
     }
     return SPMV_OK;
@@ -883,6 +945,12 @@ spmv_status_t spmv_plan_info(spmv_plan_t p, spmv_plan_info_t *info) {
     info->long_segment_nnz = kLongSegmentNnz;
     info->num_long_segments = p->num_segs;
     info->rgcsr_slots = p->rg_slots;
+    if (p->kernel == SPMV_KERNEL_MERGE_PATH && p->m > 0) {
+        const bool aligned = reinterpret_cast<uintptr_t>(p->row_ptr) % 16 == 0 &&
+                             reinterpret_cast<uintptr_t>(p->col_idx) % 16 == 0 &&
+                             reinterpret_cast<uintptr_t>(p->vals) % 16 == 0;
+        info->merge_path_warps = merge_path_num_warps(p->dtype, p->ipt, aligned, p->num_tiles);
+    }
     return SPMV_OK;
 }
 
@@ -996,11 +1064,11 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     // entries of A of the dense rows: e_off, then their products: pp
     int64_t *tmp = nullptr;
     const int64_t scan_d = scan_scratch_elems(D);
-    cudaError_t e = cudaMalloc(&tmp, sizeof(int64_t) * (size_t)(2 * (D + 1) + scan_d));
+    cudaError_t e = dev_malloc(&tmp, sizeof(int64_t) * (size_t)(2 * (D + 1) + scan_d));
     if (e != cudaSuccess) return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM dense layout: ") + cudaGetErrorString(e));
     int64_t *alen = tmp, *e_off_tmp = tmp + (D + 1), *scan_tmp = tmp + 2 * (D + 1);
     int64_t entries = 0;
-    e = launch_spgemm_dense_layout(a, drows, D, alen, e_off_tmp, scan_tmp, stream);
+    e = LAUNCH(launch_spgemm_dense_layout(a, drows, D, alen, e_off_tmp, scan_tmp, stream));
     if (e == cudaSuccess) e = cudaMemcpyAsync(&entries, e_off_tmp + D, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
@@ -1031,7 +1099,7 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     off = align_up(off + sizeof(int64_t) * (size_t)scan_scratch_elems(nseg), 256);
     const size_t first_bytes = off;
     void *first = nullptr;
-    e = cudaMalloc(&first, first_bytes);
+    e = dev_malloc(&first, first_bytes);
     if (e != cudaSuccess) {
         cudaFree(tmp);
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM dense layout: ") + cudaGetErrorString(e));
@@ -1043,8 +1111,8 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     std::vector<int64_t> h_rowp((size_t)D + 1);
     e = cudaMemcpyAsync(e_off, e_off_tmp, sizeof(int64_t) * (size_t)(D + 1), cudaMemcpyDeviceToDevice, stream);
     if (e == cudaSuccess)
-        e = launch_spgemm_dense_products(a, drows, D, e_off, entries, reinterpret_cast<int64_t *>(fb + o_blen), pp,
-                                         rowp, reinterpret_cast<int64_t *>(fb + o_scan), stream);
+        e = LAUNCH(launch_spgemm_dense_products(a, drows, D, e_off, entries, reinterpret_cast<int64_t *>(fb + o_blen), pp,
+                                         rowp, reinterpret_cast<int64_t *>(fb + o_scan), stream));
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(h_rowp.data(), rowp, sizeof(int64_t) * (size_t)(D + 1), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -1076,7 +1144,7 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     if (need > o_segcnt - o_blen) {
         // a separate allocation for the pieces
         void *more = nullptr;
-        e = cudaMalloc(&more, need);
+        e = dev_malloc(&more, need);
         if (e != cudaSuccess) return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM pieces: ") + cudaGetErrorString(e));
         h->pieces = more;
         h->layout_bytes += need;
@@ -1088,7 +1156,7 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     e = cudaMemcpyAsync(d_k0, piece_k0.data(), sizeof(int64_t) * (size_t)(P + 1), cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(d_prow, piece_row.data(), sizeof(int32_t) * (size_t)P, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = launch_spgemm_dense_locate(P, d_k0, pp, entries, d_pe, stream);
+    if (e == cudaSuccess) e = LAUNCH(launch_spgemm_dense_locate(P, d_k0, pp, entries, d_pe, stream));
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "SpGEMM pieces");
     a.dense_e_off = e_off;
@@ -1111,7 +1179,7 @@ static spmv_status_t spgemm_dense_plan(spmv_spgemm_s *h, cudaStream_t stream) {
     S = std::max<int64_t>(1, std::min<int64_t>(S, (int64_t)((size_t(8) << 30) / std::max<size_t>(per_slot, 1))));
     const size_t vals_bytes = align_up((size_t)n * vs * (size_t)S, 256);
     h->dense_bytes = vals_bytes + align_up(words * sizeof(unsigned) * (size_t)S, 256);
-    e = cudaMalloc(&h->dense, h->dense_bytes);
+    e = dev_malloc(&h->dense, h->dense_bytes);
     if (e != cudaSuccess) {
         h->dense = nullptr;
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM dense rows: ") + cudaGetErrorString(e));
@@ -1139,6 +1207,8 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
                                  const int32_t *a_row_ptr, const int32_t *a_col_idx, int32_t b_nnz,
                                  const int32_t *b_row_ptr, const int32_t *b_col_idx, spmv_dtype_t dtype,
                                  int64_t *c_nnz, spmv_stream_t stream_handle) {
+    g_last_error.clear();
+    FaultScope fault_scope;
     if (!out) return fail(SPMV_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!c_nnz) return fail(SPMV_ERR_INVALID_ARG, "c_nnz is NULL");
@@ -1197,9 +1267,10 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
     const size_t off_err = off;
     off = align_up(off + sizeof(int32_t), 256);
     h->arena_bytes = off;
-    e = cudaMalloc(&h->arena, h->arena_bytes);
+    e = dev_malloc(&h->arena, h->arena_bytes);
     if (e != cudaSuccess) {
         h->arena = nullptr;
+        cudaStreamSynchronize(stream);
         destroy_spgemm(h);
         return fail(SPMV_ERR_ALLOC, std::string("cudaMalloc of the SpGEMM workspace: ") + cudaGetErrorString(e));
     }
@@ -1227,21 +1298,23 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
     spmv_row_stats_t st[2];
     e = cudaMemsetAsync(base, 0, h->arena_bytes, stream);
     if (e == cudaSuccess)
-        e = launch_row_stats(m, k, a_nnz, a_row_ptr, a_col_idx, reinterpret_cast<StatsPartial *>(base + off_pa),
-                             ctas_a, d_stats, stream);
+        e = LAUNCH(launch_row_stats(m, k, a_nnz, a_row_ptr, a_col_idx, reinterpret_cast<StatsPartial *>(base + off_pa),
+                             ctas_a, d_stats, stream));
     if (e == cudaSuccess)
-        e = launch_row_stats(k, n, b_nnz, b_row_ptr, b_col_idx, reinterpret_cast<StatsPartial *>(base + off_pb),
-                             ctas_b, d_stats + 1, stream);
+        e = LAUNCH(launch_row_stats(k, n, b_nnz, b_row_ptr, b_col_idx, reinterpret_cast<StatsPartial *>(base + off_pb),
+                             ctas_b, d_stats + 1, stream));
     if (e == cudaSuccess) e = cudaMemcpyAsync(st, d_stats, sizeof st, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
+        cudaStreamSynchronize(stream);
         destroy_spgemm(h);
         return cuda_fail(e, "SpGEMM analysis");
     }
     for (int w = 0; w < 2; ++w)
         if (st[w].flags) {
             const int f = st[w].flags;
-            destroy_spgemm(h);
+            cudaStreamSynchronize(stream);
+        destroy_spgemm(h);
             char msg[160];
             std::snprintf(msg, sizeof msg, "invalid CSR (%s):%s%s%s%s", w ? "B" : "A", (f & 1) ? " row_ptr[0] != 0;" : "",
                           (f & 2) ? " row_ptr decreases;" : "", (f & 4) ? " row_ptr[m] != nnz;" : "",
@@ -1250,13 +1323,14 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
         }
 
     // ---- products per row and bins
-    e = launch_spgemm_analysis(a, counts, offsets, scan, stream);
+    e = LAUNCH(launch_spgemm_analysis(a, counts, offsets, scan, stream));
     int64_t host_off[kSpgemmBins + 1] = {};
     if (e == cudaSuccess && m > 0)
         for (int b = 0; b <= kSpgemmBins && e == cudaSuccess; ++b)
             e = cudaMemcpyAsync(host_off + b, offsets + b * chunks, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
+        cudaStreamSynchronize(stream);
         destroy_spgemm(h);
         return cuda_fail(e, "SpGEMM binning");
     }
@@ -1268,30 +1342,32 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
     if (dense_rows > 0) {
         const spmv_status_t st = spgemm_dense_plan(h, stream);
         if (st != SPMV_OK) {
-            destroy_spgemm(h);
+            cudaStreamSynchronize(stream);
+        destroy_spgemm(h);
             return st;
         }
     }
 
     // ---- symbolic phase: the size of every row of C
-    e = launch_spgemm_symbolic(dtype, a, scan, stream);
+    e = LAUNCH(launch_spgemm_symbolic(dtype, a, scan, stream));
     int64_t tot[2] = {0, 0};
     if (e == cudaSuccess && m > 0) e = cudaMemcpyAsync(tot, a.c_ptr + m, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess && m > 0) {
         // the total of the products (for the info), summed into row_nnz,
         // which the numeric phase does not use
-        e = launch_exclusive_scan(a.products, m, a.row_nnz, scan, stream);
+        e = LAUNCH(launch_exclusive_scan(a.products, m, a.row_nnz, scan, stream));
         if (e == cudaSuccess) e = cudaMemcpyAsync(tot + 1, a.row_nnz + m, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     }
     // ---- the numeric phase's bins, by the entries of each row of C (row_nnz as the key)
     int64_t num_off[kSpgemmBins + 1] = {};
     if (e == cudaSuccess && m > 0) {
-        e = launch_spgemm_numeric_bins(a, a.row_nnz, counts, offsets, scan, num_rows, stream);
+        e = LAUNCH(launch_spgemm_numeric_bins(a, a.row_nnz, counts, offsets, scan, num_rows, stream));
         for (int b = 0; b <= kSpgemmBins && e == cudaSuccess; ++b)
             e = cudaMemcpyAsync(num_off + b, offsets + b * chunks, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
+        cudaStreamSynchronize(stream);
         destroy_spgemm(h);
         return cuda_fail(e, "SpGEMM symbolic phase");
     }
@@ -1300,6 +1376,7 @@ spmv_status_t spmv_spgemm_create(spmv_spgemm_t *out, int32_t m, int32_t k, int32
     h->products = tot[1];
     *c_nnz = h->c_nnz;
     if (h->c_nnz >= (1LL << 31)) {
+        cudaStreamSynchronize(stream);
         destroy_spgemm(h);
         return fail(SPMV_ERR_INVALID_ARG, "C has 2^31 entries or more (int32 indices)");
     }
@@ -1314,7 +1391,7 @@ spmv_status_t spmv_spgemm_compute(spmv_spgemm_t h, const void *a_vals, const voi
     if ((h->a_nnz > 0 && !a_vals) || (h->b_nnz > 0 && !b_vals)) return fail(SPMV_ERR_INVALID_ARG, "a_vals or b_vals is NULL");
     if (h->c_nnz > 0 && (!c_col_idx || !c_vals)) return fail(SPMV_ERR_INVALID_ARG, "c_col_idx or c_vals is NULL");
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
-    const cudaError_t e = launch_spgemm_numeric(h->dtype, h->args, a_vals, b_vals, c_row_ptr, c_col_idx, c_vals, stream);
+    const cudaError_t e = LAUNCH(launch_spgemm_numeric(h->dtype, h->args, a_vals, b_vals, c_row_ptr, c_col_idx, c_vals, stream));
     if (e != cudaSuccess) return cuda_fail(e, "spmv_spgemm_compute launch");
     return SPMV_OK;
 }

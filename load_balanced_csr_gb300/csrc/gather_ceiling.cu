@@ -22,6 +22,24 @@
 //   TMA4_16  TMA4 over rows of 16 bytes (the narrowest row a tensor copy
 //            takes)
 //
+// and, to see what bringing in the matrix stream costs the gathers, three
+// paths that also read the values (L1 gathers in all three):
+//
+//   STREAM_LDG      columns and values by coalesced loads into registers
+//   STREAM_BULK     columns and values by one bulk copy each per chunk into
+//                   shared memory (two stages per warp)
+//   STREAM_CPASYNC  columns and values by 16-byte cp.async per lane into
+//                   shared memory (two stages per warp)
+//   STREAM_LDG_OCC  as STREAM_LDG, with the shared memory of the staged
+//                   paths reserved (the same warps per SM)
+//   STREAM_LDG_STS  coalesced loads into registers, stored to shared memory
+//                   and read back by the lanes (staging done by the lanes)
+//   STREAM_LDG_FEW  as STREAM_LDG, with no shared memory but only as many
+//                   CTAs per SM as the staged paths fit
+//   STREAM_LDG_RES_k (k = 1..6)  as STREAM_LDG with 4 CTAs per SM and
+//                   32 * k KB of shared memory reserved per SM, unused: how
+//                   the gathers depend on the L1 left to them
+//
 // Each warp takes chunks of 32 * U consecutive nonzeros (grid-stride), loads
 // their columns with coalesced loads and adds the bit patterns of the
 // gathered x values into a 64-bit checksum, identical for every path.
@@ -67,6 +85,7 @@ struct GatherParams {
     int32_t n;
     const int32_t *col;
     const V *x;
+    const V *vals;       // STREAM_* paths
     int32_t rows;        // TMA4: rows in the 2-D view of x
     unsigned long long *checksum;
     int32_t *error;
@@ -234,6 +253,131 @@ __global__ void __launch_bounds__(kGThreads) gather_ceiling_kernel(const GatherP
     if (lane == 0 && sum) atomicAdd(p.checksum, sum);
 }
 
+
+// Paths 8-10: the gather with the matrix stream (columns and values).  Each
+// warp takes chunks of 256 nonzeros; the checksum adds the gathered x and
+// the values' bit patterns.  Full chunks go through the path's staging; the
+// last, partial chunk is loaded directly.
+constexpr int kSChunk = 256;
+
+template <typename V>
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+template <typename V, int PATH>
+__global__ void __launch_bounds__(kGThreads) stream_gather_kernel(const GatherParams<V> p) {
+    constexpr int U = kSChunk / 32;
+    constexpr int SB = kSChunk * (4 + (int)sizeof(V));  // columns, then values
+    extern __shared__ __align__(16) unsigned char dsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t base_u32 = smem_u32(dsm);
+    unsigned char *aligned = dsm + (((base_u32 + 127u) & ~127u) - base_u32);
+    unsigned char *region = aligned + (size_t)warp * (128 + 2 * SB);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(region);
+    unsigned char *stages = region + 128;
+    const uint64_t pol = l2_policy_evict_last();
+    const uint64_t spol = l2_policy_evict_first();
+    const long long chunks = (p.nnz + kSChunk - 1) / kSChunk;
+    const long long full = p.nnz / kSChunk;
+    const long long gw = (long long)blockIdx.x * kGWarps + warp;
+    const long long step = (long long)gridDim.x * kGWarps;
+    unsigned long long sum = 0;
+
+    auto direct = [&](long long c) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long k = c * kSChunk + u * 32 + lane;
+            if (k < p.nnz) sum += bits_of(gather_keep(p.x + ld_stream(p.col + k), pol)) + bits_of(ld_stream(p.vals + k));
+        }
+    };
+    if (PATH == 8 || PATH == 11 || PATH >= 13) {
+        for (long long c = gw; c < chunks; c += step) direct(c);
+    } else if (PATH == 12) {
+        int *sc = reinterpret_cast<int *>(stages);
+        V *sv = reinterpret_cast<V *>(stages + kSChunk * 4);
+        for (long long c = gw; c < full; c += step) {
+            int cr[U];
+            V vr[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                cr[u] = ld_stream(p.col + c * kSChunk + u * 32 + lane);
+                vr[u] = ld_stream(p.vals + c * kSChunk + u * 32 + lane);
+            }
+            __syncwarp();  // the previous chunk is read
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                sc[u * 32 + lane] = cr[u];
+                sv[u * 32 + lane] = vr[u];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < U; ++u)  // read back in another lane order
+                sum += bits_of(gather_keep(p.x + sc[u * 32 + (lane ^ 1)], pol)) + bits_of(sv[u * 32 + (lane ^ 1)]);
+        }
+        for (long long t = full + ((gw - full) % step + step) % step; t < chunks; t += step) direct(t);
+    } else {
+        if (PATH == 9 && lane == 0) {
+            mbar_init(bars);
+            mbar_init(bars + 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+        auto issue = [&](long long c, int s) {
+            unsigned char *st = stages + s * SB;
+            if (PATH == 9) {
+                if (lane == 0) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(bars + s, (uint32_t)SB);
+                    bulk_copy(st, p.col + c * kSChunk, kSChunk * 4u, bars + s, spol);
+                    bulk_copy(st + kSChunk * 4, p.vals + c * kSChunk, kSChunk * (uint32_t)sizeof(V), bars + s, spol);
+                }
+            } else {
+                const unsigned char *gc = reinterpret_cast<const unsigned char *>(p.col + c * kSChunk);
+                const unsigned char *gv = reinterpret_cast<const unsigned char *>(p.vals + c * kSChunk);
+                for (int q = lane; q < kSChunk * 4 / 16; q += 32) cp_async16<V>(st + q * 16, gc + q * 16);
+                for (int q = lane; q < kSChunk * (int)sizeof(V) / 16; q += 32)
+                    cp_async16<V>(st + kSChunk * 4 + q * 16, gv + q * 16);
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            }
+        };
+        uint32_t uses = 0u;
+        long long c = gw;
+        if (c < full) issue(c, 0);
+        int s = 0;
+        for (; c < full; c += step) {
+            const long long cn = c + step;
+            const bool more = cn < full;
+            if (more) issue(cn, s ^ 1);
+            if (PATH == 9) {
+                const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + s, (uses >> s) & 1u));
+                if (!ok) {
+                    if (lane == 0) atomicOr(p.error, 1);
+                    if (more) mbar_wait_bounded(bars + (s ^ 1), (uses >> (s ^ 1)) & 1u);
+                    return;
+                }
+                uses ^= 1u << s;
+            } else {
+                if (more) asm volatile("cp.async.wait_group 1;" ::: "memory");
+                else asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+            }
+            const unsigned char *st = stages + s * SB;
+            const int *sc = reinterpret_cast<const int *>(st);
+            const V *sv = reinterpret_cast<const V *>(st + kSChunk * 4);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                sum += bits_of(gather_keep(p.x + sc[u * 32 + lane], pol)) + bits_of(sv[u * 32 + lane]);
+            __syncwarp();  // the stage is read before it is refilled
+            s ^= 1;
+        }
+        for (long long t = full + ((gw - full) % step + step) % step; t < chunks; t += step) direct(t);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0 && sum) atomicAdd(p.checksum, sum);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -258,6 +402,9 @@ cudaError_t launch_gather(const GatherParams<V> &p, const CUtensorMap &map, cuda
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGThreads, smem);
     if (e != cudaSuccess) return e;
+    const int pct = carveout_percent(per_sm > 0 ? per_sm : 1, smem);
+    if (pct >= 0 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, pct)) != cudaSuccess)
+        return e;
     const long long chunks = (p.nnz + 32 * U - 1) / (32 * U);
     long long grid = (long long)(per_sm > 0 ? per_sm : 1) * device_sm_count();
     const long long need = (chunks + kGWarps - 1) / kGWarps;
@@ -267,14 +414,44 @@ cudaError_t launch_gather(const GatherParams<V> &p, const CUtensorMap &map, cuda
     return cudaGetLastError();
 }
 
+
+template <typename V, int PATH>
+cudaError_t launch_stream_gather(const GatherParams<V> &p, cudaStream_t stream) {
+    const size_t staged = 128 + (size_t)kGWarps * (128 + 2 * kSChunk * (4 + sizeof(V)));
+    // PATH 11 reserves the staged paths' shared memory without using it;
+    // PATH 13 uses none but launches as few CTAs as they fit
+    const size_t smem = PATH == 8 || PATH == 13 ? 0 : PATH >= 14 ? (size_t)(PATH - 13) * 8192 - 1024 : staged;
+    auto kern = stream_gather_kernel<V, PATH>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(staged > smem ? staged : smem));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGThreads, PATH == 13 ? staged : smem);
+    if (e != cudaSuccess) return e;
+    // STREAM_LDG_OCC keeps the runtime's own choice (it shows what reserved
+    // shared memory costs); the others leave the rest of the SM to L1
+    if (PATH >= 14) per_sm = per_sm < 4 ? per_sm : 4;
+    const int pct = PATH == 11 || PATH == 13 ? -1 : carveout_percent(per_sm > 0 ? per_sm : 1, smem);
+    if (pct >= 0 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, pct)) != cudaSuccess)
+        return e;
+    const long long chunks = (p.nnz + kSChunk - 1) / kSChunk;
+    long long grid = (long long)(per_sm > 0 ? per_sm : 1) * device_sm_count();
+    const long long need = (chunks + kGWarps - 1) / kGWarps;
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    kern<<<(unsigned)grid, kGThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename V>
-spmv_status_t gather_typed(int path, int32_t nnz, const int32_t *col, int32_t n, const void *x,
+spmv_status_t gather_typed(int path, int32_t nnz, const int32_t *col, int32_t n, const void *x, const void *vals,
                            unsigned long long *checksum, int32_t *error, cudaStream_t stream) {
     GatherParams<V> p;
     p.nnz = nnz;
     p.n = n;
     p.col = col;
     p.x = static_cast<const V *>(x);
+    p.vals = static_cast<const V *>(vals);
     const int row_bytes = g_row_bytes(path);
     p.rows = (int32_t)(((long long)n * (long long)sizeof(V)) / row_bytes);
     p.checksum = checksum;
@@ -282,7 +459,11 @@ spmv_status_t gather_typed(int path, int32_t nnz, const int32_t *col, int32_t n,
     CUtensorMap map;
     memset(&map, 0, sizeof(map));
     if (path == 3 && reinterpret_cast<uintptr_t>(x) % 16 != 0) return SPMV_ERR_UNSUPPORTED;
-    if (path >= 4) {
+    if (path == 9 || path == 10) {
+        if (reinterpret_cast<uintptr_t>(col) % 16 != 0 || reinterpret_cast<uintptr_t>(vals) % 16 != 0)
+            return SPMV_ERR_UNSUPPORTED;
+    }
+    if (path >= 4 && path <= 7) {
         if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || p.rows < 1) return SPMV_ERR_UNSUPPORTED;
         PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
         if (!enc) return SPMV_ERR_UNSUPPORTED;
@@ -306,6 +487,18 @@ spmv_status_t gather_typed(int path, int32_t nnz, const int32_t *col, int32_t n,
     case 5: e = launch_gather<V, 5, 4>(p, map, stream); break;
     case 6: e = launch_gather<V, 6, 4>(p, map, stream); break;
     case 7: e = launch_gather<V, 7, 4>(p, map, stream); break;
+    case 8: e = launch_stream_gather<V, 8>(p, stream); break;
+    case 9: e = launch_stream_gather<V, 9>(p, stream); break;
+    case 10: e = launch_stream_gather<V, 10>(p, stream); break;
+    case 11: e = launch_stream_gather<V, 11>(p, stream); break;
+    case 12: e = launch_stream_gather<V, 12>(p, stream); break;
+    case 13: e = launch_stream_gather<V, 13>(p, stream); break;
+    case 14: e = launch_stream_gather<V, 14>(p, stream); break;
+    case 15: e = launch_stream_gather<V, 15>(p, stream); break;
+    case 16: e = launch_stream_gather<V, 16>(p, stream); break;
+    case 17: e = launch_stream_gather<V, 17>(p, stream); break;
+    case 18: e = launch_stream_gather<V, 18>(p, stream); break;
+    case 19: e = launch_stream_gather<V, 19>(p, stream); break;
     default: return SPMV_ERR_INVALID_ARG;
     }
     return e == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
@@ -317,14 +510,15 @@ spmv_status_t gather_typed(int path, int32_t nnz, const int32_t *col, int32_t n,
 using namespace lbcsr;
 
 extern "C" spmv_status_t spmv_gather_ceiling(int32_t path, int32_t nnz, const int32_t *col_idx, int32_t n,
-                                             const void *x, spmv_dtype_t dtype, uint64_t *checksum,
-                                             int32_t *error, spmv_stream_t stream) {
-    if (path < 0 || path > 7 || nnz < 0 || n < 0) return SPMV_ERR_INVALID_ARG;
+                                             const void *x, const void *vals, spmv_dtype_t dtype,
+                                             uint64_t *checksum, int32_t *error, spmv_stream_t stream) {
+    if (path < 0 || path > 19 || nnz < 0 || n < 0) return SPMV_ERR_INVALID_ARG;
     if (dtype != SPMV_F32 && dtype != SPMV_F64) return SPMV_ERR_INVALID_ARG;
     if (nnz == 0) return SPMV_OK;
-    if (!col_idx || !checksum || !error || (path > 0 && (!x || n < 1))) return SPMV_ERR_INVALID_ARG;
+    if (!col_idx || !checksum || !error || (path > 0 && (!x || n < 1)) || (path >= 8 && !vals))
+        return SPMV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     unsigned long long *cs = reinterpret_cast<unsigned long long *>(checksum);
-    return dtype == SPMV_F64 ? gather_typed<double>(path, nnz, col_idx, n, x, cs, error, s)
-                             : gather_typed<float>(path, nnz, col_idx, n, x, cs, error, s);
+    return dtype == SPMV_F64 ? gather_typed<double>(path, nnz, col_idx, n, x, vals, cs, error, s)
+                             : gather_typed<float>(path, nnz, col_idx, n, x, vals, cs, error, s);
 }

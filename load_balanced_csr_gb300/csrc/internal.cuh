@@ -62,10 +62,11 @@ struct MergePathArgs {
     double beta;
     const int2 *part;      // num_tiles + 1 splits
     int64_t num_tiles;
-    void *tail_partial;    // [num_tiles] value type: partial of the row open at a tile's end
-    void *head_partial;    // [num_tiles] value type: partial of a split row finished in a tile
-    int32_t *arrivals;     // [num_tiles] zero between executions
+    void *tail_partial;    // [warps] value type: partial of the row open at a warp's run end
+    void *head_partial;    // [warps] value type: partial of a cut row finished in a warp's run
+    int32_t *arrivals;     // [warps] zero between executions (warps <= num_tiles)
     int32_t *error = nullptr;  // device word: bit 0 set if a copy never completed
+    int64_t max_warps = 0;     // > 0: at most this many warps (tail/head/arrivals hold that many)
 };
 
 bool merge_path_supported(int items_per_thread);
@@ -74,6 +75,10 @@ int merge_path_min_items();                     // smallest supported items per 
 int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_t &stats);
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int items_per_thread, const MergePathArgs &a,
                                    cudaStream_t stream);
+// Warps the merge-path kernel runs for num_tiles tiles (each owns a run of
+// tiles); `aligned`: the kernel variant for 16-byte aligned arrays.  -1 on a
+// CUDA error.
+int64_t merge_path_num_warps(spmv_dtype_t dtype, int items_per_thread, bool aligned, int64_t num_tiles);
 
 // ---------------------------------------------------------------- plan-time layouts
 // Exclusive prefix sum of n int64 values: out[0..n] (out[n] = total).
@@ -206,5 +211,8 @@ cudaError_t launch_transpose_values(spmv_dtype_t dtype, int32_t nnz, const int32
                                     const void *vals, int32_t *t_idx, void *t_vals, cudaStream_t stream);
 
 int device_sm_count();
+// Smallest shared-memory carve-out (percent) holding `ctas` CTAs of
+// `smem_per_cta` bytes per SM (-1 if the device cannot be queried).
+int carveout_percent(int ctas, size_t smem_per_cta);
 
 }  // namespace lbcsr

@@ -50,6 +50,7 @@
 // warp arrives last, so results are deterministic.  (The CUB implementation
 // the paper compares with runs a separate fix-up step for these rows.)
 #include <climits>
+#include <cstdlib>
 
 #include "internal.cuh"
 #include "tma.cuh"
@@ -62,7 +63,27 @@ using namespace tma;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 2;
+// Copy stages per warp (stages_for below): 2 keeps the next tile's copy in
+// flight while a tile is processed; 1 halves the shared memory, and the copy
+// of tile t + 1 starts when tile t is done.  Shared memory is taken from the
+// SM's L1, where the x gathers in flight live: measured on GB300, the random
+// gathers slow down once more than about 96 KB per SM goes to shared memory
+// (by 1.3x at 160 KB and 1.7x at 192 KB), so large tiles take one stage.
+// LBCSR_MP_STAGES (1 or 2) overrides the choice at build time, for tuning.
+template <typename V, int IPL>
+__host__ __device__ constexpr int stage_bytes();
+template <typename V, int IPL>
+__host__ __device__ constexpr int stages_for() {
+#ifdef LBCSR_MP_STAGES
+    return LBCSR_MP_STAGES;
+#else
+    // fp32 with 24 items per lane is the banded case (the plan picks it for
+    // matrices within n/64 of the diagonal): its gathers hit L1, so the
+    // copy in flight pays (27-point stencil 128^3: 89 us with two stages,
+    // 117 us with one)
+    return (2 * stage_bytes<V, IPL>() <= 7168 || (sizeof(V) == 4 && IPL == 24)) ? 2 : 1;
+#endif
+}
 
 template <typename V>
 struct MPParams {
@@ -98,10 +119,10 @@ __host__ __device__ constexpr int stage_bytes() {
     constexpr int per_unit = sizeof(int) + sizeof(V);
     return ((per_unit * (T + 16) + 4 * (T / 32 + 16)) + 15) & ~15;
 }
-// A warp's region: two mbarriers (16 bytes), then its two stages.
+// A warp's region: two mbarriers (16 bytes), then its stages.
 template <typename V, int IPL>
 __host__ __device__ constexpr int warp_region_bytes() {
-    return 16 + kStages * stage_bytes<V, IPL>();
+    return 16 + stages_for<V, IPL>() * stage_bytes<V, IPL>();
 }
 
 // Where a tile's arrays sit in its stage.
@@ -223,6 +244,74 @@ __device__ __forceinline__ long long warp_of_tile(long long t, long long P, long
     return ((t + 1) * W - 1) / P;  // warp w owns tiles [w*P/W, (w+1)*P/W)
 }
 
+
+// The tile's finished rows, written to y coalesced: row q's sum is in the
+// slot of its last nonzero in the tile (a row with none there contributes 0,
+// or the carried sum when it is the tile's first row).  MODE (bit 0: alpha
+// != 1, bit 1: beta != 0) is fixed per launch; taking it as a template
+// parameter keeps the alpha and beta arithmetic out of the loop when it is
+// not needed.  Returns the first row's sum when that row is cut between
+// warps (it is then finished by the cut-row protocol, not written here).
+template <typename V, int MODE>
+__device__ __forceinline__ V finish_rows(const MPParams<V> &p, const StageView<V> &sv, int i0, int j0, int nrows,
+                                         int sh, V carry_row0, bool cut_head, int lane, uint64_t pol) {
+    V head_val = V(0);
+    int prev_last = 0;  // end of the row before this round's first (tile-relative)
+    for (int base = 0; base < nrows; base += 32) {
+        const int q = base + lane;
+        const int e = q < nrows ? sv.re[q] - j0 : 0;
+        const int up = __shfl_up_sync(0xffffffffu, e, 1);
+        const int ep = lane == 0 ? prev_last : up;
+        prev_last = __shfl_sync(0xffffffffu, e, 31);
+        if (q < nrows) {
+            const V sum = e > ep ? sv.val[e - 1 + sh] : (q == 0 ? carry_row0 : V(0));
+            if (q == 0 && cut_head) {
+                head_val = sum;
+            } else {
+                V res = sum;
+                if (MODE & 1) res = p.alpha * res;
+                if (MODE & 2) res = fma(p.beta, sv.yo[q], res);
+                store_stream(p.y + i0 + q, res, pol);
+            }
+        }
+    }
+    return head_val;
+}
+
+// The tail partials of warps first .. last-1, summed in a fixed order whose
+// depth grows with the logarithm of their number: chunks of 32 warps by a
+// shuffle tree, the chunk sums pairwise by a binary counter (level k holds
+// the sum of 2^k chunks).  A row cut across W warps then goes through at
+// most 5 + 2 log2(W / 32) + 1 additions here (W < 2^17 for every size the
+// interface accepts).
+template <typename V>
+__device__ __forceinline__ V sum_partials(const V *tail, long long first, long long last, int lane) {
+    constexpr int kLevels = 16;  // up to 2^16 chunks of 32 warps
+    V level[kLevels];
+    unsigned occupied = 0;
+    for (long long c = first; c < last; c += 32) {
+        V s = c + lane < last ? __ldcg(tail + c + lane) : V(0);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+#pragma unroll
+        for (int k = 0; k < kLevels; ++k) {
+            if (occupied & (1u << k)) {
+                s = level[k] + s;
+                occupied &= ~(1u << k);
+            } else {
+                level[k] = s;
+                occupied |= 1u << k;
+                break;
+            }
+        }
+    }
+    V total = V(0);
+#pragma unroll
+    for (int k = 0; k < kLevels; ++k)
+        if (occupied & (1u << k)) total = level[k] + total;
+    return total;
+}
+
 // Cut rows: store this warp's partial, count in; the last to arrive adds all
 // partials (warps first..last-1 as tails, warp last as head) and writes y.
 // Called by the whole warp; `lane_with_value` holds the partial.
@@ -239,10 +328,7 @@ __device__ void cut_row(const MPParams<V> &p, int lane, int lane_with_value, V p
         if (finisher) __threadfence();
     }
     if (!__shfl_sync(0xffffffffu, finisher, lane_with_value)) return;
-    V s = V(0);
-    for (long long t = first + lane; t < last; t += 32) s += __ldcg(p.tail_partial + t);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    V s = sum_partials(p.tail_partial, first, last, lane);
     if (lane == 0) {
         s += __ldcg(p.head_partial + last);
         p.y[row] = finish_row(s, p.alpha, p.beta, p.mode, p.y, row);
@@ -254,6 +340,8 @@ template <typename V, int IPL, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 merge_path_spmv_kernel(const MPParams<V> p) {
     constexpr int T = 32 * IPL;
+    constexpr int kStages = stages_for<V, IPL>();
+    static_assert(kStages == 1 || kStages == 2, "one or two stages");
     extern __shared__ __align__(16) unsigned char dsm[];
 
     const int lane = threadIdx.x & 31;
@@ -285,22 +373,19 @@ merge_path_spmv_kernel(const MPParams<V> p) {
     int4 cur = first_tile;
     int4 nxt = make_int4(0, 0, 0, 0);
     issue_tile<V, VEC>(p, stages, bars, cur, lane, stream_pol);
-    if (t_begin + 1 < t_end) {
+    if (kStages == 2 && t_begin + 1 < t_end) {
         nxt = tile_bounds(p.part, t_begin + 1);
         issue_tile<V, VEC>(p, stages + stage_bytes<V, IPL>(), bars + 1, nxt, lane, stream_pol);
     }
 
     const bool with_y = p.mode & 2;
     V carry = V(0);  // sum of the row open at the previous tile's end
-    // fp32: tiles that lie inside one row (no row end) leave their sums in
-    // the lanes, one per lane, and skip the scan; the lanes' shares join
-    // the carry once, when a row end or the end of the run comes.  (fp64
-    // keeps the scan: the extra registers cost more than the skipped adds,
-    // measured on the skewed matrix.)
+    // tiles that lie inside one row (no row end) leave their sums in the
+    // lanes, one per lane, and skip the scan
     V lane_part = V(0);
     bool parts_pending = false;
     for (long long t = t_begin; t < t_end; ++t) {
-        const int s = (int)((t - t_begin) & 1);
+        const int s = kStages == 2 ? (int)((t - t_begin) & 1) : 0;
         unsigned char *stage = stages + s * stage_bytes<V, IPL>();
         const int i0 = cur.x, j0 = cur.y, i1 = cur.z, j1 = cur.w;
         const int nrows = i1 - i0;
@@ -309,43 +394,69 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const StageView<V> sv = stage_view<V>(stage, cur, with_y);
         const int nwords = (nnzt + 31) >> 5;
         // bounds of the tile that goes into this stage next (load early)
-        const int4 after = t + 2 < t_end ? tile_bounds(p.part, t + 2) : cur;
+        const int4 after = t + kStages < t_end ? tile_bounds(p.part, t + kStages) : cur;
 
         if (VEC) {  // this tile's copies are done (the next tile's may not be)
-            const uint32_t parity = (uint32_t)(((t - t_begin) >> 1) & 1);
+            const uint32_t parity = (uint32_t)(((t - t_begin) / kStages) & 1);
             const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + s, parity));
             if (!ok) {  // a copy never completed: report it and stop this warp
                 if (lane == 0 && p.error) atomicOr(p.error, 1);
                 mbar_wait_bounded(bars + s, parity);
-                if (t + 1 < t_end) mbar_wait_bounded(bars + (s ^ 1), (uint32_t)(((t + 1 - t_begin) >> 1) & 1));
+                if (kStages == 2 && t + 1 < t_end)
+                    mbar_wait_bounded(bars + (s ^ 1), (uint32_t)(((t + 1 - t_begin) >> 1) & 1));
                 return;
             }
         }
         __syncwarp();  // the lanes' tail loads are visible too
 
-        // ---- this lane's run [k0, k0 + run): values and x into registers
+        // ---- values and x into registers.  A tile with row ends splits its
+        // nonzeros into lane runs [k0, k0 + run) of Q consecutive ones (Q
+        // odd, so the lanes' shared-memory reads hit distinct banks).  A tile
+        // that lies inside one row may split them any way: it takes them
+        // interleaved (nonzero lane + 32 i), so that the gathers of a row
+        // with dense columns share cache lines.
+        const bool inside = nrows == 0;
         const int Q = ((nnzt + 31) >> 5) | 1;
         const int k0 = min(lane * Q, nnzt);
         const int run = min(Q, nnzt - k0);
+        const int steps = inside ? (nnzt + 31) >> 5 : Q;  // the same for all lanes
         V xr[IPL + 1], vr[IPL + 1];
+        if (inside) {
+            const int *c = sv.col + sh + lane;
+            const V *w = sv.val + sh + lane;
 #pragma unroll
-        for (int i = 0; i <= IPL; ++i) {
-            if (sizeof(V) == 8 && i >= Q) break;  // Q is the same for all lanes
-            xr[i] = i < run ? gather_keep(p.x + sv.col[k0 + i + sh], x_pol) : V(0);
-            vr[i] = i < run ? sv.val[k0 + i + sh] : V(0);
-        }
-
-        if (sizeof(V) == 4 && nrows == 0) {  // the whole tile belongs to the open row
-            V acc = V(0);
+            for (int i = 0; i <= IPL; ++i) {
+                if (sizeof(V) == 8 && i >= steps) break;
+                const bool in = i * 32 + lane < nnzt;
+                xr[i] = in ? gather_keep(p.x + c[i * 32], x_pol) : V(0);
+                vr[i] = in ? w[i * 32] : V(0);
+            }
+        } else {
+            const int *c = sv.col + sh + k0;
+            const V *w = sv.val + sh + k0;
 #pragma unroll
             for (int i = 0; i <= IPL; ++i) {
                 if (sizeof(V) == 8 && i >= Q) break;
+                xr[i] = i < run ? gather_keep(p.x + c[i], x_pol) : V(0);
+                vr[i] = i < run ? w[i] : V(0);
+            }
+        }
+        if (inside) {
+            // the lanes keep their shares; they join the carry once, when a
+            // row end or the end of the run comes
+            V acc = V(0);
+#pragma unroll
+            for (int i = 0; i <= IPL; ++i) {
+                if (sizeof(V) == 8 && i >= steps) break;
                 acc = fma(vr[i], xr[i], acc);
             }
             lane_part += acc;
             parts_pending = true;
         } else {
-        if (sizeof(V) == 4 && parts_pending) {
+        // lanes past the tile's last nonzero take no part (lane 0 always
+        // does: it brings the carried sum)
+        const int last_lane = nnzt > 0 ? (nnzt - 1) / Q : 0;
+        if (parts_pending) {
             carry += warp_sum(lane_part);
             lane_part = V(0);
             parts_pending = false;
@@ -355,13 +466,33 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         __syncwarp();
         // The carried sum belongs to row i0.  If that row ends before the
         // tile's first nonzero, it takes the carry and nothing flows on.
-        const bool row0_ends_first = nrows > 0 && sv.re[0] == j0;
+        const bool row0_ends_first = sv.re[0] == j0;
         const V carry_row0 = row0_ends_first ? carry : V(0);
         if (row0_ends_first) carry = V(0);
-        for (int r = lane; r < nrows; r += 32) {
-            const int e = sv.re[r] - j0;
-            const int ep = r == 0 ? 0 : sv.re[r - 1] - j0;
-            if (e > ep) atomicOr(sv.bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
+        {
+            // lane L takes the block of rows [L nrows / 32, (L + 1) nrows / 32):
+            // their ends increase, so the lane collects the bits of one word
+            // at a time in a register and ORs each word in once (lanes share
+            // a word only at the edges of their blocks)
+            const int r_lo = (lane * nrows) >> 5;
+            const int r_hi = ((lane + 1) * nrows) >> 5;
+            int prev = r_lo == 0 ? 0 : sv.re[r_lo - 1] - j0;
+            int word = -1;
+            unsigned mask = 0u;
+            for (int r = r_lo; r < r_hi; ++r) {
+                const int e = sv.re[r] - j0;
+                if (e > prev) {
+                    const int w = (e - 1) >> 5;
+                    if (w != word) {
+                        if (mask) atomicOr(sv.bm + word, mask);
+                        word = w;
+                        mask = 0u;
+                    }
+                    mask |= 1u << ((e - 1) & 31);
+                }
+                prev = e;
+            }
+            if (mask) atomicOr(sv.bm + word, mask);
         }
         __syncwarp();
         // bit i of `bits`: nonzero k0 + i is the last of a row in this tile
@@ -371,9 +502,13 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const unsigned long long run_mask = run >= 64 ? ~0ull : ((1ull << run) - 1);
         const unsigned long long bits = shifted & run_mask;
 
-        // ---- add the run up; a row's sum goes to the slot of its last nonzero
-        // (the first closed row's slot gets the carry from earlier lanes below)
-        V acc = V(0);
+        // ---- add the run up.  Lane 0 starts from the carried sum.  A lane's
+        // first closed row stays in a register (it still lacks the sum
+        // carried in from earlier lanes); later closed rows go to the slot
+        // of their last nonzero, which no other lane touches.
+        V acc = lane == 0 ? carry : V(0);
+        V first_sum = V(0);
+        bool closed = false;
 #pragma unroll
         for (int i = 0; i <= IPL; ++i) {
             // fp64: every warp-wide FMA costs the fp64 unit the same, so stop
@@ -381,15 +516,18 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             if (sizeof(V) == 8 && i >= Q) break;
             acc = fma(vr[i], xr[i], acc);  // vr[i] = 0 past the run
             if ((bits >> i) & 1ull) {
-                sv.val[k0 + i + sh] = acc;  // only this lane touches the slot
+                if (closed) sv.val[k0 + i + sh] = acc;
+                else first_sum = acc;
+                closed = true;
                 acc = V(0);
             }
         }
         const int first_pos = bits ? k0 + (__ffsll((long long)bits) - 1) : -1;
 
-        // ---- segmented inclusive scan of (row closed, running sum)
-        V v = acc;
-        int f = first_pos >= 0;
+        // ---- segmented inclusive scan of (row closed, running sum) over the
+        // lanes that hold nonzeros; lane last_lane ends with the open sum
+        V v = lane <= last_lane ? acc : V(0);
+        int f = first_pos >= 0 || lane > last_lane;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             if (!__any_sync(0xffffffffu, !f && lane >= off)) break;
@@ -400,30 +538,19 @@ merge_path_spmv_kernel(const MPParams<V> p) {
                 f = pf;
             }
         }
-        if (__any_sync(0xffffffffu, !f)) {
-            if (!f) v = carry + v;  // the segment reaches back into the previous tile
-        }
-        V carry_in = __shfl_up_sync(0xffffffffu, v, 1);
-        if (lane == 0) carry_in = carry;
-        if (first_pos >= 0) sv.val[first_pos + sh] = carry_in + sv.val[first_pos + sh];
-        carry = __shfl_sync(0xffffffffu, v, 31);
+        const V carry_in = __shfl_up_sync(0xffffffffu, v, 1);
+        if (first_pos >= 0) sv.val[first_pos + sh] = lane == 0 ? first_sum : carry_in + first_sum;
+        carry = __shfl_sync(0xffffffffu, v, last_lane);
         __syncwarp();
 
         // ---- finished rows; the warp's first row end may be a cut row
-        const bool cut_head = head_pending && nrows > 0;
+        const bool cut_head = head_pending;
         V head_val = V(0);
-        for (int q = lane; q < nrows; q += 32) {
-            const int e = sv.re[q] - j0;
-            const int ep = q == 0 ? 0 : sv.re[q - 1] - j0;
-            const V sum = e > ep ? sv.val[e - 1 + sh] : (q == 0 ? carry_row0 : V(0));
-            if (q == 0 && cut_head) {
-                head_val = sum;
-            } else {
-                V res = sum;
-                if (p.mode & 1) res = p.alpha * res;
-                if (with_y) res = fma(p.beta, sv.yo[q], res);
-                store_stream(p.y + i0 + q, res, stream_pol);
-            }
+        switch (p.mode) {
+        case 0: head_val = finish_rows<V, 0>(p, sv, i0, j0, nrows, sh, carry_row0, cut_head, lane, stream_pol); break;
+        case 1: head_val = finish_rows<V, 1>(p, sv, i0, j0, nrows, sh, carry_row0, cut_head, lane, stream_pol); break;
+        case 2: head_val = finish_rows<V, 2>(p, sv, i0, j0, nrows, sh, carry_row0, cut_head, lane, stream_pol); break;
+        default: head_val = finish_rows<V, 3>(p, sv, i0, j0, nrows, sh, carry_row0, cut_head, lane, stream_pol);
         }
         if (cut_head) {
             head_pending = false;
@@ -433,15 +560,20 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         }  // nrows > 0
         __syncwarp();  // this stage may now be refilled
 
-        // ---- tile t + 2 goes into this stage
-        cur = nxt;
-        if (t + 2 < t_end) {
-            nxt = after;
-            issue_tile<V, VEC>(p, stage, bars + s, nxt, lane, stream_pol);
+        // ---- tile t + kStages goes into this stage
+        if (kStages == 2) {
+            cur = nxt;
+            if (t + 2 < t_end) {
+                nxt = after;
+                issue_tile<V, VEC>(p, stage, bars + s, nxt, lane, stream_pol);
+            }
+        } else {
+            cur = after;
+            if (t + 1 < t_end) issue_tile<V, VEC>(p, stage, bars + s, cur, lane, stream_pol);
         }
     }
 
-    if (sizeof(V) == 4 && parts_pending) carry += warp_sum(lane_part);
+    if (parts_pending) carry += warp_sum(lane_part);
     // ---- the row open at the end of the warp's run, if it has nonzeros here
     const int4 last_tile = tile_bounds(p.part, t_end - 1);
     const int ie = last_tile.z, je = last_tile.w;
@@ -457,9 +589,20 @@ merge_path_spmv_kernel(const MPParams<V> p) {
 
 int g_ctas_per_sm[2][33][2][64];  // occupancy per (type, IPL, VEC, device)
 
+// Tuning override of the CTAs per SM (SPMV_MP_CTAS_PER_SM, 0 = as many as
+// fit), read once.
+int ctas_per_sm_override() {
+    static const int v = [] {
+        const char *s = getenv("SPMV_MP_CTAS_PER_SM");
+        return s ? atoi(s) : 0;
+    }();
+    return v;
+}
+
+// CTAs of the kernel per SM (cached per device), with its attributes set:
+// as many as fit, and the rest of the SM's storage left to L1.
 template <typename V, int IPL, bool VEC>
-cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
-    if (a.num_tiles <= 0) return cudaSuccess;
+cudaError_t ctas_per_sm(int &out) {
     constexpr size_t smem = (size_t)kWarps * warp_region_bytes<V, IPL>();
     int dev = 0;
     cudaGetDevice(&dev);
@@ -471,9 +614,50 @@ cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
         int nb = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, merge_path_spmv_kernel<V, IPL, VEC>, kThreads, smem);
         if (e != cudaSuccess) return e;
-        per_sm = nb > 0 ? nb : 1;
+        int want = nb > 0 ? nb : 1;
+        if (ctas_per_sm_override() > 0 && ctas_per_sm_override() < want) want = ctas_per_sm_override();
+        // leave the rest of the SM's storage to L1, where the x gathers in
+        // flight live
+        const int pct = carveout_percent(want, smem);
+        if (pct >= 0) {
+            e = cudaFuncSetAttribute(merge_path_spmv_kernel<V, IPL, VEC>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+            if (e != cudaSuccess) return e;
+        }
+        per_sm = want;
     }
+    out = per_sm;
+    return cudaSuccess;
+}
+
+// Warps with a run of tiles: one per tile, as many as the GPU holds at once,
+// and more (queued behind the first wave; warps never wait for each other)
+// when a run would otherwise exceed max_run(IPL) tiles -- so that the sum of
+// a long row stays shallow at every size the interface accepts.  A term of
+// a row's sum passes, at most, through: the FMA chain of its lane (Q <= IPL
+// + 1), one addition per later tile of the run (K), the warp's tree (5), the
+// carry into the next tile's lane 0 and that lane's chain (1 + Q), the scan
+// (5), the pairwise sum over the warps the row spans (5 + 2 * 12 + 1), and
+// alpha and beta (2): 2 Q + K + 43 roundings.  With K <= 120 - 2 (IPL + 1)
+// that is at most 163, and 163 * 2^-24 < 1e-5, the fp32 accuracy bound (for
+// fp64, 163 * 2^-53 is far below 1e-13).  At most cap warps when cap > 0.
+long long max_run(int ipl) { return 120 - 2 * (ipl + 1); }
+long long warps_for(long long num_tiles, int per_sm, int ipl, int64_t cap) {
     const long long max_warps = (long long)per_sm * device_sm_count() * kWarps;
+    long long w = num_tiles < max_warps ? num_tiles : max_warps;
+    const long long run = max_run(ipl);
+    if (num_tiles > w * run) w = (num_tiles + run - 1) / run;
+    if (cap > 0 && w > cap) w = cap;
+    return w;
+}
+
+template <typename V, int IPL, bool VEC>
+cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
+    if (a.num_tiles <= 0) return cudaSuccess;
+    constexpr size_t smem = (size_t)kWarps * warp_region_bytes<V, IPL>();
+    int per_sm = 0;
+    cudaError_t e = ctas_per_sm<V, IPL, VEC>(per_sm);
+    if (e != cudaSuccess) return e;
     MPParams<V> p;
     p.m = a.m;
     p.nnz = a.nnz;
@@ -487,7 +671,7 @@ cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     p.mode = (p.alpha != V(1) ? 1 : 0) | (p.beta != V(0) ? 2 : 0);
     p.part = a.part;
     p.num_tiles = a.num_tiles;
-    p.num_warps = a.num_tiles < max_warps ? a.num_tiles : max_warps;
+    p.num_warps = warps_for(a.num_tiles, per_sm, IPL, a.max_warps);
     p.tail_partial = static_cast<V *>(a.tail_partial);
     p.head_partial = static_cast<V *>(a.head_partial);
     p.arrivals = a.arrivals;
@@ -509,7 +693,28 @@ cudaError_t launch_ipl(int ipl, const MergePathArgs &a, cudaStream_t stream) {
     }
 }
 
+template <typename V, bool VEC>
+cudaError_t ctas_ipl(int ipl, int &out) {
+    switch (ipl) {
+    case 8: return ctas_per_sm<V, 8, VEC>(out);
+    case 12: return ctas_per_sm<V, 12, VEC>(out);
+    case 16: return ctas_per_sm<V, 16, VEC>(out);
+    case 24: return ctas_per_sm<V, 24, VEC>(out);
+    case 32: return ctas_per_sm<V, 32, VEC>(out);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
+
+int64_t merge_path_num_warps(spmv_dtype_t dtype, int ipl, bool aligned, int64_t num_tiles) {
+    if (num_tiles <= 0) return 0;
+    int per_sm = 0;
+    cudaError_t e = dtype == SPMV_F64 ? (aligned ? ctas_ipl<double, true>(ipl, per_sm) : ctas_ipl<double, false>(ipl, per_sm))
+                                      : (aligned ? ctas_ipl<float, true>(ipl, per_sm) : ctas_ipl<float, false>(ipl, per_sm));
+    if (e != cudaSuccess) return -1;
+    return warps_for(num_tiles, per_sm, ipl, 0);
+}
 
 bool merge_path_supported(int ipl) { return ipl == 8 || ipl == 12 || ipl == 16 || ipl == 24 || ipl == 32; }
 
@@ -520,12 +725,14 @@ int merge_path_min_items() { return 8; }
 // Tile size from the row statistics.  Measured on GB300: matrices whose
 // nonzeros stay near the diagonal (the gathers of a tile hit few cache lines)
 // run best with large tiles, which spread the per-tile work over more
-// nonzeros; scattered columns run best with smaller ones, which keep fewer
-// gathers outstanding per SM (too many of them stall the whole memory
-// pipeline).  fp32: 24 items per lane when the bandwidth is below n/64, else
-// 12.  fp64: 12 when the bandwidth is below 4096, else 8.
+// nonzeros; scattered columns run best with smaller ones, which keep the
+// shared memory per SM small and so leave L1 room for the gathers in flight.
+// fp32: 24 items per lane when the bandwidth is below n/64, else 12.
+// fp64: 16 when the bandwidth is below 4096, else 12 (short rows in a band
+// of +-1024: 216 us at 16 against 236 us at 12 with two stages; skew: 242 us
+// at 12 against 287 us at 8).
 int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_t &s) {
-    if (dtype == SPMV_F64) return s.bandwidth <= 4096 ? 12 : 8;
+    if (dtype == SPMV_F64) return s.bandwidth <= 4096 ? 16 : 12;
     return (int64_t)s.bandwidth * 64 <= (int64_t)n ? 24 : 12;
 }
 

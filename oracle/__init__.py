@@ -301,9 +301,11 @@ def spmv_transposed(row_ptr, col_idx, vals, x, n: int, alpha=1.0, beta=0.0, y_ol
     return y, mag
 
 
-def spgemm(a_ptr, a_col, a_val, b_ptr, b_col, b_val, n: int):
+def spgemm(a_ptr, a_col, a_val, b_ptr, b_col, b_val, n: int, c_row_ptr=None):
     """C = A*B (A m-by-k, B k-by-n, CSR): (c_row_ptr int64, c_col, c_val),
-    columns in increasing order in each row, sums in long double."""
+    columns in increasing order in each row, sums in long double.  A first
+    call sizes the rows; c_row_ptr, when given (the row pointers of an
+    earlier call on the same patterns), takes its place."""
     a_ptr, a_col, b_ptr, b_col = _i32(a_ptr), _i32(a_col), _i32(b_ptr), _i32(b_col)
     f64 = np.asarray(a_val).dtype == np.float64
     t = np.float64 if f64 else np.float32
@@ -311,9 +313,13 @@ def spgemm(a_ptr, a_col, a_val, b_ptr, b_col, b_val, n: int):
     b_val = np.ascontiguousarray(b_val, dtype=t)
     m, k = len(a_ptr) - 1, len(b_ptr) - 1
     fn = lib().oracle_spgemm_f64 if f64 else lib().oracle_spgemm_f32
-    rp = np.empty(m + 1, dtype=np.int64)
-    if fn(m, k, n, _p(a_ptr), _p(a_col), _p(a_val), _p(b_ptr), _p(b_col), _p(b_val), _p(rp), None, None):
-        raise ValueError("oracle_spgemm: bad arguments")
+    if c_row_ptr is not None:
+        rp = np.array(c_row_ptr, dtype=np.int64)
+        assert len(rp) == m + 1
+    else:
+        rp = np.empty(m + 1, dtype=np.int64)
+        if fn(m, k, n, _p(a_ptr), _p(a_col), _p(a_val), _p(b_ptr), _p(b_col), _p(b_val), _p(rp), None, None):
+            raise ValueError("oracle_spgemm: bad arguments")
     col = np.empty(int(rp[-1]), dtype=np.int32)
     val = np.empty(int(rp[-1]), dtype=t)
     if fn(m, k, n, _p(a_ptr), _p(a_col), _p(a_val), _p(b_ptr), _p(b_col), _p(b_val), _p(rp), _p(col), _p(val)):

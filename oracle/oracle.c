@@ -377,7 +377,14 @@ ORACLE_SPMV_T(oracle_spmv_transposed_f64, double)
 ORACLE_SPMV_T(oracle_spmv_transposed_f32, float)
 
 /* Row by row: scatter every product of row i into a dense long double row
- * with a mark per column, then gather the marked columns in order. */
+ * with a mark per column, listing each column the first time a product
+ * lands on it; then sort that list and gather the row's entries in column
+ * order.  (Only the listed columns are visited, so a row costs its products
+ * plus the sort of its entries, not a pass over all n columns.) */
+static int cmp_i32(const void *a, const void *b) {
+    const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
 #define ORACLE_SPGEMM(NAME, T)                                                                            \
     int NAME(int32_t m, int32_t k, int32_t n, const int32_t *a_ptr, const int32_t *a_col, const T *a_val, \
              const int32_t *b_ptr, const int32_t *b_col, const T *b_val, int64_t *c_row_ptr,              \
@@ -386,27 +393,37 @@ ORACLE_SPMV_T(oracle_spmv_transposed_f32, float)
             return 1;                                                                                     \
         long double *acc = (long double *)calloc((size_t)(n > 0 ? n : 1), sizeof(long double));           \
         char *mark = (char *)calloc((size_t)(n > 0 ? n : 1), 1);                                          \
-        if (!acc || !mark) {                                                                              \
+        int32_t *touched = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));                  \
+        if (!acc || !mark || !touched) {                                                                  \
             free(acc);                                                                                    \
             free(mark);                                                                                   \
+            free(touched);                                                                                \
             return 1;                                                                                     \
         }                                                                                                 \
         c_row_ptr[0] = 0;                                                                                 \
         for (int32_t i = 0; i < m; ++i) {                                                                 \
+            int64_t nt = 0;                                                                               \
             for (int32_t p = a_ptr[i]; p < a_ptr[i + 1]; ++p) {                                           \
                 int32_t q = a_col[p];                                                                     \
                 if (q < 0 || q >= k) {                                                                    \
                     free(acc);                                                                            \
                     free(mark);                                                                           \
+                    free(touched);                                                                        \
                     return 1;                                                                             \
                 }                                                                                         \
                 for (int32_t r = b_ptr[q]; r < b_ptr[q + 1]; ++r) {                                       \
-                    acc[b_col[r]] += (long double)a_val[p] * (long double)b_val[r];                        \
-                    mark[b_col[r]] = 1;                                                                   \
+                    const int32_t j = b_col[r];                                                           \
+                    acc[j] += (long double)a_val[p] * (long double)b_val[r];                              \
+                    if (!mark[j]) {                                                                       \
+                        mark[j] = 1;                                                                      \
+                        touched[nt++] = j;                                                                \
+                    }                                                                                     \
                 }                                                                                         \
             }                                                                                             \
+            qsort(touched, (size_t)nt, sizeof(int32_t), cmp_i32);                                         \
             int64_t cnt = 0, out = c_row_ptr[i];                                                          \
-            for (int32_t j = 0; j < n; ++j)                                                               \
+            for (int64_t t = 0; t < nt; ++t) {                                                            \
+                const int32_t j = touched[t];                                                             \
                 if (mark[j]) {                                                                            \
                     if (c_col) {                                                                          \
                         c_col[out + cnt] = j;                                                             \
@@ -416,10 +433,12 @@ ORACLE_SPMV_T(oracle_spmv_transposed_f32, float)
                     mark[j] = 0;                                                                          \
                     acc[j] = 0.0L;                                                                        \
                 }                                                                                         \
+            }                                                                                             \
             c_row_ptr[i + 1] = c_row_ptr[i] + cnt;                                                        \
         }                                                                                                 \
         free(acc);                                                                                        \
         free(mark);                                                                                       \
+        free(touched);                                                                                    \
         return 0;                                                                                         \
     }
 ORACLE_SPGEMM(oracle_spgemm_f64, double)

@@ -35,9 +35,10 @@ def reference(A, B, rows=None):
         A = submatrix_rows(A, rows)
     rp, col, val = oracle.spgemm(A.row_ptr, A.col_idx, A.vals, B.row_ptr, B.col_idx, B.vals, B.n)
     ones = lambda v: np.ones(len(v), dtype=np.float64)
-    _, _, cnt = oracle.spgemm(A.row_ptr, A.col_idx, ones(A.vals), B.row_ptr, B.col_idx, ones(B.vals), B.n)
+    _, _, cnt = oracle.spgemm(A.row_ptr, A.col_idx, ones(A.vals), B.row_ptr, B.col_idx, ones(B.vals), B.n,
+                              c_row_ptr=rp)
     _, _, mag = oracle.spgemm(A.row_ptr, A.col_idx, np.abs(A.vals).astype(np.float64), B.row_ptr, B.col_idx,
-                              np.abs(B.vals).astype(np.float64), B.n)
+                              np.abs(B.vals).astype(np.float64), B.n, c_row_ptr=rp)
     return rp, col, val, cnt, mag
 
 
@@ -253,10 +254,13 @@ def test_spgemm_numeric_phase_again(dtype):
 
 @pytest.mark.parametrize("name", ["stencil27_128", "powerlaw_4M", "skew_8M"])
 def test_spgemm_full_size_square(name):
-    """C = A*A of a full-size workload: the pattern checked everywhere for
-    its invariants (columns strictly increasing in each row, inside [0, n)),
-    and the rows of a sample -- random rows plus the rows with the most
-    products, which are the dense bin's -- against the oracle."""
+    """C = A*A of a full-size workload, every row of C against the oracle:
+    row sizes and columns exactly, values within the summation bound.  The
+    oracle runs on blocks of rows in threads (plain C through ctypes, which
+    releases the interpreter lock; its arithmetic is unchanged), and each
+    block is compared as it comes so that host memory stays bounded."""
+    import concurrent.futures as cf
+    import os
     import torch
     import load_balanced_csr_gb300 as lb
     A = synth.workload(name).A
@@ -267,24 +271,28 @@ def test_spgemm_full_size_square(name):
         assert h.device_status() == 0
         info = h.info()
     assert rp[0].item() == 0 and rp[-1].item() == h.c_nnz
-    lens = rp[1:] - rp[:-1]
-    assert bool((lens >= 0).all())
-    if h.c_nnz > 1:
-        same_row = torch.repeat_interleave(torch.arange(A.m, device="cuda"), lens.long())
-        inc = (col[1:] > col[:-1]) | (same_row[1:] != same_row[:-1])
-        assert bool(inc.all()), "columns not strictly increasing within rows"
-        assert int(col.min()) >= 0 and int(col.max()) < A.n
     bl = np.diff(A.row_ptr).astype(np.int64)
     prod = np.add.reduceat(np.concatenate([bl[A.col_idx], [0]]), A.row_ptr[:-1])
     prod = np.where(np.diff(A.row_ptr) > 0, prod, 0)
     assert info["products"] == int(prod.sum())
-    heavy = np.argsort(prod, kind="stable")[-40:]
-    sample = np.unique(np.concatenate([np.random.default_rng(0).integers(0, A.m, 3000), heavy]))
-    r_rp, r_col, r_val, cnt, mag = reference(A, A, rows=sample)
     rp_h = rp.cpu().numpy().astype(np.int64)
-    pos = np.concatenate([np.arange(rp_h[r], rp_h[r + 1]) for r in sample])
-    np.testing.assert_array_equal(np.diff(rp_h)[sample], np.diff(r_rp), err_msg=f"{name}: row sizes")
-    got_col = col[torch.from_numpy(pos).cuda()].cpu().numpy()
-    got_val = val[torch.from_numpy(pos).cuda()].cpu().numpy()
-    np.testing.assert_array_equal(got_col, r_col, err_msg=f"{name}: columns")
-    check_values(got_val, r_val, cnt, mag, A.dtype, f"{name} A*A")
+    nb = 2 * (os.cpu_count() or 4)  # few blocks: each oracle call allocates an n-long accumulator
+    edges = np.linspace(0, A.m, nb + 1).astype(np.int64)
+    blocks = [(int(edges[i]), int(edges[i + 1])) for i in range(nb) if edges[i + 1] > edges[i]]
+
+    def block_reference(b):  # rows [r0, r1) of A as a CSR matrix of their own (views, no copies)
+        r0, r1 = b
+        lo, hi = int(A.row_ptr[r0]), int(A.row_ptr[r1])
+        sub = synth.CSR(r1 - r0, A.n, (A.row_ptr[r0:r1 + 1] - lo).astype(np.int32), A.col_idx[lo:hi],
+                        A.vals[lo:hi])
+        return reference(sub, A)
+
+    checked = 0
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        for (r0, r1), (r_rp, r_col, r_val, cnt, mag) in zip(blocks, ex.map(block_reference, blocks)):
+            np.testing.assert_array_equal(np.diff(rp_h[r0:r1 + 1]), np.diff(r_rp), err_msg=f"{name}: row sizes")
+            lo, hi = int(rp_h[r0]), int(rp_h[r1])
+            np.testing.assert_array_equal(col[lo:hi].cpu().numpy(), r_col, err_msg=f"{name}: columns")
+            check_values(val[lo:hi].cpu().numpy(), r_val, cnt, mag, A.dtype, f"{name} A*A rows {r0}..{r1}")
+            checked += r1 - r0
+    assert checked == A.m

@@ -125,7 +125,7 @@ def test_transpose_degenerate_and_checks():
 @pytest.mark.parametrize("name", ["skew_8M", "powerlaw_4M"])
 def test_transpose_full_size(name):
     """Full-size matrices: the whole transpose bit for bit, and the product
-    on sampled columns plus the sum of y against 1^T A x."""
+    in every column against the oracle."""
     import torch
     W = synth.workload(name)
     A = W.A
@@ -140,7 +140,5 @@ def test_transpose_full_size(name):
     torch.cuda.synchronize()
     got = yd.cpu().numpy()
     assert np.all(np.isfinite(got))
-    cols = np.unique(np.concatenate([np.random.default_rng(0).integers(0, A.n, 20000),
-                                     np.argsort(np.diff(tp))[-200:]]))
-    check_product(A, x, None, got, 1.0, 0.0, f"A^T x {name}", cols=cols)
+    check_product(A, x, None, got, 1.0, 0.0, f"A^T x {name}")
     plan.close()
