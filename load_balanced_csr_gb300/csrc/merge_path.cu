@@ -256,23 +256,17 @@ template <typename V, int MODE>
 __device__ __forceinline__ V finish_rows(const MPParams<V> &p, const StageView<V> &sv, int i0, int j0, int nrows,
                                          int sh, V carry_row0, bool cut_head, int lane, uint64_t pol) {
     V head_val = V(0);
-    int prev_last = 0;  // end of the row before this round's first (tile-relative)
-    for (int base = 0; base < nrows; base += 32) {
-        const int q = base + lane;
-        const int e = q < nrows ? sv.re[q] - j0 : 0;
-        const int up = __shfl_up_sync(0xffffffffu, e, 1);
-        const int ep = lane == 0 ? prev_last : up;
-        prev_last = __shfl_sync(0xffffffffu, e, 31);
-        if (q < nrows) {
-            const V sum = e > ep ? sv.val[e - 1 + sh] : (q == 0 ? carry_row0 : V(0));
-            if (q == 0 && cut_head) {
-                head_val = sum;
-            } else {
-                V res = sum;
-                if (MODE & 1) res = p.alpha * res;
-                if (MODE & 2) res = fma(p.beta, sv.yo[q], res);
-                store_stream(p.y + i0 + q, res, pol);
-            }
+    for (int q = lane; q < nrows; q += 32) {
+        const int e = sv.re[q] - j0;
+        const int ep = q == 0 ? 0 : sv.re[q - 1] - j0;
+        const V sum = e > ep ? sv.val[e - 1 + sh] : (q == 0 ? carry_row0 : V(0));
+        if (q == 0 && cut_head) {
+            head_val = sum;
+        } else {
+            V res = sum;
+            if (MODE & 1) res = p.alpha * res;
+            if (MODE & 2) res = fma(p.beta, sv.yo[q], res);
+            store_stream(p.y + i0 + q, res, pol);
         }
     }
     return head_val;
@@ -336,8 +330,20 @@ __device__ void cut_row(const MPParams<V> &p, int lane, int lane_with_value, V p
     }
 }
 
+// Resident CTAs the register allocation must allow (0: the compiler's
+// choice).  LBCSR_MP_FP64_MIN_CTAS sets it for fp64 tiles of at most 12
+// items per lane, for tuning.
+template <typename V, int IPL>
+constexpr int min_ctas() {
+#ifdef LBCSR_MP_FP64_MIN_CTAS
+    return sizeof(V) == 8 && IPL <= 12 ? LBCSR_MP_FP64_MIN_CTAS : 0;
+#else
+    return 0;
+#endif
+}
+
 template <typename V, int IPL, bool VEC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, min_ctas<V, IPL>())
 merge_path_spmv_kernel(const MPParams<V> p) {
     constexpr int T = 32 * IPL;
     constexpr int kStages = stages_for<V, IPL>();
@@ -455,7 +461,8 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         } else {
         // lanes past the tile's last nonzero take no part (lane 0 always
         // does: it brings the carried sum)
-        const int last_lane = nnzt > 0 ? (nnzt - 1) / Q : 0;
+        const unsigned holding = __ballot_sync(0xffffffffu, run > 0);
+        const int last_lane = holding ? 31 - __clz(holding) : 0;
         if (parts_pending) {
             carry += warp_sum(lane_part);
             lane_part = V(0);
@@ -469,30 +476,10 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const bool row0_ends_first = sv.re[0] == j0;
         const V carry_row0 = row0_ends_first ? carry : V(0);
         if (row0_ends_first) carry = V(0);
-        {
-            // lane L takes the block of rows [L nrows / 32, (L + 1) nrows / 32):
-            // their ends increase, so the lane collects the bits of one word
-            // at a time in a register and ORs each word in once (lanes share
-            // a word only at the edges of their blocks)
-            const int r_lo = (lane * nrows) >> 5;
-            const int r_hi = ((lane + 1) * nrows) >> 5;
-            int prev = r_lo == 0 ? 0 : sv.re[r_lo - 1] - j0;
-            int word = -1;
-            unsigned mask = 0u;
-            for (int r = r_lo; r < r_hi; ++r) {
-                const int e = sv.re[r] - j0;
-                if (e > prev) {
-                    const int w = (e - 1) >> 5;
-                    if (w != word) {
-                        if (mask) atomicOr(sv.bm + word, mask);
-                        word = w;
-                        mask = 0u;
-                    }
-                    mask |= 1u << ((e - 1) & 31);
-                }
-                prev = e;
-            }
-            if (mask) atomicOr(sv.bm + word, mask);
+        for (int r = lane; r < nrows; r += 32) {
+            const int e = sv.re[r] - j0;
+            const int ep = r == 0 ? 0 : sv.re[r - 1] - j0;
+            if (e > ep) atomicOr(sv.bm + ((e - 1) >> 5), 1u << ((e - 1) & 31));
         }
         __syncwarp();
         // bit i of `bits`: nonzero k0 + i is the last of a row in this tile
@@ -502,10 +489,13 @@ merge_path_spmv_kernel(const MPParams<V> p) {
         const unsigned long long run_mask = run >= 64 ? ~0ull : ((1ull << run) - 1);
         const unsigned long long bits = shifted & run_mask;
 
-        // ---- add the run up.  Lane 0 starts from the carried sum.  A lane's
-        // first closed row stays in a register (it still lacks the sum
-        // carried in from earlier lanes); later closed rows go to the slot
-        // of their last nonzero, which no other lane touches.
+        // ---- add the run up.  Lane 0 starts from the carried sum.  A closed
+        // row's sum goes to the slot of its last nonzero, which no other lane
+        // touches.  fp64 keeps a lane's first closed row in a register
+        // instead (it still lacks the sum carried in from earlier lanes), so
+        // that the carry is added once, in registers; fp32, whose walk runs
+        // fully predicated, keeps the walk short and adds the carry to the
+        // slot afterwards.
         V acc = lane == 0 ? carry : V(0);
         V first_sum = V(0);
         bool closed = false;
@@ -516,13 +506,14 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             if (sizeof(V) == 8 && i >= Q) break;
             acc = fma(vr[i], xr[i], acc);  // vr[i] = 0 past the run
             if ((bits >> i) & 1ull) {
-                if (closed) sv.val[k0 + i + sh] = acc;
+                if (sizeof(V) == 4 || closed) sv.val[k0 + i + sh] = acc;
                 else first_sum = acc;
                 closed = true;
                 acc = V(0);
             }
         }
         const int first_pos = bits ? k0 + (__ffsll((long long)bits) - 1) : -1;
+        if (sizeof(V) == 4 && first_pos >= 0) first_sum = sv.val[first_pos + sh];
 
         // ---- segmented inclusive scan of (row closed, running sum) over the
         // lanes that hold nonzeros; lane last_lane ends with the open sum
