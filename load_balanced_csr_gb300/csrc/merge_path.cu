@@ -331,15 +331,17 @@ __device__ void cut_row(const MPParams<V> &p, int lane, int lane_with_value, V p
 }
 
 // Resident CTAs the register allocation must allow (0: the compiler's
-// choice).  LBCSR_MP_FP64_MIN_CTAS sets it for fp64 tiles of at most 12
-// items per lane, for tuning.
+// choice).  LBCSR_MP_FP64_MIN_CTAS and LBCSR_MP_FP32_MIN_CTAS set it for
+// tiles of at most 12 items per lane, for tuning.
+#ifndef LBCSR_MP_FP64_MIN_CTAS
+#define LBCSR_MP_FP64_MIN_CTAS 0
+#endif
+#ifndef LBCSR_MP_FP32_MIN_CTAS
+#define LBCSR_MP_FP32_MIN_CTAS 0
+#endif
 template <typename V, int IPL>
 constexpr int min_ctas() {
-#ifdef LBCSR_MP_FP64_MIN_CTAS
-    return sizeof(V) == 8 && IPL <= 12 ? LBCSR_MP_FP64_MIN_CTAS : 0;
-#else
-    return 0;
-#endif
+    return IPL > 12 ? 0 : sizeof(V) == 8 ? LBCSR_MP_FP64_MIN_CTAS : LBCSR_MP_FP32_MIN_CTAS;
 }
 
 template <typename V, int IPL, bool VEC>
