@@ -111,7 +111,10 @@ template <typename V, int KB, int KP>
 __device__ __forceinline__ void spmm_warp_row(const SpmmParams<V> &p, long long j, long long stop, int lane,
                                               V (&acc)[KB]) {
     constexpr int S = 32 / KP;
-    constexpr int U = 8;
+#ifndef LBCSR_SPMM_WARP_U
+#define LBCSR_SPMM_WARP_U 8
+#endif
+    constexpr int U = LBCSR_SPMM_WARP_U;  // warp steps of loads in flight
     const int slot = lane / KP;
     const int tcol = lane % KP;
 #pragma unroll
@@ -156,7 +159,11 @@ template <typename V, int KP>
 __device__ __forceinline__ void spmm_subwarp_rows(const SpmmParams<V> &p, long long r0, long long r1, int lane,
                                                   uint64_t pol) {
     constexpr int S = 32 / KP;
-    constexpr int U = 4;  // the tree below adds exactly four sums
+#ifndef LBCSR_SPMM_SUB_U
+#define LBCSR_SPMM_SUB_U 8
+#endif
+    constexpr int U = LBCSR_SPMM_SUB_U;  // nonzeros in flight per row: 4, 8 or 16 (the tree below)
+    static_assert(U == 4 || U == 8 || U == 16, "four, eight or sixteen sums");
     const int sub = lane / KP;
     const int tcol = lane % KP;
     const bool col_ok = tcol < p.k;
@@ -188,7 +195,11 @@ __device__ __forceinline__ void spmm_subwarp_rows(const SpmmParams<V> &p, long l
             q += U;
         }
         if (has_row && col_ok) {
-            V y = p.alpha * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+#pragma unroll
+            for (int w = U / 2; w > 0; w >>= 1)  // pairwise: sums u and u + w
+#pragma unroll
+                for (int u = 0; u < w; ++u) acc[u] = acc[u] + acc[u + w];
+            V y = p.alpha * acc[0];
             if (p.beta != V(0)) y = fma(p.beta, p.Y[r * p.ldy + tcol], y);
             store_stream(p.Y + r * p.ldy + tcol, y, pol);
         }
