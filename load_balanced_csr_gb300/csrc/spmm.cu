@@ -148,13 +148,17 @@ __device__ __forceinline__ void spmm_warp_row(const SpmmParams<V> &p, long long 
 }
 
 // The rows that lie wholly inside a warp's run, [r0, r1), summed by
-// sub-warps of KP lanes (KB == 1): sub-warp s takes rows r0 + s, r0 + s + S,
-// ..., walks each row's nonzeros in order (lanes over columns) and writes
-// its row of Y.  S rows are in flight at once, which matters for short
-// rows.  A row longer than kSpmmSubRowMax would hold up the other
-// sub-warps: the whole warp sums it right after its group.
+// sub-warps of KP lanes (KB == 1), lanes over columns: S rows are in flight
+// at once, which matters for short rows.  A row longer than kSpmmSubRowMax
+// would hold up the warp: the whole warp sums it.
 constexpr int kSpmmSubRowMax = 64;
 
+// Each sub-warp walks its own rows, r0 + s, r0 + s + S, ..., one after the
+// other: a sub-warp that finishes a short row starts its next row at once
+// instead of waiting for the longest row of a group (power-law rows are
+// heavy-tailed).  The next row's bounds are loaded one row ahead.  Rows
+// longer than kSpmmSubRowMax are skipped here and summed by the whole warp
+// afterwards, in row order.
 template <typename V, int KP>
 __device__ __forceinline__ void spmm_subwarp_rows(const SpmmParams<V> &p, long long r0, long long r1, int lane,
                                                   uint64_t pol) {
@@ -167,51 +171,84 @@ __device__ __forceinline__ void spmm_subwarp_rows(const SpmmParams<V> &p, long l
     const int sub = lane / KP;
     const int tcol = lane % KP;
     const bool col_ok = tcol < p.k;
-    for (long long rr = r0; rr < r1; rr += S) {
-        const long long r = rr + sub;
-        const bool in = r < r1;
-        long long q = in ? p.row_ptr[r] : 0;
-        const long long e = in ? p.row_ptr[r + 1] : 0;
-        const bool is_long = e - q > kSpmmSubRowMax;
-        const bool has_row = in && !is_long;
-        if (!has_row) q = e;
-        V acc[U];  // nonzero q goes to sum q mod U (added as a tree below)
-#pragma unroll
-        for (int u = 0; u < U; ++u) acc[u] = V(0);
-        while (__any_sync(0xffffffffu, q < e)) {
-            int cc[U];
-            V vv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                cc[u] = q + u < e ? ld_stream(p.col_idx + q + u) : -1;
-                vv[u] = q + u < e ? ld_stream(p.vals + q + u) : V(0);
-            }
-            V xv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                xv[u] = cc[u] >= 0 && col_ok ? ld_gather(p.X + (long long)cc[u] * p.ldx + tcol) : V(0);
-#pragma unroll
-            for (int u = 0; u < U; ++u) acc[u] = fma(vv[u], xv[u], acc[u]);
-            q += U;
+    // this sub-warp's current short row [q, e) and the next row's bounds
+    long long r = r0 + sub;
+    long long q = 0, e = 0;
+    if (r < r1) {
+        q = p.row_ptr[r];
+        e = p.row_ptr[r + 1];
+    }
+    while (r < r1 && e - q > kSpmmSubRowMax) {  // skip long rows
+        r += S;
+        if (r < r1) {
+            q = p.row_ptr[r];
+            e = p.row_ptr[r + 1];
         }
-        if (has_row && col_ok) {
+    }
+    long long nq = 0, ne = 0;
+    if (r + S < r1) {
+        nq = p.row_ptr[r + S];
+        ne = p.row_ptr[r + S + 1];
+    }
+    V acc[U];  // nonzero q goes to sum (q - row start) mod U, added pairwise at the row's end
 #pragma unroll
-            for (int w = U / 2; w > 0; w >>= 1)  // pairwise: sums u and u + w
+    for (int u = 0; u < U; ++u) acc[u] = V(0);
+    while (__any_sync(0xffffffffu, r < r1)) {
+        const bool live = r < r1;
+        int cc[U];
+        V vv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            cc[u] = live && q + u < e ? ld_stream(p.col_idx + q + u) : -1;
+            vv[u] = live && q + u < e ? ld_stream(p.vals + q + u) : V(0);
+        }
+        V xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            xv[u] = cc[u] >= 0 && col_ok ? ld_gather(p.X + (long long)cc[u] * p.ldx + tcol) : V(0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = fma(vv[u], xv[u], acc[u]);
+        q += U;
+        if (live && q >= e) {  // the row is done: write it, move to the next short row
+#pragma unroll
+            for (int w = U / 2; w > 0; w >>= 1)
 #pragma unroll
                 for (int u = 0; u < w; ++u) acc[u] = acc[u] + acc[u + w];
-            V y = p.alpha * acc[0];
-            if (p.beta != V(0)) y = fma(p.beta, p.Y[r * p.ldy + tcol], y);
-            store_stream(p.Y + r * p.ldy + tcol, y, pol);
+            if (col_ok) {
+                V y = p.alpha * acc[0];
+                if (p.beta != V(0)) y = fma(p.beta, p.Y[r * p.ldy + tcol], y);
+                store_stream(p.Y + r * p.ldy + tcol, y, pol);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc[u] = V(0);
+            r += S;
+            q = nq;
+            e = ne;
+            while (r < r1 && e - q > kSpmmSubRowMax) {
+                r += S;
+                if (r < r1) {
+                    q = p.row_ptr[r];
+                    e = p.row_ptr[r + 1];
+                }
+            }
+            if (r + S < r1) {
+                nq = p.row_ptr[r + S];
+                ne = p.row_ptr[r + S + 1];
+            }
         }
-        // the group's long rows, one by one, by the whole warp
-        unsigned longs = __ballot_sync(0xffffffffu, in && is_long && tcol == 0);
+    }
+    // the run's long rows, one by one, by the whole warp
+    for (long long base = r0; base < r1; base += 32) {
+        const long long rl = base + lane;
+        const bool is_long = rl < r1 && (long long)p.row_ptr[rl + 1] - p.row_ptr[rl] > kSpmmSubRowMax;
+        unsigned longs = __ballot_sync(0xffffffffu, is_long);
         while (longs) {
             const int l = __ffs(longs) - 1;
             longs &= longs - 1;
-            const long long rl = rr + l / KP;
+            const long long row = base + l;
             V a[1];
-            spmm_warp_row<V, 1, KP>(p, p.row_ptr[rl], p.row_ptr[rl + 1], lane, a);
-            spmm_store_row<V, 1, KP>(p, rl, a, lane, pol);
+            spmm_warp_row<V, 1, KP>(p, p.row_ptr[row], p.row_ptr[row + 1], lane, a);
+            spmm_store_row<V, 1, KP>(p, row, a, lane, pol);
         }
     }
 }
