@@ -832,7 +832,11 @@ spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const v
     // on the merge path)
     const bool rare_long = p->spmm_num_long > 0 && (int64_t)p->spmm_num_long * kSpmmRowsPerLongRow <= p->m &&
                            k <= (p->dtype == SPMV_F64 ? 32 : 64);
-    if ((p->stats.max_len <= kRowSpmmMaxLen || rare_long) && row_spmm_supported(p->dtype, k, X, ldx, Y, ldy)) {
+#ifndef LBCSR_SPMM_CSR_PATH
+#define LBCSR_SPMM_CSR_PATH 1  // 0: the merge-path SpMM takes these matrices too (tuning)
+#endif
+    if (LBCSR_SPMM_CSR_PATH && (p->stats.max_len <= kRowSpmmMaxLen || rare_long) &&
+        row_spmm_supported(p->dtype, k, X, ldx, Y, ldy)) {
         // a warp per 32 rows straight from CSR, lanes sharing X rows; rows
         // longer than kRowSpmmMaxLen, if any, by a warp per 4096-nonzero segment
         RowSpmmArgs r;

@@ -64,6 +64,35 @@ def test_spmm_random(dtype, k):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_spmm_wide_lanes_and_fallbacks(dtype):
+    """16-byte lanes where X's layout allows them and one value per lane
+    where it does not: X aligned with k and ldx multiples of the values per
+    16 bytes; X starting one value past an aligned address; a row stride
+    that is not such a multiple; k with idle lanes in a row's lane group.
+    Rows of up to 300 nonzeros, so that the whole-warp walk runs too."""
+    import torch
+    import load_balanced_csr_gb300 as lb
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 12, size=6000).astype(np.int32)
+    lens[rng.choice(6000, 40, replace=False)] = rng.integers(65, 300, size=40)
+    A = synth.fill_random(lens, 5000, dist=synth.DIST_NORMAL, seed=21, dtype=dtype)
+    t = torch.float64 if dtype == "f64" else torch.float32
+    rp, col, val = to_gpu(A)
+    with lb.Plan(rp, col, val, A.n, kernel="merge_path", with_spmm=True) as plan:
+        for k, offset, ld in [(8, 0, 8), (8, 1, 12), (8, 0, 10), (12, 0, 12), (24, 0, 28), (128, 0, 128)]:
+            X, Y0 = dense_inputs(A, k, k + offset)
+            flat = torch.zeros(A.n * ld + offset, dtype=t, device="cuda")
+            Xg = flat[offset:].view(A.n, ld)[:, :k]
+            Xg.copy_(torch.from_numpy(X).cuda())
+            assert Xg.stride(0) == ld and (Xg.data_ptr() % 16 != 0) == (offset != 0)
+            Yg = torch.from_numpy(Y0).cuda()
+            plan.execute_multi(Xg, Yg, 1.25, 0.5)
+            torch.cuda.synchronize()
+            assert plan.device_status() == 0
+            check(A, X, Y0, Yg, 1.25, 0.5, f"spmm {dtype} k={k} offset={offset} ldx={ld}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
 def test_spmm_rare_long_rows(dtype):
     """A few long rows among many short ones (at most one per 4096 rows):
     with k a multiple of the values per 16 bytes, the short rows go to the
