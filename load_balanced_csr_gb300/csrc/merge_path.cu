@@ -720,13 +720,14 @@ int merge_path_min_items() { return 8; }
 // run best with large tiles, which spread the per-tile work over more
 // nonzeros; scattered columns run best with smaller ones, which keep the
 // shared memory per SM small and so leave L1 room for the gathers in flight.
-// fp32: 24 items per lane when the bandwidth is below n/64, else 12.
+// fp32: 24 items per lane when the bandwidth is below n/64, else 16 (power
+// law: 266-268 us at 16 against 269-274 us at 12 and 286 us at 8).
 // fp64: 16 when the bandwidth is below 4096, else 12 (short rows in a band
 // of +-1024: 216 us at 16 against 236 us at 12 with two stages; skew: 242 us
-// at 12 against 287 us at 8).
+// at 12 against 262 us at 16 and 287 us at 8).
 int merge_path_choose_items(spmv_dtype_t dtype, int32_t n, const spmv_row_stats_t &s) {
     if (dtype == SPMV_F64) return s.bandwidth <= 4096 ? 16 : 12;
-    return (int64_t)s.bandwidth * 64 <= (int64_t)n ? 24 : 12;
+    return (int64_t)s.bandwidth * 64 <= (int64_t)n ? 24 : 16;
 }
 
 cudaError_t launch_merge_path_spmv(spmv_dtype_t dtype, int ipl, const MergePathArgs &a, cudaStream_t stream) {
