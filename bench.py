@@ -434,6 +434,7 @@ def per_config_entry(name: str, dev, warmup: int, min_runs: int, min_seconds: fl
     bc, bc_beta = compulsory_bytes(A), compulsory_bytes(A, W.beta)
     peak, peak_kind = measured_peak()
     gbs = bc / (med * 1e-6) / 1e9
+    traffic = recorded_traffic(name, info["kernel_name"])[0]
     entry = {
         "workload": name, "description": W.description, "kernel": info["kernel_name"], "dtype": A.dtype,
         "m": A.m, "n": A.n, "nnz": A.nnz, "alpha": W.alpha, "beta": W.beta, "runs": runs, "warmup": max(warmup, 10),
@@ -447,6 +448,11 @@ def per_config_entry(name: str, dev, warmup: int, min_runs: int, min_seconds: fl
                      "frac_of_spec_8tbs": round(gbs / SPEC_HBM_GBS, 4),
                      "frac_of_copy_this_run": round(gbs / copy_gbs, 4) if copy_gbs else None,
                      "meets_70pct": bool(gbs / peak >= 0.70)},
+        # DRAM bytes per launch from the committed ncu capture of this kernel on
+        # this workload, when it was taken on the current sources (else null),
+        # and their ratio to the bytes the product needs
+        "traffic": traffic,
+        "traffic_over_needed": round(traffic / bc_beta, 3) if traffic else None,
         "plan_ms": round(plan_ms, 3), "launches_per_execute": info["launches_per_execute"],
         "items_per_tile": info["items_per_tile"], "num_tiles": info["num_tiles"],
         "device_status": status, "clocks": clocks,
