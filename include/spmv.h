@@ -201,6 +201,25 @@ spmv_status_t spmv_execute(spmv_plan_t plan, double alpha, const void *x, double
                            spmv_stream_t stream);
 
 /*
+ * The same product with x and y in HOST memory (x_host[n], y_host[m] of
+ * the plan's value type): on `stream`, copy x_host into the caller's
+ * device buffer x_dev[n] (and y_host into y_dev[m] when beta != 0), run
+ * spmv_execute(plan, alpha, x_dev, beta, y_dev, stream), and copy y_dev
+ * back into y_host -- one cudaMemcpyAsync per copy.  Asynchronous like
+ * spmv_execute: y_host holds the result once the stream has passed the
+ * last copy (synchronise the stream before reading it).  For copies that
+ * overlap other work the host buffers should be page-locked
+ * (cudaHostAlloc, or pinned torch tensors); pageable memory also works.
+ * x_dev and y_dev must not overlap each other or the plan's arrays.
+ * Allocates nothing.  This is the call an application with its vectors on
+ * the host makes; the product itself is the one above.
+ * Errors: as spmv_execute, INVALID_ARG also for a null host or device
+ * buffer the sizes need, CUDA when a copy cannot be queued.
+ */
+spmv_status_t spmv_execute_host(spmv_plan_t plan, double alpha, const void *x_host, double beta, void *y_host,
+                                void *x_dev, void *y_dev, spmv_stream_t stream);
+
+/*
  * Y = alpha * A * X + beta * Y for k right-hand sides ("A GPU
  * load-balancing programming model", section 4.3, Listing 4: the row loop
  * of SpMV with an inner loop over the columns of a dense matrix).  X is

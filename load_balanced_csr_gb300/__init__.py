@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "spmv_plan_create_ex": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int,
                                     ctypes.POINTER(Options), vp],
             "spmv_execute": [vp, dbl, vp, dbl, vp, vp],
+            "spmv_execute_host": [vp, dbl, vp, dbl, vp, vp, vp, vp],
             "spmv_plan_update_values": [vp, vp, vp],
             "spmv_plan_destroy": [vp],
             "spmv_plan_info": [vp, ctypes.POINTER(PlanInfo)],
@@ -195,6 +196,24 @@ class Plan:
         check(lib().spmv_execute(self._h, float(alpha), _ptr(x), float(beta), _ptr(y), _stream_handle(stream)),
               "spmv_execute")
         return y
+
+    def execute_host(self, x_host, y_host, x_dev, y_dev, alpha: float = 1.0, beta: float = 0.0, stream=None):
+        """y_host = alpha*A*x_host + beta*y_host with x_host and y_host CPU
+        tensors (pinned for asynchronous copies): the library copies them
+        through the device buffers x_dev and y_dev on the stream.  y_host
+        holds the result once the stream has been synchronised."""
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        for t in (x_host, y_host, x_dev, y_dev):
+            if t.dtype != self.dtype or not t.is_contiguous():
+                raise TypeError("buffers must be contiguous and of the plan's value type")
+        if x_host.numel() != self.n or x_dev.numel() != self.n or y_host.numel() != self.m or y_dev.numel() != self.m:
+            raise ValueError("x buffers must have n and y buffers m entries")
+        if x_host.is_cuda or y_host.is_cuda or not x_dev.is_cuda or not y_dev.is_cuda:
+            raise TypeError("x_host and y_host must be CPU tensors, x_dev and y_dev CUDA tensors")
+        check(lib().spmv_execute_host(self._h, float(alpha), _ptr(x_host), float(beta), _ptr(y_host), _ptr(x_dev),
+                                      _ptr(y_dev), _stream_handle(stream)), "spmv_execute_host")
+        return y_host
 
     def execute_multi(self, X, Y, alpha: float = 1.0, beta: float = 0.0, stream=None):
         """Y = alpha*A*X + beta*Y for a row-major X (n-by-k) and Y (m-by-k);

@@ -771,6 +771,28 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     return SPMV_OK;
 }
 
+spmv_status_t spmv_execute_host(spmv_plan_t p, double alpha, const void *x_host, double beta, void *y_host,
+                                void *x_dev, void *y_dev, spmv_stream_t stream_handle) {
+    if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");
+    if (p->m == 0) return SPMV_OK;
+    if (!y_host || !y_dev) return fail(SPMV_ERR_INVALID_ARG, "y_host or y_dev is NULL");
+    if (p->nnz > 0 && (!x_host || !x_dev)) return fail(SPMV_ERR_INVALID_ARG, "x_host or x_dev is NULL");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    const size_t vs = value_size(p->dtype);
+    cudaError_t e = cudaSuccess;
+    if (p->nnz > 0) e = cudaMemcpyAsync(x_dev, x_host, vs * (size_t)p->n, cudaMemcpyHostToDevice, stream);
+    // y is read when beta, rounded to the value type, is not zero
+    const bool reads_y = p->dtype == SPMV_F64 ? beta != 0.0 : (float)beta != 0.0f;
+    if (e == cudaSuccess && reads_y)
+        e = cudaMemcpyAsync(y_dev, y_host, vs * (size_t)p->m, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_host copy to the device");
+    const spmv_status_t st = spmv_execute(p, alpha, p->nnz > 0 ? x_dev : nullptr, beta, y_dev, stream_handle);
+    if (st != SPMV_OK) return st;
+    e = cudaMemcpyAsync(y_host, y_dev, vs * (size_t)p->m, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "spmv_execute_host copy to the host");
+    return SPMV_OK;
+}
+
 spmv_status_t spmv_execute_multi(spmv_plan_t p, int32_t k, double alpha, const void *X, int64_t ldx, double beta,
                                  void *Y, int64_t ldy, spmv_stream_t stream_handle) {
     if (!p) return fail(SPMV_ERR_INVALID_ARG, "plan is NULL");

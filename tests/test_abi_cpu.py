@@ -44,6 +44,7 @@ def test_argument_errors_need_no_device():
     assert L.spmv_plan_create_ex(ctypes.byref(h), 1, 1, 0, fake, None, None, 0, ctypes.byref(opt), None) == 1
     # execute / info / export / destroy on a null plan
     assert L.spmv_execute(None, 1.0, fake, 0.0, fake, None) == 1
+    assert L.spmv_execute_host(None, 1.0, fake, 0.0, fake, fake, fake, None) == 1
     assert L.spmv_plan_info(None, None) == 1
     assert L.spmv_plan_export(None, 0, None, 0, None) == 1
     assert L.spmv_plan_update_values(None, fake, None) == 1
