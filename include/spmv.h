@@ -330,6 +330,11 @@ spmv_status_t spmv_noalloc_device_status(int32_t *flags);
  * 0 = no failure.  Bit 0: a kernel's wait for its tile copies ran past its
  * time limit (about a second); the kernel then stopped that part of the work
  * instead of waiting forever, so the y of that product is incomplete.
+ * Bit 2 (value 4), debug build only (libspmv_debug.so, compiled with
+ * -DSPMV_DEBUG): an SpMV kernel met a column index outside [0, n) -- an
+ * array changed after the plan was created, which the plan borrows
+ * unmodified -- and gathered x[0] in its place; that y is wrong.  The
+ * release build does not check (creation validates every index once).
  */
 spmv_status_t spmv_plan_device_status(spmv_plan_t plan, int32_t *flags);
 

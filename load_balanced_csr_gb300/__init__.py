@@ -83,49 +83,66 @@ def lib() -> ctypes.CDLL:
     """Load libspmv.so (building it first if its sources are newer)."""
     global _lib
     if _lib is None:
-        path = _build.build()
-        if not os.path.exists(path):
-            raise RuntimeError("libspmv.so is missing and could not be built")
-        L = ctypes.CDLL(path)
-        vp, i32, sz, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_double
-        sigs = {
-            "spmv_plan_create": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int, vp],
-            "spmv_plan_create_ex": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int,
-                                    ctypes.POINTER(Options), vp],
-            "spmv_execute": [vp, dbl, vp, dbl, vp, vp],
-            "spmv_execute_host": [vp, dbl, vp, dbl, vp, vp, vp, vp],
-            "spmv_plan_update_values": [vp, vp, vp],
-            "spmv_plan_destroy": [vp],
-            "spmv_plan_info": [vp, ctypes.POINTER(PlanInfo)],
-            "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
-            "spmv_plan_device_status": [vp, ctypes.POINTER(i32)],
-            "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
-            "spmv_noalloc_device_status": [ctypes.POINTER(i32)],
-            "spmv_execute_multi": [vp, i32, dbl, vp, ctypes.c_int64, dbl, vp, ctypes.c_int64, vp],
-            "spmv_execute_transposed": [vp, dbl, vp, dbl, vp, vp],
-            "spmv_spgemm_create": [ctypes.POINTER(vp), i32, i32, i32, i32, vp, vp, i32, vp, vp, ctypes.c_int,
-                                   ctypes.POINTER(ctypes.c_int64), vp],
-            "spmv_spgemm_compute": [vp, vp, vp, vp, vp, vp, vp],
-            "spmv_spgemm_info": [vp, ctypes.POINTER(SpgemmInfo)],
-            "spmv_spgemm_device_status": [vp, ctypes.POINTER(i32)],
-            "spmv_spgemm_destroy": [vp],
-            "spmv_gather_ceiling": [i32, i32, vp, i32, vp, vp, ctypes.c_int, vp, vp, vp],
-        }
-        for name, args in sigs.items():
-            fn = getattr(L, name)
-            fn.argtypes = args
-            fn.restype = ctypes.c_int
-        L.spmv_status_string.argtypes = [ctypes.c_int]
-        L.spmv_status_string.restype = ctypes.c_char_p
-        L.spmv_last_error.argtypes = []
-        L.spmv_last_error.restype = ctypes.c_char_p
-        _lib = L
+        _lib = _load(_build.build())
     return _lib
 
 
-def check(status: int, what: str) -> None:
+_debug_lib = None
+
+
+def debug_lib() -> ctypes.CDLL:
+    """Load libspmv_debug.so, the build with device-side checks of the column
+    indices gathered with (-DSPMV_DEBUG), building it first if needed.  Same
+    functions as lib(); an index outside [0, n) sets bit 2 of the plan's
+    device status instead of reading outside x."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _load(_build.build(debug=True))
+    return _debug_lib
+
+
+def _load(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{os.path.basename(path)} is missing and could not be built")
+    L = ctypes.CDLL(path)
+    vp, i32, sz, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_double
+    sigs = {
+        "spmv_plan_create": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int, vp],
+        "spmv_plan_create_ex": [ctypes.POINTER(vp), i32, i32, i32, vp, vp, vp, ctypes.c_int,
+                                ctypes.POINTER(Options), vp],
+        "spmv_execute": [vp, dbl, vp, dbl, vp, vp],
+        "spmv_execute_host": [vp, dbl, vp, dbl, vp, vp, vp, vp],
+        "spmv_plan_update_values": [vp, vp, vp],
+        "spmv_plan_destroy": [vp],
+        "spmv_plan_info": [vp, ctypes.POINTER(PlanInfo)],
+        "spmv_plan_export": [vp, ctypes.c_int, vp, sz, ctypes.POINTER(sz)],
+        "spmv_plan_device_status": [vp, ctypes.POINTER(i32)],
+        "spmv_execute_noalloc": [i32, i32, i32, vp, vp, vp, ctypes.c_int, dbl, vp, dbl, vp, vp],
+        "spmv_noalloc_device_status": [ctypes.POINTER(i32)],
+        "spmv_execute_multi": [vp, i32, dbl, vp, ctypes.c_int64, dbl, vp, ctypes.c_int64, vp],
+        "spmv_execute_transposed": [vp, dbl, vp, dbl, vp, vp],
+        "spmv_spgemm_create": [ctypes.POINTER(vp), i32, i32, i32, i32, vp, vp, i32, vp, vp, ctypes.c_int,
+                               ctypes.POINTER(ctypes.c_int64), vp],
+        "spmv_spgemm_compute": [vp, vp, vp, vp, vp, vp, vp],
+        "spmv_spgemm_info": [vp, ctypes.POINTER(SpgemmInfo)],
+        "spmv_spgemm_device_status": [vp, ctypes.POINTER(i32)],
+        "spmv_spgemm_destroy": [vp],
+        "spmv_gather_ceiling": [i32, i32, vp, i32, vp, vp, ctypes.c_int, vp, vp, vp],
+    }
+    for name, args in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    L.spmv_status_string.argtypes = [ctypes.c_int]
+    L.spmv_status_string.restype = ctypes.c_char_p
+    L.spmv_last_error.argtypes = []
+    L.spmv_last_error.restype = ctypes.c_char_p
+    return L
+
+
+def check(status: int, what: str, L: ctypes.CDLL | None = None) -> None:
     if status != 0:
-        raise SpmvError(status, what, lib().spmv_last_error().decode())
+        raise SpmvError(status, what, (L or lib()).spmv_last_error().decode())
 
 
 def _stream_handle(stream) -> int:
@@ -157,7 +174,7 @@ class Plan:
 
     def __init__(self, row_ptr, col_idx, vals, n: int, *, kernel: str = "auto", items_per_thread: int = 0,
                  rgcsr_group: int = 0, long_row_min: int = 0, with_spmm: bool = False, with_transpose: bool = False,
-                 stream=None):
+                 stream=None, debug: bool = False):
         import torch
         for name, t, dt in (("row_ptr", row_ptr, torch.int32), ("col_idx", col_idx, torch.int32)):
             if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
@@ -169,15 +186,18 @@ class Plan:
         if vals.numel() != nnz:
             raise ValueError("vals and col_idx differ in length")
         self._keep = (row_ptr, col_idx, vals)
+        # debug: run on the build with device-side checks of the column
+        # indices (an index outside [0, n) sets bit 2 of device_status())
+        self._L = debug_lib() if debug else lib()
         self.m, self.n, self.nnz = m, int(n), nnz
         self.dtype = vals.dtype
         opts = Options(KERNELS[kernel], items_per_thread, rgcsr_group, long_row_min, int(bool(with_spmm)),
                        int(bool(with_transpose)))
         handle = ctypes.c_void_p()
         with torch.cuda.device(row_ptr.device):
-            check(lib().spmv_plan_create_ex(ctypes.byref(handle), m, self.n, nnz, _ptr(row_ptr), _ptr(col_idx),
+            check(self._L.spmv_plan_create_ex(ctypes.byref(handle), m, self.n, nnz, _ptr(row_ptr), _ptr(col_idx),
                                             _ptr(vals), _dtype_code(vals), ctypes.byref(opts),
-                                            _stream_handle(stream)), "spmv_plan_create")
+                                            _stream_handle(stream)), "spmv_plan_create", self._L)
         self._h = handle
         self.device = row_ptr.device
 
@@ -193,8 +213,8 @@ class Plan:
             raise ValueError("x must have n and y m contiguous entries")
         if not x.is_cuda or not y.is_cuda:
             raise TypeError("x and y must be CUDA tensors")
-        check(lib().spmv_execute(self._h, float(alpha), _ptr(x), float(beta), _ptr(y), _stream_handle(stream)),
-              "spmv_execute")
+        check(self._L.spmv_execute(self._h, float(alpha), _ptr(x), float(beta), _ptr(y), _stream_handle(stream)),
+              "spmv_execute", self._L)
         return y
 
     def execute_host(self, x_host, y_host, x_dev, y_dev, alpha: float = 1.0, beta: float = 0.0, stream=None):
@@ -211,8 +231,8 @@ class Plan:
             raise ValueError("x buffers must have n and y buffers m entries")
         if x_host.is_cuda or y_host.is_cuda or not x_dev.is_cuda or not y_dev.is_cuda:
             raise TypeError("x_host and y_host must be CPU tensors, x_dev and y_dev CUDA tensors")
-        check(lib().spmv_execute_host(self._h, float(alpha), _ptr(x_host), float(beta), _ptr(y_host), _ptr(x_dev),
-                                      _ptr(y_dev), _stream_handle(stream)), "spmv_execute_host")
+        check(self._L.spmv_execute_host(self._h, float(alpha), _ptr(x_host), float(beta), _ptr(y_host), _ptr(x_dev),
+                                      _ptr(y_dev), _stream_handle(stream)), "spmv_execute_host", self._L)
         return y_host
 
     def execute_multi(self, X, Y, alpha: float = 1.0, beta: float = 0.0, stream=None):
@@ -232,8 +252,8 @@ class Plan:
         k = X.shape[1]
         ldx = X.stride(0) if X.shape[0] > 1 else k
         ldy = Y.stride(0) if Y.shape[0] > 1 else k
-        check(lib().spmv_execute_multi(self._h, k, float(alpha), _ptr(X), ldx, float(beta), _ptr(Y), ldy,
-                                       _stream_handle(stream)), "spmv_execute_multi")
+        check(self._L.spmv_execute_multi(self._h, k, float(alpha), _ptr(X), ldx, float(beta), _ptr(Y), ldy,
+                                       _stream_handle(stream)), "spmv_execute_multi", self._L)
         return Y
 
     def execute_transposed(self, x, y, alpha: float = 1.0, beta: float = 0.0, stream=None):
@@ -246,19 +266,20 @@ class Plan:
             raise ValueError("x must have m and y n contiguous entries")
         if not x.is_cuda or not y.is_cuda:
             raise TypeError("x and y must be CUDA tensors")
-        check(lib().spmv_execute_transposed(self._h, float(alpha), _ptr(x), float(beta), _ptr(y),
-                                            _stream_handle(stream)), "spmv_execute_transposed")
+        check(self._L.spmv_execute_transposed(self._h, float(alpha), _ptr(x), float(beta), _ptr(y),
+                                            _stream_handle(stream)), "spmv_execute_transposed", self._L)
         return y
 
     def update_values(self, vals, stream=None):
         if vals.numel() != self.nnz or vals.dtype != self.dtype or not vals.is_contiguous():
             raise ValueError("vals must match the plan's nnz and value type")
-        check(lib().spmv_plan_update_values(self._h, _ptr(vals), _stream_handle(stream)), "spmv_plan_update_values")
+        check(self._L.spmv_plan_update_values(self._h, _ptr(vals), _stream_handle(stream)), "spmv_plan_update_values",
+              self._L)
         self._keep = (self._keep[0], self._keep[1], vals)
 
     def info(self) -> dict:
         inf = PlanInfo()
-        check(lib().spmv_plan_info(self._h, ctypes.byref(inf)), "spmv_plan_info")
+        check(self._L.spmv_plan_info(self._h, ctypes.byref(inf)), "spmv_plan_info", self._L)
         out = {f: getattr(inf, f) for f, _ in PlanInfo._fields_ if f != "stats"}
         s = inf.stats
         out["stats"] = {"hist": list(s.hist), "sum_len": s.sum_len, "rg_slots": list(s.rg_slots),
@@ -270,27 +291,27 @@ class Plan:
     def device_status(self) -> int:
         """Kernel-side failure flags (0 = none); waits for the device."""
         flags = ctypes.c_int32(0)
-        check(lib().spmv_plan_device_status(self._h, ctypes.byref(flags)), "spmv_plan_device_status")
+        check(self._L.spmv_plan_device_status(self._h, ctypes.byref(flags)), "spmv_plan_device_status", self._L)
         return flags.value
 
     def export(self, what: str):
         import numpy as np
         code = EXPORTS[what]
         need = ctypes.c_size_t(0)
-        check(lib().spmv_plan_export(self._h, code, None, 0, ctypes.byref(need)), "spmv_plan_export")
+        check(self._L.spmv_plan_export(self._h, code, None, 0, ctypes.byref(need)), "spmv_plan_export", self._L)
         dtype = {"partition": np.int32, "rg_group_ptr": np.int64, "rg_row_len": np.int32, "rg_col": np.int32,
                  "long_rows": np.int32, "long_seg_begin": np.int64, "rg_perm": np.int32, "t_ptr": np.int32,
                  "t_idx": np.int32, "t_src": np.int32,
                  "t_vals": np.float64 if str(self.dtype) == "torch.float64" else np.float32,
                  "rg_val": np.float64 if str(self.dtype) == "torch.float64" else np.float32}[what]
         buf = np.empty(need.value // np.dtype(dtype).itemsize, dtype=dtype)
-        check(lib().spmv_plan_export(self._h, code, buf.ctypes.data if buf.size else None, need.value, None),
-              "spmv_plan_export")
+        check(self._L.spmv_plan_export(self._h, code, buf.ctypes.data if buf.size else None, need.value, None),
+              "spmv_plan_export", self._L)
         return buf.reshape(-1, 2) if what == "partition" else buf
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:
-            check(lib().spmv_plan_destroy(self._h), "spmv_plan_destroy")
+            check(self._L.spmv_plan_destroy(self._h), "spmv_plan_destroy", self._L)
         self._h = None
 
     def __del__(self):

@@ -491,6 +491,8 @@ spmv_status_t build_transpose(spmv_plan_s *p, cudaStream_t stream) {
 cudaError_t launch_long_part(const spmv_plan_s *p, const void *x, void *y, double alpha, double beta,
                              cudaStream_t stream) {
     LongRowsArgs a;
+    a.n = p->n;
+    a.error = p->device_error;
     a.row_ptr = p->row_ptr;
     a.col_idx = p->col_idx;
     a.vals = p->vals;
@@ -726,29 +728,32 @@ spmv_status_t spmv_execute(spmv_plan_t p, double alpha, const void *x, double be
     cudaError_t e = cudaSuccess;
     switch (p->kernel) {
     case SPMV_KERNEL_THREAD_ROW:
-        e = LAUNCH(launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, 0, stream));
+        e = LAUNCH(launch_thread_per_row(p->dtype, p->m, p->n, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, 0,
+                                         p->device_error, stream));
         break;
     case SPMV_KERNEL_GROUP_MAPPED:
-        e = LAUNCH(launch_group_mapped(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta, stream));
+        e = LAUNCH(launch_group_mapped(p->dtype, p->m, p->n, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta,
+                                       p->device_error, stream));
         break;
     case SPMV_KERNEL_LONG_ROWS:
         // long rows first (they take longest), then the others
         if (p->num_long_rows > 0) e = LAUNCH(launch_long_part(p, x, y, alpha, beta, stream));
         if (e == cudaSuccess)
-            e = LAUNCH(launch_thread_per_row(p->dtype, p->m, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta,
-                                      p->num_long_rows > 0 ? p->long_min : 0, stream));
+            e = LAUNCH(launch_thread_per_row(p->dtype, p->m, p->n, p->row_ptr, p->col_idx, p->vals, x, y, alpha, beta,
+                                             p->num_long_rows > 0 ? p->long_min : 0, p->device_error, stream));
         break;
     case SPMV_KERNEL_RGCSR:
     case SPMV_KERNEL_RGCSR_SORTED:
         if (p->num_long_rows > 0) e = LAUNCH(launch_long_part(p, x, y, alpha, beta, stream));
         if (e == cudaSuccess)
-            e = LAUNCH(launch_rgcsr_spmv(p->dtype, p->m, p->g_log2, p->group_ptr, p->row_len, p->perm, p->rg_col, p->rg_val,
+            e = LAUNCH(launch_rgcsr_spmv(p->dtype, p->m, p->n, p->g_log2, p->group_ptr, p->row_len, p->perm, p->rg_col, p->rg_val,
                                   x, y, alpha, beta, p->device_error, stream));
         break;
     case SPMV_KERNEL_MERGE_PATH:
     default: {
         MergePathArgs a;
         a.m = p->m;
+        a.n = p->n;
         a.nnz = p->nnz;
         a.row_ptr = p->row_ptr;
         a.col_idx = p->col_idx;

@@ -27,7 +27,8 @@ constexpr int kGmItems = kGmChunk / kGmThreads;
 template <typename V>
 __global__ void __launch_bounds__(kGmThreads)
 group_mapped_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
-                    const V *__restrict__ val, const V *__restrict__ x, V *__restrict__ y, V alpha, V beta) {
+                    const V *__restrict__ val, const V *__restrict__ x, V *__restrict__ y, V alpha, V beta,
+                    int32_t n, int32_t *error) {
     __shared__ int pre[kGmThreads + 1];
     __shared__ int s_warp[kGmThreads / 32];
     __shared__ V prod[kGmChunk];
@@ -81,7 +82,7 @@ group_mapped_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__
 #pragma unroll
         for (int i = 0; i < kGmItems; ++i) {
             const int a = t + i * kGmThreads;
-            if (a < cn) prod[a] = vv[i] * ld_gather(x + cc[i]);
+            if (a < cn) prod[a] = vv[i] * ld_gather(x + debug_col(cc[i], n, error));
         }
         __syncthreads();
         // my row's atoms in this chunk, in order
@@ -104,19 +105,19 @@ group_mapped_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__
 
 }  // namespace
 
-cudaError_t launch_group_mapped(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
-                                const void *vals, const void *x, void *y, double alpha, double beta,
-                                cudaStream_t stream) {
+cudaError_t launch_group_mapped(spmv_dtype_t dtype, int32_t m, int32_t n, const int32_t *row_ptr,
+                                const int32_t *col_idx, const void *vals, const void *x, void *y, double alpha,
+                                double beta, int32_t *error, cudaStream_t stream) {
     if (m <= 0) return cudaSuccess;
     const unsigned groups = (unsigned)(((int64_t)m + kGmThreads - 1) / kGmThreads);
     if (dtype == SPMV_F64)
         group_mapped_kernel<double><<<groups, kGmThreads, 0, stream>>>(
             m, row_ptr, col_idx, static_cast<const double *>(vals), static_cast<const double *>(x),
-            static_cast<double *>(y), alpha, beta);
+            static_cast<double *>(y), alpha, beta, n, error);
     else
         group_mapped_kernel<float><<<groups, kGmThreads, 0, stream>>>(
             m, row_ptr, col_idx, static_cast<const float *>(vals), static_cast<const float *>(x),
-            static_cast<float *>(y), (float)alpha, (float)beta);
+            static_cast<float *>(y), (float)alpha, (float)beta, n, error);
     return cudaGetLastError();
 }
 

@@ -23,6 +23,23 @@ __device__ __forceinline__ T ld_gather(const T *p) {
     return __ldg(p);
 }
 
+// Debug build (-DSPMV_DEBUG): every column index an SpMV kernel gathers x
+// with is checked against [0, n).  One outside it sets kErrIndex in the
+// plan's error word and reads x[0] instead, so the gather stays inside x and
+// nothing traps.  Plan creation validates every index; this catches arrays
+// changed after it (the plan borrows them unmodified).  Without SPMV_DEBUG
+// the check compiles to nothing.
+constexpr int32_t kErrIndex = 4;
+#ifdef SPMV_DEBUG
+__device__ __forceinline__ int debug_col(int c, int n, int32_t *error) {
+    if ((unsigned)c < (unsigned)n) return c;
+    if (error) atomicOr(error, kErrIndex);
+    return 0;
+}
+#else
+__device__ __forceinline__ int debug_col(int c, int, int32_t *) { return c; }
+#endif
+
 // ---------------------------------------------------------------- statistics
 constexpr int kStatsThreads = 256;
 constexpr int kStatsRowsPerCta = 4096;  // multiple of 256: Row-grouped groups never straddle CTAs
@@ -52,6 +69,7 @@ cudaError_t launch_merge_path_partition(int32_t m, int32_t nnz, const int32_t *r
 
 struct MergePathArgs {
     int32_t m;
+    int32_t n = 0;  // columns (the debug build checks gathers against it)
     int32_t nnz;
     const int32_t *row_ptr;
     const int32_t *col_idx;
@@ -119,19 +137,20 @@ cudaError_t launch_rgcsr_pack(spmv_dtype_t dtype, int32_t m, const int32_t *row_
 
 // ---------------------------------------------------------------- row kernels
 // Group-mapped schedule: a CTA per 256 rows, atoms staged by chunks.
-cudaError_t launch_group_mapped(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr, const int32_t *col_idx,
-                                const void *vals, const void *x, void *y, double alpha, double beta,
-                                cudaStream_t stream);
+cudaError_t launch_group_mapped(spmv_dtype_t dtype, int32_t m, int32_t n, const int32_t *row_ptr,
+                                const int32_t *col_idx, const void *vals, const void *x, void *y, double alpha,
+                                double beta, int32_t *error, cudaStream_t stream);
 
 // Thread per row; rows of length >= skip_min_len (when > 0) are skipped.
-cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr,
+cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, int32_t n, const int32_t *row_ptr,
                                   const int32_t *col_idx, const void *vals, const void *x, void *y,
-                                  double alpha, double beta, int32_t skip_min_len, cudaStream_t stream);
+                                  double alpha, double beta, int32_t skip_min_len, int32_t *error,
+                                  cudaStream_t stream);
 
 // Row-grouped CSR, thread per row (rows with row_len < 0 are skipped).
 // rg_col and rg_val must be 128-byte aligned (the plan allocates them).
 // perm (G = 32 only): the row at each position, null for the natural order.
-cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const int64_t *group_ptr,
+cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int32_t n, int g_log2, const int64_t *group_ptr,
                               const int32_t *row_len, const int32_t *perm, const int32_t *rg_col,
                               const void *rg_val, const void *x, void *y, double alpha, double beta,
                               int32_t *error, cudaStream_t stream);
@@ -139,6 +158,8 @@ cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const i
 // Long rows: one warp per segment of kLongSegmentNnz nonzeros; rows with
 // several segments are finished by the last segment to arrive.
 struct LongRowsArgs {
+    int32_t n = 0;             // columns (the debug build checks gathers against it)
+    int32_t *error = nullptr;  // the plan's error word (debug build)
     const int32_t *row_ptr;
     const int32_t *col_idx;
     const void *vals;

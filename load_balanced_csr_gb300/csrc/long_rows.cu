@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(kLongThreads)
 long_rows_kernel(const int32_t *__restrict__ rp, const int32_t *__restrict__ col, const V *__restrict__ val,
                  const V *__restrict__ x, V *__restrict__ y, V alpha, V beta,
                  const int32_t *__restrict__ long_rows, const int64_t *__restrict__ seg_begin, int32_t num_long,
-                 int64_t num_segs, V *__restrict__ seg_partial, int32_t *__restrict__ arrivals) {
+                 int64_t num_segs, V *__restrict__ seg_partial, int32_t *__restrict__ arrivals, int32_t n,
+                 int32_t *error) {
     const int lane = threadIdx.x & 31;
     const int64_t s = (int64_t)blockIdx.x * kLongWarps + (threadIdx.x >> 5);
     if (s >= num_segs) return;
@@ -62,11 +63,13 @@ long_rows_kernel(const int32_t *__restrict__ rp, const int32_t *__restrict__ col
             v[u] = ld_stream(val + k + u * 32);
         }
 #pragma unroll
-        for (int u = 0; u < kLongU; ++u) acc[u] = fma(v[u], ld_gather(x + c[u]), acc[u]);
+        for (int u = 0; u < kLongU; ++u) acc[u] = fma(v[u], ld_gather(x + debug_col(c[u], n, error)), acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < kLongU - 1; ++u)
-        if (k + u * 32 < e) acc[u] = fma(ld_stream(val + k + u * 32), ld_gather(x + ld_stream(col + k + u * 32)), acc[u]);
+        if (k + u * 32 < e)
+            acc[u] = fma(ld_stream(val + k + u * 32), ld_gather(x + debug_col(ld_stream(col + k + u * 32), n, error)),
+                         acc[u]);
 #pragma unroll
     for (int w = 1; w < kLongU; w <<= 1)
 #pragma unroll
@@ -112,12 +115,12 @@ cudaError_t launch_long_rows_spmv(spmv_dtype_t dtype, const LongRowsArgs &a, cud
         long_rows_kernel<double><<<blocks, kLongThreads, 0, stream>>>(
             a.row_ptr, a.col_idx, static_cast<const double *>(a.vals), static_cast<const double *>(a.x),
             static_cast<double *>(a.y), a.alpha, a.beta, a.long_rows, a.seg_begin, a.num_long, a.num_segs,
-            static_cast<double *>(a.seg_partial), a.arrivals);
+            static_cast<double *>(a.seg_partial), a.arrivals, a.n, a.error);
     else
         long_rows_kernel<float><<<blocks, kLongThreads, 0, stream>>>(
             a.row_ptr, a.col_idx, static_cast<const float *>(a.vals), static_cast<const float *>(a.x),
             static_cast<float *>(a.y), (float)a.alpha, (float)a.beta, a.long_rows, a.seg_begin, a.num_long,
-            a.num_segs, static_cast<float *>(a.seg_partial), a.arrivals);
+            a.num_segs, static_cast<float *>(a.seg_partial), a.arrivals, a.n, a.error);
     return cudaGetLastError();
 }
 

@@ -88,6 +88,7 @@ __host__ __device__ constexpr int stages_for() {
 template <typename V>
 struct MPParams {
     int32_t m;
+    int32_t n;  // columns (the debug build checks the gathers against it)
     int32_t nnz;
     const int32_t *row_ptr;
     const int32_t *col_idx;
@@ -436,7 +437,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
             for (int i = 0; i <= IPL; ++i) {
                 if (sizeof(V) == 8 && i >= steps) break;
                 const bool in = i * 32 + lane < nnzt;
-                xr[i] = in ? gather_keep(p.x + c[i * 32], x_pol) : V(0);
+                xr[i] = in ? gather_keep(p.x + debug_col(c[i * 32], p.n, p.error), x_pol) : V(0);
                 vr[i] = in ? w[i * 32] : V(0);
             }
         } else {
@@ -445,7 +446,7 @@ merge_path_spmv_kernel(const MPParams<V> p) {
 #pragma unroll
             for (int i = 0; i <= IPL; ++i) {
                 if (sizeof(V) == 8 && i >= Q) break;
-                xr[i] = i < run ? gather_keep(p.x + c[i], x_pol) : V(0);
+                xr[i] = i < run ? gather_keep(p.x + debug_col(c[i], p.n, p.error), x_pol) : V(0);
                 vr[i] = i < run ? w[i] : V(0);
             }
         }
@@ -653,6 +654,7 @@ cudaError_t launch_typed(const MergePathArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     MPParams<V> p;
     p.m = a.m;
+    p.n = a.n;
     p.nnz = a.nnz;
     p.row_ptr = a.row_ptr;
     p.col_idx = a.col_idx;

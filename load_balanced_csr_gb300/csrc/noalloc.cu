@@ -85,6 +85,7 @@ extern "C" spmv_status_t spmv_execute_noalloc(int32_t m, int32_t n, int32_t nnz,
         return SPMV_ERR_CUDA;
     MergePathArgs a;
     a.m = m;
+    a.n = n;
     a.nnz = nnz;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;

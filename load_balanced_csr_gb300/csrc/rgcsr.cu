@@ -39,6 +39,7 @@ constexpr int kRgStageTarget = 16384;  // bytes of slots per stage (at most)
 template <typename V>
 struct RgParams {
     int32_t m;
+    int32_t n;  // columns (the debug build checks the gathers against it)
     int g_log2;
     long long ngroups;
     const int64_t *gp;
@@ -166,13 +167,13 @@ rgcsr_tma_kernel(const RgParams<V> p) {
             for (; k + U <= mine; k += U) {
                 V xv[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) xv[u] = gather_keep(p.x + scol[(k + u) * G + t], x_pol);
+                for (int u = 0; u < U; ++u) xv[u] = gather_keep(p.x + debug_col(scol[(k + u) * G + t], p.n, p.error), x_pol);
 #pragma unroll
                 for (int u = 0; u < U; ++u) acc[u] = fma(sval[(k + u) * G + t], xv[u], acc[u]);
             }
 #pragma unroll
             for (int u = 0; u < U - 1; ++u)
-                if (k + u < mine) acc[u] = fma(sval[(k + u) * G + t], gather_keep(p.x + scol[(k + u) * G + t], x_pol), acc[u]);
+                if (k + u < mine) acc[u] = fma(sval[(k + u) * G + t], gather_keep(p.x + debug_col(scol[(k + u) * G + t], p.n, p.error), x_pol), acc[u]);
             __syncthreads();  // the stage is free
             if (t == 0 && ig < p.ngroups) {
                 rg_issue(p, stages + s * sbytes, bars + s, ig, ic, stream_pol);
@@ -337,14 +338,14 @@ rgcsr_warp_kernel(const RgParams<V> p) {
             for (; k + U <= mine; k += U) {
                 V xv[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) xv[u] = gather_keep(p.x + scol[(k + u) * 32 + lane], x_pol);
+                for (int u = 0; u < U; ++u) xv[u] = gather_keep(p.x + debug_col(scol[(k + u) * 32 + lane], p.n, p.error), x_pol);
 #pragma unroll
                 for (int u = 0; u < U; ++u) acc[u] = fma(sval[(k + u) * 32 + lane], xv[u], acc[u]);
             }
 #pragma unroll
             for (int u = 0; u < U - 1; ++u)
                 if (k + u < mine)
-                    acc[u] = fma(sval[(k + u) * 32 + lane], gather_keep(p.x + scol[(k + u) * 32 + lane], x_pol), acc[u]);
+                    acc[u] = fma(sval[(k + u) * 32 + lane], gather_keep(p.x + debug_col(scol[(k + u) * 32 + lane], p.n, p.error), x_pol), acc[u]);
             __syncwarp();  // the stage is free
             if (lane == 0 && ig < g_end) {
                 rg_issue_slots(p, stages + s * sbytes, bars + s, ib, ie, ic, stream_pol);
@@ -407,13 +408,14 @@ size_t rg_smem(int G) {
 }
 
 template <typename V>
-cudaError_t launch_rg(int32_t m, int g_log2, const int64_t *group_ptr, const int32_t *row_len, const int32_t *perm,
+cudaError_t launch_rg(int32_t m, int32_t n, int g_log2, const int64_t *group_ptr, const int32_t *row_len, const int32_t *perm,
                       const int32_t *rg_col, const void *rg_val, const void *x, void *y, double alpha, double beta,
                       int32_t *error, cudaStream_t stream) {
     const int G = 1 << g_log2;
     if (perm && G != 32) return cudaErrorInvalidValue;
     RgParams<V> p;
     p.m = m;
+    p.n = n;
     p.g_log2 = g_log2;
     p.ngroups = ((long long)m + G - 1) >> g_log2;
     p.gp = group_ptr;
@@ -456,15 +458,15 @@ cudaError_t launch_rg(int32_t m, int g_log2, const int64_t *group_ptr, const int
 
 }  // namespace
 
-cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int g_log2, const int64_t *group_ptr,
+cudaError_t launch_rgcsr_spmv(spmv_dtype_t dtype, int32_t m, int32_t n, int g_log2, const int64_t *group_ptr,
                               const int32_t *row_len, const int32_t *perm, const int32_t *rg_col,
                               const void *rg_val, const void *x, void *y, double alpha, double beta,
                               int32_t *error, cudaStream_t stream) {
     if (m <= 0) return cudaSuccess;
     if (dtype == SPMV_F64)
-        return launch_rg<double>(m, g_log2, group_ptr, row_len, perm, rg_col, rg_val, x, y, alpha, beta, error,
+        return launch_rg<double>(m, n, g_log2, group_ptr, row_len, perm, rg_col, rg_val, x, y, alpha, beta, error,
                                  stream);
-    return launch_rg<float>(m, g_log2, group_ptr, row_len, perm, rg_col, rg_val, x, y, alpha, beta, error, stream);
+    return launch_rg<float>(m, n, g_log2, group_ptr, row_len, perm, rg_col, rg_val, x, y, alpha, beta, error, stream);
 }
 
 }  // namespace lbcsr

@@ -41,7 +41,7 @@ template <typename V>
 __global__ void __launch_bounds__(256)
 thread_per_row_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
                       const V *__restrict__ val, const V *__restrict__ x, V *__restrict__ y, V alpha,
-                      V beta, int32_t skip_min_len) {
+                      V beta, int32_t skip_min_len, int32_t n, int32_t *error) {
     constexpr int U = 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < m; row += stride) {
@@ -60,11 +60,12 @@ thread_per_row_kernel(int32_t m, const int32_t *__restrict__ rp, const int32_t *
                 v[u] = ld_stream(val + k + u);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc[u] = fma(v[u], ld_gather(x + c[u]), acc[u]);
+            for (int u = 0; u < U; ++u) acc[u] = fma(v[u], ld_gather(x + debug_col(c[u], n, error)), acc[u]);
         }
 #pragma unroll
         for (int u = 0; u < U - 1; ++u)
-            if (k + u < e) acc[u] = fma(ld_stream(val + k + u), ld_gather(x + ld_stream(col + k + u)), acc[u]);
+            if (k + u < e)
+                acc[u] = fma(ld_stream(val + k + u), ld_gather(x + debug_col(ld_stream(col + k + u), n, error)), acc[u]);
         y[row] = finish(tree_sum(acc), alpha, beta, y, row);
     }
 }
@@ -98,9 +99,10 @@ int carveout_percent(int ctas, size_t smem_per_cta) {
     return (int)(pct < 0 ? 0 : pct > 100 ? 100 : pct);
 }
 
-cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *row_ptr,
+cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, int32_t n, const int32_t *row_ptr,
                                   const int32_t *col_idx, const void *vals, const void *x, void *y,
-                                  double alpha, double beta, int32_t skip_min_len, cudaStream_t stream) {
+                                  double alpha, double beta, int32_t skip_min_len, int32_t *error,
+                                  cudaStream_t stream) {
     if (m <= 0) return cudaSuccess;
     const int64_t want = ((int64_t)m + 255) / 256;
     const int64_t cap = (int64_t)device_sm_count() * 8;
@@ -108,11 +110,11 @@ cudaError_t launch_thread_per_row(spmv_dtype_t dtype, int32_t m, const int32_t *
     if (dtype == SPMV_F64)
         thread_per_row_kernel<double><<<blocks, 256, 0, stream>>>(
             m, row_ptr, col_idx, static_cast<const double *>(vals), static_cast<const double *>(x),
-            static_cast<double *>(y), alpha, beta, skip_min_len);
+            static_cast<double *>(y), alpha, beta, skip_min_len, n, error);
     else
         thread_per_row_kernel<float><<<blocks, 256, 0, stream>>>(
             m, row_ptr, col_idx, static_cast<const float *>(vals), static_cast<const float *>(x),
-            static_cast<float *>(y), (float)alpha, (float)beta, skip_min_len);
+            static_cast<float *>(y), (float)alpha, (float)beta, skip_min_len, n, error);
     return cudaGetLastError();
 }
 
