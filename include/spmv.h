@@ -176,6 +176,12 @@ typedef enum {
  * finds a malformed row_ptr or a column index outside [0, n); ALLOC; CUDA;
  * UNSUPPORTED when the current device is not compute capability 10.3.
  * On error *out is set to NULL and nothing is leaked.
+ * Environment, read at each creation: SPMV_LOG=1 prints one line per plan
+ * on stderr (the row statistics, the kernel and the rule that chose it);
+ * SPMV_FORCE_KERNEL (a kernel name) and SPMV_ITEMS_PER_THREAD override the
+ * choice when the options leave it open; SPMV_FAULT=alloc:N|launch:N makes
+ * the N-th device allocation or launch step of the call fail, for testing
+ * the clean-up paths.
  */
 spmv_status_t spmv_plan_create(spmv_plan_t *out, int32_t m, int32_t n, int32_t nnz,
                                const int32_t *row_ptr, const int32_t *col_idx, const void *vals,

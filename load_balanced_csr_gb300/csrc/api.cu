@@ -221,13 +221,55 @@ spmv_kernel_t env_kernel() {
 //    90.0 us; 5-point Laplacian 64x64: 8.2 us against 12.6 us) and 2-8x
 //    slower on irregular ones;
 //  * everything else: merge path.
-spmv_kernel_t choose_kernel(const spmv_plan_s &p) {
+// `why`, when given, receives the rule that decided.
+spmv_kernel_t choose_kernel(const spmv_plan_s &p, const char **why = nullptr) {
     const spmv_row_stats_t &s = p.stats;
-    if (p.n == 1 && s.max_len <= 32) return SPMV_KERNEL_THREAD_ROW;
-    if ((p.m < 500 || p.n < 500) && p.nnz < 10000 && s.max_len <= 256) return SPMV_KERNEL_THREAD_ROW;
-    if (p.m <= 65536 && s.max_len <= 64) return SPMV_KERNEL_THREAD_ROW;
-    if (p.nnz > 0 && (double)s.rg_slots[0] <= 1.1 * (double)p.nnz) return SPMV_KERNEL_RGCSR;
+    const char *unused = nullptr;
+    const char *&rule = why ? *why : unused;
+    if (p.n == 1 && s.max_len <= 32) {
+        rule = "one column, rows of at most 32";
+        return SPMV_KERNEL_THREAD_ROW;
+    }
+    if ((p.m < 500 || p.n < 500) && p.nnz < 10000 && s.max_len <= 256) {
+        rule = "small matrix (rows or columns < 500, nnz < 10000)";
+        return SPMV_KERNEL_THREAD_ROW;
+    }
+    if (p.m <= 65536 && s.max_len <= 64) {
+        rule = "at most 65536 rows of at most 64";
+        return SPMV_KERNEL_THREAD_ROW;
+    }
+    if (p.nnz > 0 && (double)s.rg_slots[0] <= 1.1 * (double)p.nnz) {
+        rule = "Row-grouped copy pads at most 10 %";
+        return SPMV_KERNEL_RGCSR;
+    }
+    rule = "default";
     return SPMV_KERNEL_MERGE_PATH;
+}
+
+const char *kernel_name(spmv_kernel_t k) {
+    switch (k) {
+    case SPMV_KERNEL_MERGE_PATH: return "merge_path";
+    case SPMV_KERNEL_THREAD_ROW: return "thread_row";
+    case SPMV_KERNEL_RGCSR: return "rgcsr";
+    case SPMV_KERNEL_LONG_ROWS: return "long_rows";
+    case SPMV_KERNEL_RGCSR_SORTED: return "rgcsr_sorted";
+    case SPMV_KERNEL_GROUP_MAPPED: return "group_mapped";
+    default: return "?";
+    }
+}
+
+// SPMV_LOG=1: one line per plan on stderr with its statistics and the
+// kernel choice (read at each creation; unset, it costs one getenv).
+void log_plan(const spmv_plan_s &p, const char *why) {
+    if (env_int("SPMV_LOG", 0) == 0) return;
+    const spmv_row_stats_t &s = p.stats;
+    const double fill = p.nnz > 0 ? (double)s.rg_slots[0] / (double)p.nnz - 1.0 : 0.0;
+    std::fprintf(stderr,
+                 "spmv plan: m=%d n=%d nnz=%d %s rows[min=%d max=%d mean=%.2f empty=%d] bandwidth=%d "
+                 "rgcsr32_fill=%.3f -> kernel=%s (%s) items_per_thread=%d tiles=%lld long_rows=%d\n",
+                 p.m, p.n, p.nnz, p.dtype == SPMV_F64 ? "f64" : "f32", s.min_len, s.max_len,
+                 p.m > 0 ? (double)s.sum_len / p.m : 0.0, s.n_empty, s.bandwidth, fill, kernel_name(p.kernel), why,
+                 p.ipt, (long long)p.num_tiles, p.num_long_rows);
 }
 
 // Row-grouped CSR group size: 32.  The Row-grouped CSR page needs G >= 32
@@ -642,7 +684,8 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
     }
 
     // ---- kernel choice and schedule
-    p->kernel = forced != SPMV_KERNEL_AUTO ? forced : choose_kernel(*p);
+    const char *why = "forced";
+    p->kernel = forced != SPMV_KERNEL_AUTO ? forced : choose_kernel(*p, &why);
     p->ipt = ipt_forced ? ipt_forced : merge_path_choose_items(dtype, n, p->stats);
     p->tile = (int64_t)merge_path_threads() * p->ipt;
     p->num_tiles = total > 0 ? (total + p->tile - 1) / p->tile : 1;
@@ -714,6 +757,7 @@ spmv_status_t spmv_plan_create_ex(spmv_plan_t *out, int32_t m, int32_t n, int32_
             return cuda_fail(e, "SpMM long-row partials");
         }
     }
+    log_plan(*p, why);
     *out = p;
     return SPMV_OK;
 }

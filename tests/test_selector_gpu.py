@@ -99,3 +99,31 @@ def test_rule4_row_grouped_padding():
         k, s = _kernel(_csr(lens, 200000, 4))
         assert s["rg_slots"][0] == 32 * L * groups
         assert k == want, (L, k)
+
+
+def test_plan_log_names_the_rule():
+    """SPMV_LOG=1 prints one line per plan on stderr: the statistics and
+    the kernel with the rule that chose it (checked in a child process, so
+    that the variable is read at plan creation there)."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, 'tests'); import numpy as np, torch, synth\n"
+        "import load_balanced_csr_gb300 as lb\n"
+        "from helpers import to_gpu\n"
+        "A = synth.fill_random(np.full(300, 3, np.int32), 200, seed=1, dtype='f32')\n"
+        "rp, col, val = to_gpu(A)\n"
+        "lb.Plan(rp, col, val, A.n).close()\n"
+        "B = synth.fill_random(synth.lengths_uniform(200000, 0, 80, 2), 200000, seed=2, dtype='f64')\n"
+        "rp, col, val = to_gpu(B)\n"
+        "lb.Plan(rp, col, val, B.n).close()\n"
+    )
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SPMV_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("spmv plan:")]
+    assert len(lines) == 2, r.stderr[-2000:]
+    assert "m=300 n=200 nnz=900 f32" in lines[0] and "kernel=thread_row (small matrix" in lines[0]
+    assert "kernel=merge_path (default)" in lines[1] and "f64" in lines[1]
