@@ -475,9 +475,8 @@ def per_config_entry(name: str, dev, warmup: int, min_runs: int, min_seconds: fl
 
 
 def run_per_config(args) -> dict:
-    """Every workload on one GPU (spec: each config's median time per
-    product, GFLOP/s, GB/s and roofline fractions, with the oracle beside
-    it)."""
+    """Every workload on one GPU: each one's median time per product,
+    GFLOP/s, GB/s and roofline fractions, with the oracle beside it."""
     import torch
     _, _, local = dist_env()
     dev = torch.device("cuda", local)
