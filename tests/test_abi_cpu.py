@@ -13,6 +13,14 @@ def test_library_exports_every_header_function():
         assert hasattr(L, name), name
 
 
+def test_debug_library_exports_every_header_function():
+    """The debug build (device-side index checks) has the same interface."""
+    L = lb.debug_lib()
+    for name in lb.header_functions():
+        assert hasattr(L, name), name
+    assert L.spmv_status_string(0).decode() == lb.STATUS[0]
+
+
 def test_status_strings():
     L = lb.lib()
     for code, text in lb.STATUS.items():
