@@ -397,7 +397,9 @@ typedef enum {
     SPMV_GATHER_STREAM_LDG_STS = 12,
     SPMV_GATHER_STREAM_LDG_FEW = 13,
     SPMV_GATHER_STREAM_LDG_RES_1 = 14, /* .. _RES_6 = 19 */
-    SPMV_GATHER_STREAM_LDG_RES_6 = 19
+    SPMV_GATHER_STREAM_LDG_RES_6 = 19,
+    SPMV_GATHER_TEX = 20               /* element fetches from a linear texture object over x (the call
+                                          synchronises the stream: the object must outlive the launch) */
 } spmv_gather_path_t;
 
 spmv_status_t spmv_gather_ceiling(int32_t path, int32_t nnz, const int32_t *col_idx, int32_t n, const void *x,

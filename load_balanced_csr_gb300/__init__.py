@@ -421,7 +421,8 @@ def spgemm(a_row_ptr, a_col_idx, a_vals, b_row_ptr, b_col_idx, b_vals, n: int, s
 
 GATHER_PATHS = {"stream": 0, "l1": 1, "l2": 2, "bulk16": 3, "tma4": 4, "l1_tma4": 5, "l1_tma4_quarter": 6,
                 "tma4_16": 7, "stream_ldg": 8, "stream_bulk": 9, "stream_cpasync": 10, "stream_ldg_occ": 11,
-                "stream_ldg_sts": 12, "stream_ldg_few": 13, **{f"stream_ldg_res{32 * k}k": 13 + k for k in range(1, 7)}}
+                "stream_ldg_sts": 12, "stream_ldg_few": 13, **{f"stream_ldg_res{32 * k}k": 13 + k for k in range(1, 7)},
+                "tex": 20}
 GATHER_WITH_VALUES = tuple(k for k in GATHER_PATHS if k.startswith("stream_"))
 
 

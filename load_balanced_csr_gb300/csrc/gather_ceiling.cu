@@ -254,6 +254,79 @@ __global__ void __launch_bounds__(kGThreads) gather_ceiling_kernel(const GatherP
 }
 
 
+// Path 20: x read by element fetches from a linear texture object over x
+// (the Row-grouped CSR page reads x through the texture cache).  fp64 is
+// fetched as int2, its two 32-bit halves.
+__device__ __forceinline__ unsigned long long tex_bits(cudaTextureObject_t t, int c, float *) {
+    return __float_as_uint(tex1Dfetch<float>(t, c));
+}
+__device__ __forceinline__ unsigned long long tex_bits(cudaTextureObject_t t, int c, double *) {
+    const int2 v = tex1Dfetch<int2>(t, c);
+    return ((unsigned long long)(unsigned)v.y << 32) | (unsigned)v.x;
+}
+
+template <typename V>
+__global__ void __launch_bounds__(kGThreads) tex_gather_kernel(const GatherParams<V> p, cudaTextureObject_t tex) {
+    constexpr int U = 8, CH = 32 * U;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long chunks = (p.nnz + CH - 1) / CH;
+    const long long gw = (long long)blockIdx.x * kGWarps + warp;
+    const long long step = (long long)gridDim.x * kGWarps;
+    unsigned long long sum = 0;
+    for (long long c = gw; c < chunks; c += step) {
+        int cc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long k = c * CH + u * 32 + lane;
+            cc[u] = k < p.nnz ? ld_stream(p.col + k) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (cc[u] >= 0) sum += tex_bits(tex, cc[u], static_cast<V *>(nullptr));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0 && sum) atomicAdd(p.checksum, sum);
+}
+
+template <typename V>
+cudaError_t launch_tex_gather(const GatherParams<V> &p, cudaStream_t stream) {
+    int max_width = 0, dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_width, cudaDevAttrMaxTexture1DLinearWidth, dev);
+    if (e != cudaSuccess) return e;
+    if ((long long)p.n > max_width) return cudaErrorInvalidValue;
+    cudaResourceDesc res;
+    memset(&res, 0, sizeof(res));
+    res.resType = cudaResourceTypeLinear;
+    res.res.linear.devPtr = const_cast<V *>(p.x);
+    res.res.linear.desc = sizeof(V) == 8 ? cudaCreateChannelDesc<int2>() : cudaCreateChannelDesc<float>();
+    res.res.linear.sizeInBytes = (size_t)p.n * sizeof(V);
+    cudaTextureDesc td;
+    memset(&td, 0, sizeof(td));
+    td.readMode = cudaReadModeElementType;
+    td.filterMode = cudaFilterModePoint;
+    td.addressMode[0] = cudaAddressModeClamp;
+    cudaTextureObject_t tex = 0;
+    e = cudaCreateTextureObject(&tex, &res, &td, nullptr);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tex_gather_kernel<V>, kGThreads, 0);
+    if (e == cudaSuccess) {
+        const long long chunks = (p.nnz + 255) / 256;
+        long long grid = (long long)(per_sm > 0 ? per_sm : 1) * device_sm_count();
+        const long long need = (chunks + kGWarps - 1) / kGWarps;
+        if (grid > need) grid = need;
+        if (grid < 1) grid = 1;
+        tex_gather_kernel<V><<<(unsigned)grid, kGThreads, 0, stream>>>(p, tex);
+        e = cudaGetLastError();
+    }
+    // the object must outlive the launch that uses it
+    const cudaError_t es = cudaStreamSynchronize(stream);
+    cudaDestroyTextureObject(tex);
+    return e != cudaSuccess ? e : es;
+}
+
 // Paths 8-10: the gather with the matrix stream (columns and values).  Each
 // warp takes chunks of 256 nonzeros; the checksum adds the gathered x and
 // the values' bit patterns.  Full chunks go through the path's staging; the
@@ -499,6 +572,7 @@ spmv_status_t gather_typed(int path, int32_t nnz, const int32_t *col, int32_t n,
     case 17: e = launch_stream_gather<V, 17>(p, stream); break;
     case 18: e = launch_stream_gather<V, 18>(p, stream); break;
     case 19: e = launch_stream_gather<V, 19>(p, stream); break;
+    case 20: e = launch_tex_gather<V>(p, stream); break;
     default: return SPMV_ERR_INVALID_ARG;
     }
     return e == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
@@ -512,7 +586,7 @@ using namespace lbcsr;
 extern "C" spmv_status_t spmv_gather_ceiling(int32_t path, int32_t nnz, const int32_t *col_idx, int32_t n,
                                              const void *x, const void *vals, spmv_dtype_t dtype,
                                              uint64_t *checksum, int32_t *error, spmv_stream_t stream) {
-    if (path < 0 || path > 19 || nnz < 0 || n < 0) return SPMV_ERR_INVALID_ARG;
+    if (path < 0 || path > 20 || nnz < 0 || n < 0) return SPMV_ERR_INVALID_ARG;
     if (dtype != SPMV_F32 && dtype != SPMV_F64) return SPMV_ERR_INVALID_ARG;
     if (nnz == 0) return SPMV_OK;
     if (!col_idx || !checksum || !error || (path > 0 && (!x || n < 1)) || (path >= 8 && !vals))
