@@ -52,6 +52,8 @@
 #include <climits>
 #include <cstdlib>
 
+#include <atomic>
+
 #include "internal.cuh"
 #include "tma.cuh"
 
@@ -581,7 +583,9 @@ merge_path_spmv_kernel(const MPParams<V> p) {
     }
 }
 
-int g_ctas_per_sm[2][33][2][64];  // occupancy per (type, IPL, VEC, device)
+// occupancy per (type, IPL, VEC, device); 0 until first computed.  Host
+// threads may fill an entry at the same time: they compute the same value.
+std::atomic<int> g_ctas_per_sm[2][33][2][64];
 
 // Tuning override of the CTAs per SM (SPMV_MP_CTAS_PER_SM, 0 = as many as
 // fit), read once.
@@ -600,7 +604,8 @@ cudaError_t ctas_per_sm(int &out) {
     constexpr size_t smem = (size_t)kWarps * warp_region_bytes<V, IPL>();
     int dev = 0;
     cudaGetDevice(&dev);
-    int &per_sm = g_ctas_per_sm[sizeof(V) == 8][IPL][VEC][dev & 63];
+    std::atomic<int> &cached = g_ctas_per_sm[sizeof(V) == 8][IPL][VEC][dev & 63];
+    int per_sm = cached.load(std::memory_order_acquire);
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(merge_path_spmv_kernel<V, IPL, VEC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -619,6 +624,7 @@ cudaError_t ctas_per_sm(int &out) {
             if (e != cudaSuccess) return e;
         }
         per_sm = want;
+        cached.store(want, std::memory_order_release);
     }
     out = per_sm;
     return cudaSuccess;

@@ -24,6 +24,8 @@
 //
 // Each thread keeps U partial sums (level k goes to sum k mod U) and adds
 // them as a tree, so the rounding error grows with length / U.
+#include <atomic>
+
 #include "internal.cuh"
 #include "tma.cuh"
 
@@ -373,7 +375,9 @@ rgcsr_warp_kernel(const RgParams<V> p) {
     }
 }
 
-int g_rg_warp_ctas_per_sm[2][64];  // occupancy of the warp kernel per (type, device)
+// Per-device launch settings, 0 (false) until first computed.  Host threads
+// may fill an entry at the same time: they compute the same value.
+std::atomic<int> g_rg_warp_ctas_per_sm[2][64];  // occupancy of the warp kernel per (type, device)
 
 template <typename V>
 cudaError_t launch_rg_warp(RgParams<V> p, cudaStream_t stream) {
@@ -382,7 +386,8 @@ cudaError_t launch_rg_warp(RgParams<V> p, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int &per_sm = g_rg_warp_ctas_per_sm[sizeof(V) == 8][dev & 63];
+    std::atomic<int> &cached = g_rg_warp_ctas_per_sm[sizeof(V) == 8][dev & 63];
+    int per_sm = cached.load(std::memory_order_acquire);
     if (per_sm == 0) {
         e = cudaFuncSetAttribute(rgcsr_warp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -390,6 +395,7 @@ cudaError_t launch_rg_warp(RgParams<V> p, cudaStream_t stream) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, rgcsr_warp_kernel<V>, kWarpThreads, smem);
         if (e != cudaSuccess) return e;
         per_sm = nb > 0 ? nb : 1;
+        cached.store(per_sm, std::memory_order_release);
     }
     const long long max_warps = (long long)per_sm * device_sm_count() * (kWarpThreads / 32);
     p.num_warps = p.ngroups < max_warps ? p.ngroups : max_warps;
@@ -399,8 +405,8 @@ cudaError_t launch_rg_warp(RgParams<V> p, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------- G > 32: one CTA per group
-int g_rg_ctas_per_sm[2][9][64];  // occupancy per (type, log2 G, device)
-bool g_rg_smem_set[2][64];         // kernel's shared-memory limit raised (per type, device)
+std::atomic<int> g_rg_ctas_per_sm[2][9][64];  // occupancy per (type, log2 G, device)
+std::atomic<bool> g_rg_smem_set[2][64];         // kernel's shared-memory limit raised (per type, device)
 
 template <typename V>
 size_t rg_smem(int G) {
@@ -435,20 +441,22 @@ cudaError_t launch_rg(int32_t m, int32_t n, int g_log2, const int64_t *group_ptr
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (!g_rg_smem_set[sizeof(V) == 8][dev & 63]) {
+    if (!g_rg_smem_set[sizeof(V) == 8][dev & 63].load(std::memory_order_acquire)) {
         // one limit for every group size: the largest they need
         size_t most = 0;
         for (int gl = 5; gl <= 8; ++gl) most = rg_smem<V>(1 << gl) > most ? rg_smem<V>(1 << gl) : most;
         e = cudaFuncSetAttribute(rgcsr_tma_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
         if (e != cudaSuccess) return e;
-        g_rg_smem_set[sizeof(V) == 8][dev & 63] = true;
+        g_rg_smem_set[sizeof(V) == 8][dev & 63].store(true, std::memory_order_release);
     }
-    int &per_sm = g_rg_ctas_per_sm[sizeof(V) == 8][g_log2][dev & 63];
+    std::atomic<int> &cached_g = g_rg_ctas_per_sm[sizeof(V) == 8][g_log2][dev & 63];
+    int per_sm = cached_g.load(std::memory_order_acquire);
     if (per_sm == 0) {
         int nb = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, rgcsr_tma_kernel<V>, G, smem);
         if (e != cudaSuccess) return e;
         per_sm = nb > 0 ? nb : 1;
+        cached_g.store(per_sm, std::memory_order_release);
     }
     const long long cap = (long long)per_sm * device_sm_count();
     const unsigned grid = (unsigned)(p.ngroups < cap ? p.ngroups : cap);
